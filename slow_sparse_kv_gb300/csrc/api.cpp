@@ -1,0 +1,312 @@
+// C ABI of libsfi: host-side validation, workspace planning and kernel
+// dispatch for the slow step, the selector and the fast step.  Every check
+// happens before anything is enqueued; errors carry a thread-local message.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "sfi_internal.h"
+
+namespace sfi {
+
+cudaError_t launch_attn_f32(const AttnArgs& a, int D, int G, cudaStream_t st);
+cudaError_t launch_attn_bf16(const AttnArgs& a, int D, int G, cudaStream_t st);
+int attn_stage_rows_f32(int D);
+int attn_stage_rows_bf16(int D);
+
+namespace {
+thread_local std::string g_err;
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+}  // namespace
+
+sfi_status fail(sfi_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+sfi_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SFI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+WsPlan plan_workspace(int B, int H_q, int H_kv, int D, int max_len) {
+  (void)D;
+  const int G = H_q / H_kv;
+  const size_t units = size_t(B) * H_kv;
+  WsPlan p{};
+  p.max_items = int(units) * kItemSlotsPerUnit;
+  size_t off = 0;
+  p.status_off = off;
+  off += 256;
+  p.counters_off = off;
+  off += align256(units * 4);
+  p.partials_off = off;
+  off += align256(size_t(p.max_items) * G * (D + 2) * 4);
+  p.logits_off = off;
+  off += align256(units * size_t(max_len) * G * 4);
+  p.stats_off = off;
+  off += align256(size_t(B) * H_q * 2 * 4);
+  p.s_off = off;
+  off += align256(units * size_t(max_len) * 4);
+  p.total = off;
+  return p;
+}
+
+sfi_status check_layout(const sfi_layout* L) {
+  if (!L) return fail(SFI_ERR_INVALID_ARG, "layout is NULL");
+  if (L->batch < 1) return fail(SFI_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", L->batch);
+  if (L->batch > kMaxBatch)
+    return fail(SFI_ERR_CAPACITY, "batch %d exceeds the limit %d", L->batch, kMaxBatch);
+  if (L->n_kv_heads < 1 || L->n_q_heads < 1 || L->n_q_heads % L->n_kv_heads != 0)
+    return fail(SFI_ERR_INVALID_ARG, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
+                L->n_q_heads, L->n_kv_heads);
+  const int G = L->n_q_heads / L->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(SFI_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", G);
+  if (L->head_dim != 64 && L->head_dim != 128)
+    return fail(SFI_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", L->head_dim);
+  if (L->dtype != SFI_F32 && L->dtype != SFI_BF16)
+    return fail(SFI_ERR_UNSUPPORTED, "dtype must be SFI_F32 or SFI_BF16 (got %d)", L->dtype);
+  if (L->max_len < 1) return fail(SFI_ERR_INVALID_ARG, "max_len must be >= 1 (got %d)", L->max_len);
+  if (size_t(L->batch) * L->n_kv_heads > size_t(kMaxUnits))
+    return fail(SFI_ERR_CAPACITY, "batch * n_kv_heads = %d exceeds the limit %d",
+                L->batch * L->n_kv_heads, kMaxUnits);
+  if (!L->kv_offset || !L->kv_cap || !L->len)
+    return fail(SFI_ERR_INVALID_ARG, "layout kv_offset, kv_cap and len must be device pointers");
+  return SFI_OK;
+}
+
+sfi_status check_params(const sfi_params* P, bool for_select) {
+  if (!P) return fail(SFI_ERR_INVALID_ARG, "params is NULL");
+  if (P->k < 1) return fail(SFI_ERR_INVALID_ARG, "k must be >= 1 (got %d)", P->k);
+  if (P->n_sink < 0 || P->window < 0)
+    return fail(SFI_ERR_INVALID_ARG, "n_sink and window must be >= 0 (got %d, %d)", P->n_sink,
+                P->window);
+  if (!(P->lambda >= 0.f && P->lambda <= 1.f))
+    return fail(SFI_ERR_INVALID_ARG, "lambda must lie in [0, 1] (got %g)", double(P->lambda));
+  if (P->mode != SFI_SELECT_FUSED && P->mode != SFI_SELECT_LOGIT_SUM_SEQ)
+    return fail(SFI_ERR_INVALID_ARG, "unknown selection mode %d", P->mode);
+  if (for_select && P->mode == SFI_SELECT_LOGIT_SUM_SEQ && (P->lambda != 0.f || P->n_sink != 0))
+    return fail(SFI_ERR_INVALID_ARG, "logit-sum selection takes lambda = 0 and n_sink = 0");
+  if (!for_select && P->n_sink + (long long)P->window < 1)
+    return fail(SFI_ERR_INVALID_ARG,
+                "n_sink + window must be >= 1 so every fast step attends to at least one row");
+  return SFI_OK;
+}
+
+sfi_status check_ws(const sfi_layout* L, void* ws, size_t ws_bytes) {
+  const WsPlan p = plan_workspace(L->batch, L->n_q_heads, L->n_kv_heads, L->head_dim, L->max_len);
+  if (!ws) return fail(SFI_ERR_WORKSPACE, "workspace is NULL");
+  if (ws_bytes < p.total)
+    return fail(SFI_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu required",
+                ws_bytes, p.total);
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+    return fail(SFI_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  return SFI_OK;
+}
+
+int stage_rows(int dtype, int D) {
+  return dtype == SFI_F32 ? attn_stage_rows_f32(D) : attn_stage_rows_bf16(D);
+}
+
+int choose_rows_per_item(long long total_rows, int max_unit_rows, int sr, int grid) {
+  long long min_rpi = ceil_div(ceil_div(max_unit_rows, kItemSlotsPerUnit), sr) * sr;
+  if (min_rpi < sr) min_rpi = sr;
+  // items of at most ~4096 rows, as a whole number of waves over the grid
+  long long waves = ceil_div(total_rows, (long long)grid * 4096);
+  if (waves < 1) waves = 1;
+  long long rpi = ceil_div(ceil_div(total_rows, grid * waves), sr) * sr;
+  if (rpi < min_rpi) rpi = min_rpi;
+  return int(rpi);
+}
+
+void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const void* k,
+                      const void* v, float* out, char* ws, const WsPlan& p) {
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.kv_offset = L->kv_offset;
+  a.kv_cap = L->kv_cap;
+  a.len = L->len;
+  a.out = out;
+  a.B = L->batch;
+  a.H_q = L->n_q_heads;
+  a.H_kv = L->n_kv_heads;
+  a.max_len = L->max_len;
+  a.max_items = p.max_items;
+  a.qscale = float(1.4426950408889634 / std::sqrt(double(L->head_dim)));
+  a.partials = reinterpret_cast<float*>(ws + p.partials_off);
+  a.counters = reinterpret_cast<int32_t*>(ws + p.counters_off);
+  a.status = reinterpret_cast<uint32_t*>(ws + p.status_off);
+  a.logits = reinterpret_cast<float*>(ws + p.logits_off);
+  a.stats = reinterpret_cast<float*>(ws + p.stats_off);
+}
+
+sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long total_rows, int max_unit_rows,
+                    cudaStream_t st) {
+  const int G = L->n_q_heads / L->n_kv_heads;
+  a.rows_per_item =
+      choose_rows_per_item(total_rows, max_unit_rows, stage_rows(L->dtype, L->head_dim),
+                           device_sm_count());
+  const cudaError_t e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st)
+                                            : launch_attn_bf16(a, L->head_dim, G, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return SFI_OK;
+}
+
+int fast_unit_rows_bound(const sfi_layout* L, const sfi_params* P) {
+  long long r = (long long)P->n_sink + P->k + P->window;
+  return int(r < L->max_len ? r : L->max_len);
+}
+
+}  // namespace sfi
+
+using namespace sfi;
+
+extern "C" {
+
+const char* sfi_last_error(void) { return sfi::g_err.c_str(); }
+
+int32_t sfi_device_sm_count(void) { return device_sm_count(); }
+
+sfi_status sfi_read_status(void* ws, uint32_t* status_host, sfi_stream stream) {
+  if (!ws || !status_host) return fail(SFI_ERR_INVALID_ARG, "workspace and status_host must be set");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(status_host, ws, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+  return SFI_OK;
+}
+
+size_t sfi_slow_attn_workspace_size(const sfi_layout* L) {
+  if (check_layout(L) != SFI_OK) return 0;
+  return plan_workspace(L->batch, L->n_q_heads, L->n_kv_heads, L->head_dim, L->max_len).total;
+}
+
+size_t sfi_select_workspace_size(const sfi_layout* L, const sfi_params* P) {
+  (void)P;
+  return sfi_slow_attn_workspace_size(L);
+}
+
+size_t sfi_fast_attn_workspace_size(const sfi_layout* L, const sfi_params* P) {
+  (void)P;
+  return sfi_slow_attn_workspace_size(L);
+}
+
+sfi_status sfi_slow_attn(const sfi_layout* L, const void* q, const void* k, const void* v,
+                         float* out, float* f_out, float* knorm_out, void* ws, size_t ws_bytes,
+                         sfi_stream stream) {
+  sfi_status s = check_layout(L);
+  if (s != SFI_OK) return s;
+  if (!q || !k || !v || !out) return fail(SFI_ERR_INVALID_ARG, "q, k, v and out must be set");
+  if ((s = check_ws(L, ws, ws_bytes)) != SFI_OK) return s;
+  const WsPlan p = plan_workspace(L->batch, L->n_q_heads, L->n_kv_heads, L->head_dim, L->max_len);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AttnArgs a;
+  fill_attn_common(a, L, q, k, v, out, static_cast<char*>(ws), p);
+  for (int b = 0; b < L->batch; ++b) a.slow.bits[b >> 5] |= 1u << (b & 31);
+  a.emit = (f_out || knorm_out) ? 1 : 0;
+  a.knorm = knorm_out;
+  const long long total = (long long)L->batch * L->n_kv_heads * L->max_len;
+  if ((s = run_attn(a, L, total, L->max_len, st)) != SFI_OK) return s;
+  if (f_out) {
+    FpassArgs fa{};
+    fa.logits = a.logits;
+    fa.stats = a.stats;
+    fa.len = L->len;
+    fa.f = f_out;
+    fa.B = L->batch;
+    fa.H_q = L->n_q_heads;
+    fa.H_kv = L->n_kv_heads;
+    fa.max_len = L->max_len;
+    fa.slow = a.slow;
+    fa.status = a.status;
+    const cudaError_t e = launch_fpass(fa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "evidence pass launch");
+  }
+  return SFI_OK;
+}
+
+sfi_status sfi_select(const sfi_layout* L, const sfi_params* P, const float* evidence,
+                      const float* knorm, int32_t* idx_out, int32_t* count_out, float* s_out,
+                      void* ws, size_t ws_bytes, sfi_stream stream) {
+  sfi_status s = check_layout(L);
+  if (s != SFI_OK) return s;
+  if ((s = check_params(P, true)) != SFI_OK) return s;
+  if (!evidence || !idx_out || !count_out)
+    return fail(SFI_ERR_INVALID_ARG, "evidence, idx_out and count_out must be set");
+  if (P->mode == SFI_SELECT_FUSED && !knorm)
+    return fail(SFI_ERR_INVALID_ARG, "fused selection needs the key norms");
+  if ((s = check_ws(L, ws, ws_bytes)) != SFI_OK) return s;
+  const WsPlan p = plan_workspace(L->batch, L->n_q_heads, L->n_kv_heads, L->head_dim, L->max_len);
+  char* w = static_cast<char*>(ws);
+  SelectArgs a{};
+  a.evidence = evidence;
+  a.knorm = knorm;
+  a.len = L->len;
+  a.idx = idx_out;
+  a.count = count_out;
+  a.s = s_out ? s_out : reinterpret_cast<float*>(w + p.s_off);
+  a.B = L->batch;
+  a.H_kv = L->n_kv_heads;
+  a.max_len = L->max_len;
+  a.n_sink = P->n_sink;
+  a.window = P->window;
+  a.k = P->k;
+  a.lambda = P->lambda;
+  a.mode = P->mode;
+  for (int b = 0; b < L->batch; ++b) a.active.bits[b >> 5] |= 1u << (b & 31);
+  a.status = reinterpret_cast<uint32_t*>(w + p.status_off);
+  const cudaError_t e = launch_select(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "selector launch");
+  return SFI_OK;
+}
+
+sfi_status sfi_fast_attn(const sfi_layout* L, const sfi_params* P, const void* q, const void* k,
+                         const void* v, const int32_t* idx, const int32_t* count, float* out,
+                         void* ws, size_t ws_bytes, sfi_stream stream) {
+  sfi_status s = check_layout(L);
+  if (s != SFI_OK) return s;
+  if ((s = check_params(P, false)) != SFI_OK) return s;
+  if (!q || !k || !v || !out || !idx || !count)
+    return fail(SFI_ERR_INVALID_ARG, "q, k, v, idx, count and out must be set");
+  if ((s = check_ws(L, ws, ws_bytes)) != SFI_OK) return s;
+  const WsPlan p = plan_workspace(L->batch, L->n_q_heads, L->n_kv_heads, L->head_dim, L->max_len);
+  AttnArgs a;
+  fill_attn_common(a, L, q, k, v, out, static_cast<char*>(ws), p);
+  a.idx = idx;
+  a.count = count;
+  a.idx_stride = P->k;
+  a.n_sink = P->n_sink;
+  a.window = P->window;
+  const int bound = fast_unit_rows_bound(L, P);
+  const long long total = (long long)L->batch * L->n_kv_heads * bound;
+  return run_attn(a, L, total, bound, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

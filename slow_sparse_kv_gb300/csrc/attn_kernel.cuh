@@ -1,0 +1,499 @@
+// Split-K decode attention over the KV cache for slow and fast steps.
+//
+// SFI (gist.science 2603.12038, "Slow-Fast paradigm"): a slow step attends
+// densely to the whole history and its logits become the evidence; a fast
+// step attends only to the managed sparse state (sink tokens, the selected
+// memory, the recent window).  Both are the same computation over a list of
+// cache rows per (sequence, KV head) unit -- the list is [0, n) for a slow
+// unit and [sinks | selected | window] for a fast one -- so one persistent
+// kernel serves a mixed batch.
+//
+// Design (GB300, HBM-bound matrix-vector work, G = H_q / H_kv query heads per
+// KV head, so no tensor-core contraction):
+//  * the rows of each unit are cut into equal work items; CTAs (one per SM)
+//    walk the items round-robin;
+//  * one producer warp streams K and V rows into a ring of shared-memory
+//    stages with bulk asynchronous copies (cp.async.bulk, completion on
+//    mbarriers): one copy per contiguous stage for dense rows, one 16-byte-
+//    aligned row copy per gathered row for the managed state;
+//  * eight consumer warps each take a slice of every stage: lanes are grouped
+//    LPR = row_bytes / 16 per row, each lane owns 16 bytes of the row, keeps
+//    its slice of the G query vectors in registers, and the per-row dot
+//    products are finished with a transpose-reduce across the group;
+//  * online softmax in the log2 domain (q is pre-scaled by log2(e)/sqrt(d)),
+//    fp32 accumulation of p.v per lane;
+//  * slow units also write their logits ([pos][G], contiguous per warp) and
+//    the key norms, which the evidence pass and the selector read back;
+//  * the consumer warps merge their states per item; a unit cut into several
+//    items writes per-item partials and the last CTA to finish a unit (an
+//    atomic counter per unit, reset after use) merges them into the output.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+
+namespace sfi {
+
+template <typename T, int D, int G>
+struct AttnCfg {
+  static constexpr int ES = sizeof(T);
+  static constexpr int ROWB = D * ES;       // bytes per cache row
+  static constexpr int LPR = ROWB / 16;     // lanes per row
+  static constexpr int EPL = 16 / ES;       // elements per lane
+  static constexpr int RPI = 32 / LPR;      // rows per warp-wide 16-byte load
+  static constexpr int R = 4;               // rows per lane group per stage
+  static constexpr int RB = RPI * R;        // rows per warp per stage
+  static constexpr int NCW = 8;             // consumer warps
+  static constexpr int SR = RB * NCW;       // rows per stage
+  static constexpr int NS = 4;              // pipeline depth
+  static constexpr int NT = (NCW + 1) * 32;
+  static constexpr int STAGE_B = SR * ROWB;  // bytes of K (or V) per stage
+  static constexpr int NE = (RB * G + 31) / 32;
+  static constexpr int V = G * R;
+  static constexpr int NV = V >= LPR ? V / LPR : 1;
+  static_assert(LPR >= 8 && LPR <= 32, "row must be 128..512 bytes");
+  static_assert(R < LPR, "norm reduction assumes one value per lane");
+  static constexpr size_t OFF_K = 0;
+  static constexpr size_t OFF_V = OFF_K + size_t(NS) * STAGE_B;
+  static constexpr size_t OFF_BAR = OFF_V + size_t(NS) * STAGE_B;
+  static constexpr size_t OFF_SL = OFF_BAR + 2 * NS * 8;
+  static constexpr size_t OFF_SN = OFF_SL + size_t(NCW) * RB * G * 4;
+  static constexpr size_t OFF_RED = OFF_SN + size_t(NCW) * RB * 4;
+  static constexpr size_t OFF_MISC = OFF_RED + size_t(NCW) * G * (D + 2) * 4;
+  static constexpr size_t OFF_UNITS = OFF_MISC + 64;
+  static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1) * 4; }
+};
+
+struct ItemInfo {
+  int u, b, g, r0, r1, n, first, n_items;
+  bool slow;
+};
+
+// Rows of unit u in this launch (0 for an invalid length).
+__device__ __forceinline__ int attn_unit_rows(const AttnArgs& a, int u, bool report) {
+  const int b = u / a.H_kv;
+  const int n = a.len[b];
+  if (n < 1 || n > a.kv_cap[b] || n > a.max_len) {
+    if (report) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
+    return 0;
+  }
+  if (seq_is_slow(a.slow, b)) return n;
+  const int ns = min(a.n_sink, n);
+  const int cnt = min(max(a.count[u], 0), a.idx_stride);
+  const int wlo = max(a.n_sink, n - a.window);
+  return ns + cnt + max(n - wlo, 0);
+}
+
+template <int NT>
+__device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int* scratch) {
+  // units[u] = first item of unit u, units[n_units] = total items.
+  const int t = threadIdx.x;
+  const int per = (n_units + NT - 1) / NT;
+  const int u0 = min(t * per, n_units), u1 = min(u0 + per, n_units);
+  int local = 0;
+  for (int u = u0; u < u1; ++u) {
+    const int rows = attn_unit_rows(a, u, blockIdx.x == 0);
+    const int it = (rows + a.rows_per_item - 1) / a.rows_per_item;
+    units[u] = it;
+    local += it;
+  }
+  // block exclusive scan of `local`
+  const int lane = t & 31, w = t >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[w] = incl;
+  __syncthreads();
+  if (t == 0) {
+    int s = 0;
+    for (int i = 0; i < NT / 32; ++i) {
+      const int x = scratch[i];
+      scratch[i] = s;
+      s += x;
+    }
+    scratch[NT / 32] = s;
+  }
+  __syncthreads();
+  int run = scratch[w] + incl - local;
+  for (int u = u0; u < u1; ++u) {
+    const int it = units[u];
+    units[u] = run;
+    run += it;
+  }
+  if (t == 0) units[n_units] = scratch[NT / 32];
+  __syncthreads();
+}
+
+__device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* units, int n_units,
+                                                 int it) {
+  // largest u with units[u] <= it
+  int lo = 0, hi = n_units - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (units[mid] <= it) lo = mid;
+    else hi = mid - 1;
+  }
+  ItemInfo I;
+  I.u = lo;
+  I.b = lo / a.H_kv;
+  I.g = lo % a.H_kv;
+  I.first = units[lo];
+  I.n_items = units[lo + 1] - units[lo];
+  const int rows = attn_unit_rows(a, lo, false);
+  I.r0 = (it - I.first) * a.rows_per_item;
+  I.r1 = min(rows, I.r0 + a.rows_per_item);
+  I.n = a.len[I.b];
+  I.slow = seq_is_slow(a.slow, I.b);
+  return I;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const AttnArgs a) {
+  using C = AttnCfg<T, D, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_units = a.B * a.H_kv;
+  int* units = reinterpret_cast<int*>(smem + C::OFF_UNITS);
+  int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
+  const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
+  const uint32_t bar_empty = bar_full + C::NS * 8;
+
+  attn_build_units<C::NT>(a, units, n_units, misc);
+  const int total = units[n_units];
+  if (total > a.max_items) {
+    if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
+    return;
+  }
+  if (blockIdx.x >= total) return;
+  volatile int* abort_flag = misc + 12;
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, C::NCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == C::NCW) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = l2_evict_first_policy();
+    const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
+    uint32_t stage = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      const ItemInfo I = attn_resolve(a, units, n_units, it);
+      const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
+      const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
+      const char* vb = reinterpret_cast<const char*>(a.v) + head0 * C::ES;
+      const int n = I.n;
+      const int ns = min(a.n_sink, n);
+      const int cnt = I.slow ? 0 : min(max(a.count[I.u], 0), a.idx_stride);
+      const int wlo = max(a.n_sink, n - a.window);
+      const int32_t* ix = I.slow ? nullptr : a.idx + size_t(I.u) * a.idx_stride;
+      for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
+        const int nr = min(C::SR, I.r1 - c0);
+        const int slot = stage % C::NS;
+        const uint32_t ph = (stage / C::NS) & 1u;
+        if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
+        __syncwarp();
+        const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
+        if (I.slow) {
+          if (lane == 0) {
+            bulk_g2s(kd, kb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
+            bulk_g2s(vd, vb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
+          }
+        } else {
+          for (int j = lane; j < nr; j += 32) {
+            const int lp = c0 + j;
+            int pos;
+            if (lp < ns) {
+              pos = lp;
+            } else if (lp < ns + cnt) {
+              pos = __ldg(ix + (lp - ns));
+              if (pos < 0 || pos >= n) {
+                set_status(a.status, SFI_DEV_BAD_INDEX);
+                pos = 0;
+              }
+            } else {
+              pos = wlo + (lp - ns - cnt);
+            }
+            bulk_g2s(kd + j * C::ROWB, kb + size_t(pos) * C::ROWB, C::ROWB, bar_full + 8 * slot, pol);
+            bulk_g2s(vd + j * C::ROWB, vb + size_t(pos) * C::ROWB, C::ROWB, bar_full + 8 * slot, pol);
+          }
+        }
+        ++stage;
+      }
+    }
+    // Let every copy that was issued land before the CTA can exit.
+    const uint32_t first = stage > uint32_t(C::NS) ? stage - C::NS : 0u;
+    for (uint32_t s = first; s < stage; ++s) mbar_wait(bar_full + 8 * (s % C::NS), (s / C::NS) & 1u);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int li = lane % C::LPR, lg = lane / C::LPR;
+  const int hl = lane % G;  // head of this lane's softmax entries
+  float* sl = reinterpret_cast<float*>(smem + C::OFF_SL) + warp * C::RB * G;
+  float* sn = reinterpret_cast<float*>(smem + C::OFF_SN) + warp * C::RB;
+  float* red_all = reinterpret_cast<float*>(smem + C::OFF_RED);
+  const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
+  const int nct = C::NCW * 32;
+  uint32_t stage = 0;
+
+  for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    const ItemInfo I = attn_resolve(a, units, n_units, it);
+    const bool emit = a.emit && I.slow;
+    const bool emit_norm = emit && a.knorm != nullptr;
+
+    float qf[G][C::EPL];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      const char* qp = reinterpret_cast<const char*>(a.q) +
+                       (size_t(I.b) * a.H_q + size_t(I.g) * G + hh) * C::ROWB + li * 16;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qp));
+      float t[C::EPL];
+      Unpack<T>::run(raw, t);
+#pragma unroll
+      for (int e = 0; e < C::EPL; ++e) qf[hh][e] = t[e] * a.qscale;
+    }
+    float m[G], acc[G][C::EPL];
+    float zl = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      m[hh] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < C::EPL; ++e) acc[hh][e] = 0.f;
+    }
+
+    for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
+      const int nr = min(C::SR, I.r1 - c0);
+      const int slot = stage % C::NS;
+      const uint32_t ph = (stage / C::NS) & 1u;
+      // On a failed wait the warp skips the stage but keeps walking the
+      // schedule, so every consumer warp reaches every named barrier.
+      const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
+      const int wr0 = warp * C::RB;
+      if (have && wr0 < nr) {
+        const int nw = min(C::RB, nr - wr0);
+        const uint32_t krow = kbase + slot * C::STAGE_B + (wr0 + lg * C::R) * C::ROWB + li * 16;
+        float x[C::V];
+        float nn[C::R];
+#pragma unroll
+        for (int r = 0; r < C::R; ++r) {
+          const bool valid = lg * C::R + r < nw;
+          uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+          if (valid) raw = lds128(krow + r * C::ROWB);
+          float kf[C::EPL];
+          Unpack<T>::run(raw, kf);
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < C::EPL; ++e) s = fmaf(qf[hh][e], kf[e], s);
+            x[hh * C::R + r] = s;
+          }
+          float s2 = 0.f;
+#pragma unroll
+          for (int e = 0; e < C::EPL; ++e) s2 = fmaf(kf[e], kf[e], s2);
+          nn[r] = s2;
+        }
+        const int jb = transpose_reduce<C::LPR>(x, li);
+#pragma unroll
+        for (int i = 0; i < C::NV; ++i) {
+          const int j = jb + i;
+          const int hh = j / C::R, row = lg * C::R + (j % C::R);
+          sl[row * G + hh] = row < nw ? x[i] : -INFINITY;
+        }
+        if (emit_norm) {
+          const int jn = transpose_reduce<C::LPR>(nn, li);
+          const int row = lg * C::R + jn;
+          if (row < nw) sn[row] = sqrtf(nn[0]);
+        }
+        __syncwarp();
+        // ---- online softmax over this warp's rows
+        float lv[C::NE];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < C::NE; ++t) {
+          const int e = lane + 32 * t;
+          lv[t] = e < C::RB * G ? sl[e] : -INFINITY;
+          tmax = fmaxf(tmax, lv[t]);
+        }
+        if (emit) {
+          float* lg_out = a.logits + (size_t(I.u) * a.max_len + c0 + wr0) * G;
+#pragma unroll
+          for (int t = 0; t < C::NE; ++t) {
+            const int e = lane + 32 * t;
+            if (e < nw * G) lg_out[e] = lv[t];
+          }
+          if (emit_norm && lane < nw) a.knorm[size_t(I.u) * a.max_len + c0 + wr0 + lane] = sn[lane];
+        }
+#pragma unroll
+        for (int o = G; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+        bool changed = false;
+        float mn[G];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float t = __shfl_sync(kFull, tmax, hh);
+          mn[hh] = fmaxf(m[hh], t);
+          changed |= mn[hh] > m[hh];
+        }
+        if (changed) {
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            const float al = exp2f(m[hh] - mn[hh]);
+#pragma unroll
+            for (int e = 0; e < C::EPL; ++e) acc[hh][e] *= al;
+            if (hl == hh) zl *= al;
+            m[hh] = mn[hh];
+          }
+        }
+        float mine = m[0];
+#pragma unroll
+        for (int hh = 1; hh < G; ++hh)
+          if (hl == hh) mine = m[hh];
+#pragma unroll
+        for (int t = 0; t < C::NE; ++t) {
+          const int e = lane + 32 * t;
+          const float p = exp2f(lv[t] - mine);
+          zl += p;
+          if (e < C::RB * G) sl[e] = p;
+        }
+        __syncwarp();
+        // ---- p . v
+        const uint32_t vrow = vbase + slot * C::STAGE_B + (wr0 + lg * C::R) * C::ROWB + li * 16;
+#pragma unroll
+        for (int r = 0; r < C::R; ++r) {
+          const int row = lg * C::R + r;
+          if (row < nw) {
+            float pp[G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) pp[hh] = sl[row * G + hh];
+            const uint4 raw = lds128(vrow + r * C::ROWB);
+            float vf[C::EPL];
+            Unpack<T>::run(raw, vf);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+              for (int e = 0; e < C::EPL; ++e) acc[hh][e] = fmaf(pp[hh], vf[e], acc[hh][e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+      ++stage;
+    }
+
+    // ---- merge the lane groups of this warp
+#pragma unroll
+    for (int o = C::LPR; o < 32; o <<= 1)
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < C::EPL; ++e) acc[hh][e] += __shfl_xor_sync(kFull, acc[hh][e], o);
+#pragma unroll
+    for (int o = G; o < 32; o <<= 1) zl += __shfl_xor_sync(kFull, zl, o);
+    float* red = red_all + warp * G * (D + 2);
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      if (lane == hh) {
+        red[hh * (D + 2)] = m[hh];
+        red[hh * (D + 2) + 1] = zl;
+      }
+    }
+    if (lg == 0) {
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < C::EPL; ++e) red[hh * (D + 2) + 2 + li * C::EPL + e] = acc[hh][e];
+    }
+    named_bar_sync(1, nct);
+
+    // ---- merge the consumer warps: item result
+    float* part = a.partials + size_t(it) * G * (D + 2);
+    const bool single = I.n_items == 1;
+    for (int j = tid; j < G * D; j += nct) {
+      const int hh = j / D, dim = j % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, red_all[(w * G + hh) * (D + 2)]);
+      float A = 0.f, Z = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::NCW; ++w) {
+        const float* rw = red_all + (w * G + hh) * (D + 2);
+        const float sc = exp2f(rw[0] - M);
+        Z = fmaf(rw[1], sc, Z);
+        A = fmaf(rw[2 + dim], sc, A);
+      }
+      const size_t qh = size_t(I.b) * a.H_q + size_t(I.g) * G + hh;
+      if (single) {
+        a.out[qh * D + dim] = A / Z;
+        if (emit && dim == 0) {
+          a.stats[qh * 2] = M;
+          a.stats[qh * 2 + 1] = Z;
+        }
+      } else {
+        __stcg(part + hh * (D + 2) + 2 + dim, A);
+        if (dim == 0) {
+          __stcg(part + hh * (D + 2), M);
+          __stcg(part + hh * (D + 2) + 1, Z);
+        }
+      }
+    }
+    if (!single) {
+      __threadfence();
+      named_bar_sync(1, nct);
+      if (tid == 0) misc[13] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
+      named_bar_sync(1, nct);
+      if (misc[13]) {
+        __threadfence();
+        for (int j = tid; j < G * D; j += nct) {
+          const int hh = j / D, dim = j % D;
+          float M = -INFINITY, A = 0.f, Z = 0.f;
+          for (int i = 0; i < I.n_items; ++i) {
+            const float* p = a.partials + (size_t(I.first + i) * G + hh) * (D + 2);
+            const float pm = __ldcg(p), pz = __ldcg(p + 1), pa = __ldcg(p + 2 + dim);
+            const float M2 = fmaxf(M, pm);
+            const float s0 = exp2f(M - M2), s1 = exp2f(pm - M2);
+            A = A * s0 + pa * s1;
+            Z = Z * s0 + pz * s1;
+            M = M2;
+          }
+          const size_t qh = size_t(I.b) * a.H_q + size_t(I.g) * G + hh;
+          a.out[qh * D + dim] = A / Z;
+          if (emit && dim == 0) {
+            a.stats[qh * 2] = M;
+            a.stats[qh * 2 + 1] = Z;
+          }
+        }
+        if (tid == 0) a.counters[I.u] = 0;
+      }
+    }
+    named_bar_sync(1, nct);
+  }
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_attn_t(const AttnArgs& a, cudaStream_t st) {
+  using C = AttnCfg<T, D, G>;
+  const int n_units = a.B * a.H_kv;
+  const size_t smem = C::smem_bytes(n_units);
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<T, D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = device_sm_count();
+  attn_kernel<T, D, G><<<grid, C::NT, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace sfi

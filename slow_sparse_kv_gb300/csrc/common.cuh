@@ -1,0 +1,194 @@
+// Device helpers shared by the libsfi kernels: mbarrier pipeline primitives,
+// bulk asynchronous global->shared copies, bounded waits, bf16 unpacking and
+// warp reductions.  sm_103a only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sfi_internal.h"
+
+namespace sfi {
+
+constexpr unsigned kFull = 0xffffffffu;
+// A pipeline wait gives up after this many SM clocks (about 2 s) and reports
+// SFI_DEV_WAIT_TIMEOUT instead of spinning forever.
+constexpr long long kWaitCycles = 4000000000LL;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Wait for the phase of parity `parity` to complete; false after kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
+// Pipeline wait of a whole warp.  Gives up when the CTA's abort flag is set
+// or after kWaitCycles (then it sets the flag and the status bit).  The
+// result is the same in every lane: true only if every lane saw the phase
+// complete, so the warp never diverges around the data it guards.
+__device__ __forceinline__ bool warp_pipe_wait(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, uint32_t* status) {
+  bool ok = mbar_try_wait(bar, parity);
+  if (!ok) {
+    const long long t0 = clock64();
+    while (true) {
+      if (mbar_try_wait(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if (*abort_flag) break;
+      if (clock64() - t0 > kWaitCycles) {
+        *abort_flag = 1;
+        set_status(status, SFI_DEV_WAIT_TIMEOUT);
+        break;
+      }
+    }
+  }
+  return __all_sync(kFull, ok);
+}
+
+// Bulk asynchronous copy global -> shared of `bytes` (multiple of 16, both
+// addresses 16-byte aligned); completion is counted on mbarrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read once per launch (KV rows): evict first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// 16 bytes of storage -> fp32 elements.
+template <typename T>
+struct Unpack;
+
+template <>
+struct Unpack<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void run(const uint4& v, float (&o)[4]) {
+    o[0] = __uint_as_float(v.x);
+    o[1] = __uint_as_float(v.y);
+    o[2] = __uint_as_float(v.z);
+    o[3] = __uint_as_float(v.w);
+  }
+};
+
+struct bf16_t {
+  uint16_t bits;
+};
+
+template <>
+struct Unpack<bf16_t> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void run(const uint4& v, float (&o)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+
+__device__ __forceinline__ bool seq_is_slow(const SeqMask& m, int b) {
+  return (m.bits[b >> 5] >> (b & 31)) & 1u;
+}
+
+// Transpose-reduce across LPR lanes (LPR a power of two, lanes grouped by
+// lane / LPR): on entry each lane holds V partial values; on exit v[0..NV)
+// hold complete sums over the LPR lanes of the entries base .. base+NV-1,
+// where NV = max(1, V / LPR).  Each level halves the entries a lane keeps
+// and exchanges the other half with its partner, so V values are reduced
+// with about V shuffles per lane instead of V * log2(LPR).
+template <int C, int O>
+struct TransposeReduce {
+  template <int V>
+  static __device__ __forceinline__ void run(float (&v)[V], int li, int& base) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (C > 1) {
+      constexpr int H = C / 2;
+      const bool up = (li & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(kFull, send, O);
+      }
+      if (up) base += H;
+      TransposeReduce<H, O / 2>::run(v, li, base);
+    } else {
+      v[0] += __shfl_xor_sync(kFull, v[0], O);
+      TransposeReduce<1, O / 2>::run(v, li, base);
+    }
+  }
+};
+
+template <int LPR, int V>
+__device__ __forceinline__ int transpose_reduce(float (&v)[V], int li) {
+  int base = 0;
+  TransposeReduce<V, LPR / 2>::run(v, li, base);
+  return base;
+}
+
+}  // namespace sfi

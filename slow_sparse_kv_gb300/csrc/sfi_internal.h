@@ -1,0 +1,101 @@
+// Internal declarations of libsfi shared by the C-ABI layer (api.cpp,
+// decode.cpp) and the CUDA kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sfi.h"
+
+namespace sfi {
+
+constexpr int kMaxBatch = 1024;  // sequences per launch (bit mask capacity)
+constexpr int kMaxUnits = 4096;  // (sequence, KV head) pairs per launch
+constexpr int kItemSlotsPerUnit = 64;  // split-K partial slots per (sequence, KV head)
+
+// Bit b set: sequence b runs a slow (dense) step in this launch.
+struct SeqMask {
+  uint32_t bits[kMaxBatch / 32];
+};
+
+// Split-K attention over either the whole cache (slow sequences) or the
+// managed sparse state (fast sequences) of every (sequence, KV head) unit.
+struct AttnArgs {
+  const void* q;  // [B][H_q][D]
+  const void* k;
+  const void* v;
+  const int64_t* kv_offset;
+  const int32_t* kv_cap;
+  const int32_t* len;
+  float* out;     // [B][H_q][D]
+  float* logits;  // [B*H_kv][max_len][G], log2-scaled logits of slow units (emit)
+  float* knorm;   // [B*H_kv][max_len] key norms of slow units (nullable)
+  float* stats;   // [B*H_q][2]: (max log2-logit, sum of 2^(l - max)) of slow units
+  const int32_t* idx;    // [B*H_kv][idx_stride] selected positions (fast units)
+  const int32_t* count;  // [B*H_kv]
+  int32_t idx_stride;
+  int32_t n_sink;
+  int32_t window;
+  int32_t B, H_q, H_kv, max_len;
+  int32_t rows_per_item;
+  int32_t max_items;
+  int32_t emit;    // slow units write logits, stats (and knorm if non-null)
+  float qscale;    // log2(e) / sqrt(D)
+  SeqMask slow;
+  float* partials;     // [max_items][G][D + 2]
+  int32_t* counters;   // [B*H_kv], zero between launches
+  uint32_t* status;
+};
+
+struct FpassArgs {
+  const float* logits;
+  const float* stats;
+  const int32_t* len;
+  float* f;  // [B*H_kv][max_len]
+  int32_t B, H_q, H_kv, max_len;
+  SeqMask slow;
+  uint32_t* status;
+};
+
+struct SelectArgs {
+  const float* evidence;  // f (fused mode) or per-KV-head logit sums (logit-sum mode)
+  const float* knorm;
+  const int32_t* len;
+  int32_t* idx;    // [B*H_kv][k]
+  int32_t* count;  // [B*H_kv]
+  float* s;        // [B*H_kv][max_len] fused scores (s_out or workspace)
+  int32_t B, H_kv, max_len;
+  int32_t n_sink, window, k;
+  float lambda;
+  int32_t mode;
+  SeqMask active;
+  uint32_t* status;
+};
+
+// Workspace plan: one layout serves every call of a given geometry.
+struct WsPlan {
+  size_t status_off, counters_off, partials_off, logits_off, stats_off, s_off, total;
+  int32_t max_items;
+};
+
+WsPlan plan_workspace(int B, int H_q, int H_kv, int D, int max_len);
+
+// Kernel launchers (return the CUDA error of the launch).
+cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
+
+int device_sm_count();
+
+// Host helpers of the C-ABI layer (api.cpp), shared with the decode driver.
+sfi_status check_layout(const sfi_layout* L);
+sfi_status check_params(const sfi_params* P, bool for_select);
+void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const void* k,
+                      const void* v, float* out, char* ws, const WsPlan& p);
+sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long total_rows, int max_unit_rows,
+                    cudaStream_t st);
+int fast_unit_rows_bound(const sfi_layout* L, const sfi_params* P);
+sfi_status fail(sfi_status s, const char* fmt, ...);
+sfi_status cuda_fail(cudaError_t e, const char* what);
+
+}  // namespace sfi

@@ -1,0 +1,122 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/sfi.h declares, and rejects bad arguments on the host before any GPU
+work; the host-only schedule step matches the oracle's schedule."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle.sfi_oracle as O
+import sfi_workloads as W
+from tests.sfi_testlib import ROOT, load_sfi
+
+HEADER = os.path.join(ROOT, "include", "sfi.h")
+
+
+@pytest.fixture(scope="module")
+def sfi():
+    return load_sfi()
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(sfi_[a-z0-9_]+)\s*\(",
+                                 txt, flags=re.M)))
+
+
+def test_header_declares_the_path_entry_points():
+    names = declared_functions()
+    for n in ["sfi_slow_attn", "sfi_select", "sfi_fast_attn", "sfi_decode_step"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_function(sfi):
+    lib = ctypes.CDLL(sfi.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in sfi.h but not exported"
+        assert name in sfi.EXPORTS, f"{name} has no binding"
+    assert set(sfi.EXPORTS) == set(declared_functions())
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails host validation first
+
+
+def layout(sfi, **kw):
+    d = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=64, dtype=sfi.SFI_F32, max_len=100,
+             kv_offset=FAKE, kv_cap=FAKE, len=FAKE)
+    d.update(kw)
+    return sfi.sfi_layout(**d)
+
+
+def slow(sfi, L, ws=FAKE, ws_bytes=1 << 40, q=FAKE):
+    return sfi.lib.sfi_slow_attn(ctypes.byref(L), q, FAKE, FAKE, FAKE, None, None, ws, ws_bytes, None)
+
+
+def test_host_validation_codes(sfi):
+    assert sfi.lib.sfi_slow_attn(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 40, None) == sfi.SFI_ERR_INVALID_ARG
+    assert slow(sfi, layout(sfi, head_dim=96)) == sfi.SFI_ERR_UNSUPPORTED
+    assert slow(sfi, layout(sfi, dtype=7)) == sfi.SFI_ERR_UNSUPPORTED
+    assert slow(sfi, layout(sfi, n_q_heads=12, n_kv_heads=4)) == sfi.SFI_ERR_UNSUPPORTED  # G = 3
+    assert slow(sfi, layout(sfi, n_q_heads=7)) == sfi.SFI_ERR_INVALID_ARG
+    assert slow(sfi, layout(sfi, batch=0)) == sfi.SFI_ERR_INVALID_ARG
+    assert slow(sfi, layout(sfi, batch=5000)) == sfi.SFI_ERR_CAPACITY
+    assert slow(sfi, layout(sfi, batch=1000, n_q_heads=64, n_kv_heads=8)) == sfi.SFI_ERR_CAPACITY
+    assert slow(sfi, layout(sfi, max_len=0)) == sfi.SFI_ERR_INVALID_ARG
+    assert slow(sfi, layout(sfi, len=None)) == sfi.SFI_ERR_INVALID_ARG
+    assert slow(sfi, layout(sfi), q=None) == sfi.SFI_ERR_INVALID_ARG
+    assert slow(sfi, layout(sfi), ws=None) == sfi.SFI_ERR_WORKSPACE
+    assert slow(sfi, layout(sfi), ws_bytes=16) == sfi.SFI_ERR_WORKSPACE
+    assert slow(sfi, layout(sfi), ws=FAKE + 8) == sfi.SFI_ERR_WORKSPACE  # misaligned
+    assert "workspace" in sfi.lib.sfi_last_error().decode()
+
+
+def test_workspace_size_grows_with_geometry(sfi):
+    small = sfi.lib.sfi_slow_attn_workspace_size(ctypes.byref(layout(sfi)))
+    big = sfi.lib.sfi_slow_attn_workspace_size(ctypes.byref(layout(sfi, max_len=10000)))
+    assert 0 < small < big
+    assert sfi.lib.sfi_slow_attn_workspace_size(ctypes.byref(layout(sfi, head_dim=3))) == 0
+
+
+def test_select_and_fast_param_validation(sfi):
+    L = layout(sfi)
+    def sel(p, ev=FAKE, kn=FAKE):
+        return sfi.lib.sfi_select(ctypes.byref(L), ctypes.byref(p), ev, kn, FAKE, FAKE, None, FAKE, 1 << 40, None)
+    def fast(p):
+        return sfi.lib.sfi_fast_attn(ctypes.byref(L), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert sel(sfi.params(4, 16, 0, 0.3)) == sfi.SFI_ERR_INVALID_ARG        # k = 0
+    assert sel(sfi.params(-1, 16, 8, 0.3)) == sfi.SFI_ERR_INVALID_ARG
+    assert sel(sfi.params(4, 16, 8, 1.5)) == sfi.SFI_ERR_INVALID_ARG        # lambda outside [0, 1]
+    assert sel(sfi.params(4, 16, 8, float("nan"))) == sfi.SFI_ERR_INVALID_ARG
+    assert sel(sfi.params(4, 16, 8, 0.3, mode=9)) == sfi.SFI_ERR_INVALID_ARG
+    assert sel(sfi.params(4, 16, 8, 0.3, mode=sfi.SFI_SELECT_LOGIT_SUM_SEQ)) == sfi.SFI_ERR_INVALID_ARG
+    assert sel(sfi.params(4, 16, 8, 0.3), kn=None) == sfi.SFI_ERR_INVALID_ARG
+    assert sel(sfi.params(4, 16, 8, 0.3), ev=None) == sfi.SFI_ERR_INVALID_ARG
+    assert fast(sfi.params(0, 0, 8, 0.3)) == sfi.SFI_ERR_INVALID_ARG        # empty fast set
+    assert sfi.lib.sfi_fast_attn(ctypes.byref(L), ctypes.byref(sfi.params(4, 16, 8, 0.3)), FAKE, FAKE, FAKE,
+                                 None, FAKE, FAKE, FAKE, 1 << 40, None) == sfi.SFI_ERR_INVALID_ARG
+
+
+def test_ctx_and_decode_validation(sfi):
+    h = ctypes.c_void_p()
+    desc = sfi.sfi_ctx_desc(2, 8, 2, 64, sfi.SFI_F32, 100, 0, sfi.params(4, 16, 8, 0.3), 4)
+    assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == sfi.SFI_ERR_INVALID_ARG  # 0 layers
+    desc = sfi.sfi_ctx_desc(2, 8, 2, 64, sfi.SFI_F32, 100, 1, sfi.params(4, 16, 8, 0.3), -1)
+    assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == sfi.SFI_ERR_INVALID_ARG  # budget < 0
+    assert sfi.lib.sfi_decode_step(None, 0, None, None, FAKE, FAKE, FAKE, FAKE, None) == sfi.SFI_ERR_INVALID_ARG
+
+
+def test_schedule_matches_oracle(sfi):
+    for budget in [0, 1, 3, 32]:
+        tr = W.cfg2(n_steps=200).boundary_trace()
+        ref = O.schedule(tr, budget)
+        B = tr.shape[1]
+        have = np.zeros(B, np.uint8)
+        since = np.zeros(B, np.int32)
+        for t in range(tr.shape[0]):
+            got = sfi.sfi_schedule(tr[t], have, since, budget)
+            assert list(got) == list(ref[t].astype(np.uint8)), (budget, t)
+    with pytest.raises(sfi.SfiError):
+        sfi.sfi_schedule(np.zeros(2, np.uint8), np.zeros(2, np.uint8), np.zeros(2, np.int32), -1)
