@@ -1,0 +1,553 @@
+#!/usr/bin/env python
+"""Benchmark of the SFI decode-attention hot path on one or more GB300s.
+
+One bench step is a whole decode pass of the workload: by default the
+Llama-3-8B attention shape (32 query / 8 KV heads, d = 128, bf16 KV) at
+context 131072 with batch 8, 32 layers and 256 decode steps, with per-sequence
+boundaries drawn geometrically (mean 20 tokens) and a refresh budget of 32,
+k = 4096, window 256, 4 sinks, lambda 0.3.  Every decode step runs each layer
+through the library's decode driver (one mixed slow/fast attention launch per
+layer, plus the evidence and selector launches when a sequence refreshes).
+
+Printed (rank 0, one JSON line): decode steps/s of the whole job (device-timed
+with CUDA events, inputs resident in HBM, inputs far larger than L2), the
+end-to-end rate through the same API with queries copied in from pinned host
+memory and outputs copied back every decode step, the attention kernel's
+achieved HBM bandwidth against the measured peak, and the fp64 CPU oracle
+timed on the host's cores on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload cfg2|cfg1] [--layers L] [--decode-steps T]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import sfi_workloads as W  # noqa: E402
+
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers (no GPU)
+
+def measured_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank decodes its own independent batch (weak scaling)."""
+    return seed if rank == 0 else W.stream_key(seed, 1000 + rank) & 0x7FFFFFFF
+
+
+def aggregate_max(value: float, world: int) -> float:
+    """Max of a per-rank value over the job (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def schedule_counts(slow_masks: np.ndarray):
+    """(slow units, fast units) of a [T, B] slow mask."""
+    s = int(slow_masks.sum())
+    return s, int(slow_masks.size - s)
+
+
+def attention_bytes(wl: W.Workload, slow_masks: np.ndarray) -> float:
+    """Algorithmic bytes the attention launches read: the whole K and V of a slow
+    (sequence, layer) step, and the gathered sink + selected + window rows of a
+    fast one.  Summed over the decode pass."""
+    sh = wl.shape
+    row = 2 * sh.n_kv_heads * sh.head_dim * sh.esize  # K and V row of every KV head
+    total = 0.0
+    T, B = slow_masks.shape
+    last_slow_n = [None] * B
+    for t in range(T):
+        for b in range(B):
+            n = wl.n0[b] + t
+            if slow_masks[t, b]:
+                total += n * row
+                last_slow_n[b] = n
+            else:
+                e = max(0, last_slow_n[b] - wl.window - wl.n_sink)
+                keff = min(wl.k, e)
+                wnd = n - max(wl.n_sink, n - wl.window)
+                total += (min(wl.n_sink, n) + keff + wnd) * row
+    return total * wl.n_layers
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def _cpu_unit_worker(args):
+    """Time the fp64 oracle on one (sequence, layer, KV head) unit: slow steps
+    and fast steps at the workload's length, for about `budget_s` seconds."""
+    n, G, d, k, ns, win, lam, budget_s, seed = args
+    import time as _t
+    import numpy as _np
+    from oracle import sfi_oracle as O
+    rng = _np.random.default_rng(seed)
+    K = rng.standard_normal((1, n + 8, d)).astype(_np.float32).astype(_np.float64)
+    V = rng.standard_normal((1, n + 8, d)).astype(_np.float32).astype(_np.float64)
+    q = rng.standard_normal((G, d))
+    ts, tf = [], []
+    idx = None
+    t_end = _t.perf_counter() + budget_s
+    while not ts or (_t.perf_counter() < t_end and len(ts) < 50):
+        t0 = _t.perf_counter()
+        st = O.slow_step(q, K, V, n, ns, win, k, lam)
+        ts.append(_t.perf_counter() - t0)
+        idx = st["idx"]
+        for j in range(4):
+            t0 = _t.perf_counter()
+            O.fast_step(q, K, V, n + 1 + j, idx, ns, win)
+            tf.append(_t.perf_counter() - t0)
+    return float(_np.mean(ts)), float(_np.mean(tf)), len(ts), len(tf)
+
+
+def cpu_oracle_rate(wl: W.Workload, slow_frac: float, budget_s: float = 2.0, workers=None):
+    """Decode steps/s of the fp64 oracle on the host: every worker process is
+    single-threaded and times (sequence, layer, KV head) units; the job rate is
+    the pool's unit throughput divided by the units of one decode step."""
+    sh = wl.shape
+    P = workers or max(1, min(16, os.cpu_count() or 1))
+    n = wl.n0[0]
+    env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k_ in env_keep:
+        os.environ[k_] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(P) as pool:
+            args = [(n, sh.group, sh.head_dim, wl.k, wl.n_sink, wl.window, wl.lam, budget_s, 17 + i)
+                    for i in range(P)]
+            t0 = time.perf_counter()
+            res = pool.map(_cpu_unit_worker, args)
+            wall = time.perf_counter() - t0
+    finally:
+        for k_, v_ in env_keep.items():
+            if v_ is None:
+                os.environ.pop(k_, None)
+            else:
+                os.environ[k_] = v_
+    t_slow = float(np.mean([r[0] for r in res]))
+    t_fast = float(np.mean([r[1] for r in res]))
+    units_per_step = wl.n_layers * sh.batch * sh.n_kv_heads
+    t_step_one_core = units_per_step * (slow_frac * t_slow + (1 - slow_frac) * t_fast)
+    rate = P / t_step_one_core
+    sample = (f"{sum(r[2] for r in res)} slow + {sum(r[3] for r in res)} fast (sequence, layer, "
+              f"KV-head) unit steps at n={n}, G={sh.group}, d={sh.head_dim}, k={wl.k} "
+              f"(random bf16-valued inputs) on {P} single-threaded processes in {wall:.1f} s; "
+              f"scaled by {units_per_step} units per decode step and slow fraction {slow_frac:.4f}")
+    return rate, P, sample, t_slow, t_fast
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names[1:], p[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU leg
+
+class Cfg2Runner:
+    """Device-resident decode workload driven through sfi_decode_step."""
+
+    def __init__(self, wl: W.Workload, device: int):
+        import torch
+        import slow_sparse_kv_gb300 as sfi
+        self.torch, self.sfi, self.wl = torch, sfi, wl
+        sh = wl.shape
+        self.dev = torch.device("cuda", device)
+        torch.cuda.set_device(self.dev)
+        self.stream = torch.cuda.current_stream()
+        gen = ctypes.CDLL(os.path.join(ROOT, "sfi_workloads", "_lib", "libsfigen.so"))
+        gen.sfigen_fill.restype = ctypes.c_int
+        gen.sfigen_fill.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_int64,
+                                    ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p]
+        self.gen = gen
+        B, L, T = sh.batch, wl.n_layers, wl.n_steps
+        dt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
+        dcode = 1 if sh.dtype == "bf16" else 0
+        per_seq = sh.n_kv_heads * wl.cap[0] * sh.head_dim
+        self.offsets = [b * per_seq for b in range(B)]
+        st = self.stream.cuda_stream
+        self.K, self.V, self.Q = [], [], []
+        for l in range(L):
+            u = wl.u_vec(l)
+            u3 = torch.tensor(3.0 * u, dtype=torch.float64, device=self.dev)
+            u2 = torch.tensor(2.0 * u, dtype=torch.float64, device=self.dev)
+            kt = torch.empty(B * per_seq, dtype=dt, device=self.dev)
+            vt = torch.empty(B * per_seq, dtype=dt, device=self.dev)
+            for b in range(B):
+                mask = torch.from_numpy(wl.heavy_mask(l, b).astype(np.uint8)).to(self.dev)
+                cap = wl.cap[b]
+                r = gen.sfigen_fill(kt.data_ptr() + self.offsets[b] * kt.element_size(), dcode,
+                                    wl.key(W.T_K, l, b), 0, per_seq, sh.head_dim, cap,
+                                    mask.data_ptr(), u3.data_ptr(), st)
+                r |= gen.sfigen_fill(vt.data_ptr() + self.offsets[b] * vt.element_size(), dcode,
+                                     wl.key(W.T_V, l, b), 0, per_seq, sh.head_dim, cap, None, None, st)
+                assert r == 0, "generator launch failed"
+            qt = torch.empty(T, B, sh.n_q_heads, sh.head_dim, dtype=dt, device=self.dev)
+            nq = sh.n_q_heads * sh.head_dim
+            for t in range(T):
+                for b in range(B):
+                    r = gen.sfigen_fill(qt[t, b].data_ptr(), dcode, wl.key(W.T_Q, l, b, t, 0), 0, nq,
+                                        sh.head_dim, 1, None, u2.data_ptr(), st)
+                    assert r == 0
+            self.K.append(kt)
+            self.V.append(vt)
+            self.Q.append(qt)
+        torch.cuda.synchronize()
+        self.out = [torch.empty(B, sh.n_q_heads, sh.head_dim, device=self.dev) for _ in range(L)]
+        # per-decode-step layouts: lengths n0 + t
+        lens = torch.tensor([[n + t for n in wl.n0] for t in range(T)], dtype=torch.int32,
+                            device=self.dev)
+        self.lens = lens
+        self.offs_t = torch.tensor(self.offsets, dtype=torch.int64, device=self.dev)
+        self.caps_t = torch.tensor(wl.cap, dtype=torch.int32, device=self.dev)
+        self.max_len = max(wl.cap)
+        self.layouts = [sfi.sfi_layout(B, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dcode,
+                                       self.max_len, self.offs_t.data_ptr(), self.caps_t.data_ptr(),
+                                       lens[t].data_ptr()) for t in range(T)]
+        self.trace = wl.boundary_trace()
+        self.bnd = [(ctypes.c_uint8 * B)(*[int(x) for x in self.trace[t]]) for t in range(T)]
+        self.ctx = sfi.DecodeContext(B, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dt, self.max_len, L,
+                                     sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget)
+        self.slow_masks = None
+        self.kp = [t.data_ptr() for t in self.K]
+        self.vp = [t.data_ptr() for t in self.V]
+        self.op = [t.data_ptr() for t in self.out]
+
+    def decode_pass(self, q_ptrs=None, token_events=None, h2d=None, d2h=None):
+        """One whole decode pass.  q_ptrs[t][l] overrides the query pointers;
+        h2d(t) / d2h(t) enqueue the per-token host copies (end-to-end mode)."""
+        sfi, wl = self.sfi, self.wl
+        lib, h = sfi.lib, self.ctx.h
+        st = self.stream.cuda_stream
+        self.ctx.reset()
+        masks = []
+        L = wl.n_layers
+        for t in range(wl.n_steps):
+            if h2d is not None:
+                h2d(t)
+            if token_events is not None:
+                token_events[t][0].record(self.stream)
+            lay = ctypes.byref(self.layouts[t])
+            for l in range(L):
+                qp = self.Q[l][t].data_ptr() if q_ptrs is None else q_ptrs(t, l)
+                r = lib.sfi_decode_step(h, l, self.bnd[t], lay, qp, self.kp[l], self.vp[l], self.op[l], st)
+                if r != 0:
+                    raise sfi.SfiError("sfi_decode_step", r)
+            if token_events is not None:
+                token_events[t][1].record(self.stream)
+            if d2h is not None:
+                d2h(t)
+            if self.slow_masks is None:
+                masks.append(self.ctx.slow_mask())
+        if self.slow_masks is None:
+            self.slow_masks = np.array(masks, dtype=np.uint8)
+
+    def dense_pass(self, n_tokens: int, ws):
+        """Full-KV dense decode (every sequence, every layer) for n_tokens steps."""
+        sfi, wl = self.sfi, self.wl
+        st = self.stream.cuda_stream
+        for t in range(n_tokens):
+            lay = ctypes.byref(self.layouts[t])
+            for l in range(wl.n_layers):
+                r = sfi.lib.sfi_slow_attn(lay, self.Q[l][t].data_ptr(), self.kp[l], self.vp[l],
+                                          self.op[l], None, None, ws.data_ptr(), ws.numel(), st)
+                if r != 0:
+                    raise sfi.SfiError("sfi_slow_attn", r)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    wl = W.cfg2(n_layers=args.layers, n_steps=args.decode_steps) if args.workload == "cfg2" else W.cfg1()
+    if world > 1:
+        wl.seed = rank_seed(wl.seed, rank)
+    t_setup = time.perf_counter()
+    R = Cfg2Runner(wl, local_rank)
+    setup_s = time.perf_counter() - t_setup
+    sfi = R.sfi
+    sh = wl.shape
+    # warm-up passes (also fix the schedule's slow masks)
+    for _ in range(args.warmup):
+        R.decode_pass()
+    torch.cuda.synchronize()
+    slow_masks = R.slow_masks
+    n_slow_units, n_fast_units = schedule_counts(slow_masks)
+    slow_frac = n_slow_units / max(1, slow_masks.size)
+    alg_bytes = attention_bytes(wl, slow_masks)
+    T = wl.n_steps
+    # ---------------- timed region: K decode passes, inputs resident in HBM
+    ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(T)]
+    tok_ms_fast, tok_ms_mixed = [], []
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    R.ctx.profile(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(args.steps):
+        R.decode_pass(token_events=ev)
+        if s == args.steps - 1:
+            pass
+    e1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = e0.elapsed_time(e1)
+    attn_ms, attn_n, sel_ms, sel_n = R.ctx.profile_read()
+    R.ctx.profile(False)
+    for t in range(T):  # token times of the last pass
+        ms = ev[t][0].elapsed_time(ev[t][1])
+        (tok_ms_mixed if slow_masks[t].any() else tok_ms_fast).append(ms)
+    total_ms = aggregate_max(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    steps_per_s = world * T * args.steps / (total_ms / 1e3)
+    # ---------------- end to end: host queries in, host outputs back, every decode step
+    L, B = wl.n_layers, sh.batch
+    dt = R.Q[0].dtype
+    q_host = torch.empty(T, L, B, sh.n_q_heads, sh.head_dim, dtype=dt, pin_memory=True)
+    for l in range(L):
+        q_host[:, l].copy_(R.Q[l].cpu())
+    o_host = torch.empty(T, L, B, sh.n_q_heads, sh.head_dim, dtype=torch.float32, pin_memory=True)
+    q_stage = torch.empty(L, B, sh.n_q_heads, sh.head_dim, dtype=dt, device=R.dev)
+    out_all = torch.stack(R.out)  # [L, B, H_q, d] staging of the outputs
+    R.op = [out_all[l].data_ptr() for l in range(L)]
+    h2d_bytes = q_stage.numel() * q_stage.element_size()
+    d2h_bytes = out_all.numel() * 4
+
+    def h2d(t):
+        q_stage.copy_(q_host[t], non_blocking=True)
+
+    def d2h(t):
+        o_host[t].copy_(out_all, non_blocking=True)
+
+    qp = [q_stage[l].data_ptr() for l in range(L)]
+    e_steps = max(1, min(args.steps, 3))
+    R.decode_pass(q_ptrs=lambda t, l: qp[l], h2d=h2d, d2h=d2h)  # warm
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        R.decode_pass(q_ptrs=lambda t, l: qp[l], h2d=h2d, d2h=d2h)
+    torch.cuda.synchronize()
+    e2e_s = aggregate_max(time.perf_counter() - t0, world)
+    e2e_rate = world * T * e_steps / e2e_s
+    # ---------------- full-KV dense baseline (every step dense, no evidence)
+    lay0 = sfi.Layout(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dt, R.offsets, wl.cap, wl.n0, R.max_len,
+                      device=R.dev)
+    ws = sfi.alloc_workspace(lay0)
+    R.op = [t.data_ptr() for t in R.out]
+    n_dense = 4
+    R.dense_pass(1, ws)
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record()
+    R.dense_pass(n_dense, ws)
+    d1.record()
+    torch.cuda.synchronize()
+    dense_rate = world * n_dense / (aggregate_max(d0.elapsed_time(d1), world) / 1e3)
+    status = sfi.sfi_read_status(ws)
+    # ---------------- roofline of the attention kernel (all its launches in the timed region)
+    peak, peak_kind = measured_peak_gbs()
+    achieved = (alg_bytes * args.steps) / (attn_ms / 1e3) / 1e9
+    gpu_launches = int(attn_n + sel_n)
+    line = {
+        "metric": "SFI decode steps/s (slow & fast) and achieved HBM GB/s as % of GB300 peak",
+        "value": round(steps_per_s, 3),
+        "unit": "decode steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if sh.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) K/V with 1% heavy hitters, Q = N(0,1) + 2u)",
+        "config": {
+            "workload": wl.name,
+            "batch_per_gpu": sh.batch, "layers": wl.n_layers, "decode_steps_per_pass": T,
+            "context": wl.n0[0], "heads": f"{sh.n_q_heads}q/{sh.n_kv_heads}kv", "head_dim": sh.head_dim,
+            "k": wl.k, "window": wl.window, "n_sink": wl.n_sink, "lambda": wl.lam,
+            "refresh_budget": wl.budget, "boundary_rate": wl.boundary_rate,
+            "l2": "inputs larger than L2 (%.1f GB of KV per GPU)" % (
+                sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9),
+            "parallelism": f"dp{world} (independent sequences per GPU)",
+        },
+        "tokens_per_s": round(steps_per_s * sh.batch, 1),
+        "breakdown": {
+            "slow_unit_fraction": round(slow_frac, 4),
+            "fast_token_ms": round(statistics.mean(tok_ms_fast), 3) if tok_ms_fast else None,
+            "refresh_token_ms": round(statistics.mean(tok_ms_mixed), 3) if tok_ms_mixed else None,
+            "attention_ms_per_pass": round(attn_ms / args.steps, 3),
+            "evidence_select_ms_per_pass": round(sel_ms / args.steps, 3),
+            "dense_full_kv_steps_per_s": round(dense_rate, 3),
+            "speedup_vs_dense": round(steps_per_s / dense_rate, 2),
+            "setup_s": round(setup_s, 1),
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "kernel": "sfi attention (mixed slow/fast launch)",
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "algorithmic_bytes_per_pass": alg_bytes,
+        },
+        "e2e": {"value": round(e2e_rate, 3), "unit": "decode steps/s",
+                "h2d_bytes_per_step": int(h2d_bytes * T), "d2h_bytes_per_step": int(d2h_bytes * T)},
+        "gpu_launches": gpu_launches,
+        "device_status": status,
+    }
+    if clk:
+        line["clocks"] = clk
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, P, sample, ts, tf = cpu_oracle_rate(wl, slow_frac, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(rate, 6), "unit": "decode steps/s", "cores": P,
+                                "kind": "oracle", "sample": sample}
+    return line
+
+
+def run_reference(args):
+    """The fp64 oracle as it stands, timed on the host cores for the same
+    workload, metric and unit (bounded sample per step)."""
+    wl = W.cfg2(n_layers=args.layers, n_steps=args.decode_steps) if args.workload == "cfg2" else W.cfg1()
+    # slow fraction of this workload's schedule (host-only bookkeeping on the seeded trace)
+    from oracle import sfi_oracle as O
+    slow = O.schedule(wl.boundary_trace(), wl.budget)
+    frac = float(slow.mean())
+    rates = []
+    sample = ""
+    P = 1
+    for s in range(args.warmup + args.steps):
+        rate, P, sample, _, _ = cpu_oracle_rate(wl, frac, budget_s=args.cpu_budget)
+        if s >= args.warmup:
+            rates.append(rate)
+    value = float(np.mean(rates))
+    units_per_step = wl.n_layers * wl.shape.batch * wl.shape.n_kv_heads
+    return {
+        "impl": "reference",
+        "metric": "SFI decode steps/s (slow & fast) and achieved HBM GB/s as % of GB300 peak",
+        "value": round(value, 6), "unit": "decode steps/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "units_per_decode_step": units_per_step},
+        "cpu_baseline": {"value": round(value, 6), "unit": "decode steps/s", "cores": P,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "decode steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="cfg2", choices=["cfg2", "cfg1"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--cpu-budget", type=float, default=1.5, help="seconds per CPU worker")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -214,6 +214,20 @@ sfi_status sfi_decode_step(sfi_ctx* ctx, int32_t layer, const uint8_t* is_bounda
 sfi_status sfi_schedule(int32_t batch, int32_t budget, const uint8_t* is_boundary,
                         uint8_t* have_sel, int32_t* since, uint8_t* slow_out);
 
+/* Forget the schedule state (every sequence starts again without a
+ * selection, so its next step is slow).  Host only. */
+sfi_status sfi_ctx_reset(sfi_ctx* ctx);
+
+/* Device-time profiling of sfi_decode_step (off by default).  enable != 0
+ * (re)starts recording: every later decode step records CUDA events around
+ * its attention launch and around its evidence + selector launches.
+ * sfi_ctx_profile_read waits for the recorded events and returns the summed
+ * device milliseconds and launch counts since the last enable.  enable == 0
+ * stops recording. */
+sfi_status sfi_ctx_profile(sfi_ctx* ctx, int32_t enable);
+sfi_status sfi_ctx_profile_read(sfi_ctx* ctx, double* attn_ms, int64_t* attn_launches,
+                                double* select_ms, int64_t* select_launches);
+
 /* The current step's decision (host [B], 1 = slow). */
 sfi_status sfi_ctx_slow_mask(const sfi_ctx* ctx, uint8_t* slow_host);
 

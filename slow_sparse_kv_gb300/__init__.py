@@ -65,6 +65,10 @@ EXPORTS = {
     "sfi_decode_step": (c_int32, [c_void_p, c_int32, c_void_p, _L, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p]),
     "sfi_schedule": (c_int32, [c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "sfi_ctx_reset": (c_int32, [c_void_p]),
+    "sfi_ctx_profile": (c_int32, [c_void_p, c_int32]),
+    "sfi_ctx_profile_read": (c_int32, [c_void_p, POINTER(ctypes.c_double), POINTER(ctypes.c_int64),
+                                       POINTER(ctypes.c_double), POINTER(ctypes.c_int64)]),
     "sfi_ctx_slow_mask": (c_int32, [c_void_p, c_void_p]),
     "sfi_ctx_selection": (c_int32, [c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
 }
@@ -240,6 +244,20 @@ class DecodeContext:
         _check("sfi_decode_step", lib.sfi_decode_step(
             self.h, int(layer), buf, ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
             _stream(stream)))
+
+    def reset(self) -> None:
+        _check("sfi_ctx_reset", lib.sfi_ctx_reset(self.h))
+
+    def profile(self, enable: bool) -> None:
+        _check("sfi_ctx_profile", lib.sfi_ctx_profile(self.h, int(bool(enable))))
+
+    def profile_read(self):
+        """(attention ms, attention launches, evidence+selector ms, their launches)."""
+        am, sm = ctypes.c_double(), ctypes.c_double()
+        al, sl = ctypes.c_int64(), ctypes.c_int64()
+        _check("sfi_ctx_profile_read", lib.sfi_ctx_profile_read(
+            self.h, ctypes.byref(am), ctypes.byref(al), ctypes.byref(sm), ctypes.byref(sl)))
+        return am.value, al.value, sm.value, sl.value
 
     def slow_mask(self):
         buf = (ctypes.c_uint8 * self.batch)()

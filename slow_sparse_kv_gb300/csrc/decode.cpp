@@ -6,6 +6,7 @@
 // per token (at layer 0) and shared by all layers.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -25,18 +26,52 @@ struct sfi_ctx {
   std::vector<uint8_t> have_sel, slow;
   std::vector<int32_t> since;
   bool decided = false;
+  // profiling: rings of event pairs, flushed into the totals when full
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_attn, ev_sel;
+  size_t n_attn_pending = 0, n_sel_pending = 0;
+  double attn_ms = 0.0, sel_ms = 0.0;
+  int64_t attn_launches = 0, sel_launches = 0;
 };
 
 namespace {
 
+constexpr size_t kProfPairs = 4096;
+
 void free_ctx(sfi_ctx* c) {
   if (!c) return;
+  for (cudaEvent_t e : c->ev_attn) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->ev_sel) cudaEventDestroy(e);
   cudaFree(c->ws);
   cudaFree(c->f);
   cudaFree(c->knorm);
   cudaFree(c->idx);
   cudaFree(c->count);
   delete c;
+}
+
+// Sum the elapsed times of the first n recorded pairs of `ev` (waits for them).
+cudaError_t flush_pairs(std::vector<cudaEvent_t>& ev, size_t& n, double& total_ms) {
+  if (n == 0) return cudaSuccess;
+  cudaError_t e = cudaEventSynchronize(ev[2 * n - 1]);
+  for (size_t i = 0; i < n && e == cudaSuccess; ++i) {
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]);
+    total_ms += ms;
+  }
+  n = 0;
+  return e;
+}
+
+cudaError_t record_pair(std::vector<cudaEvent_t>& ev, size_t& n, double& total_ms, bool second,
+                        cudaStream_t st) {
+  if (!second && n == kProfPairs) {
+    cudaError_t e = flush_pairs(ev, n, total_ms);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaEventRecord(ev[2 * n + (second ? 1 : 0)], st);
+  if (second) ++n;
+  return e;
 }
 
 }  // namespace
@@ -111,6 +146,51 @@ sfi_status sfi_schedule(int32_t batch, int32_t budget, const uint8_t* is_boundar
       since[b] += 1;
     }
   }
+  return SFI_OK;
+}
+
+sfi_status sfi_ctx_reset(sfi_ctx* c) {
+  if (!c) return fail(SFI_ERR_INVALID_ARG, "ctx is NULL");
+  std::fill(c->have_sel.begin(), c->have_sel.end(), 0);
+  std::fill(c->since.begin(), c->since.end(), 0);
+  std::fill(c->slow.begin(), c->slow.end(), 0);
+  c->decided = false;
+  return SFI_OK;
+}
+
+sfi_status sfi_ctx_profile(sfi_ctx* c, int32_t enable) {
+  if (!c) return fail(SFI_ERR_INVALID_ARG, "ctx is NULL");
+  if (enable && c->ev_attn.empty()) {
+    c->ev_attn.resize(2 * kProfPairs, nullptr);
+    c->ev_sel.resize(2 * kProfPairs, nullptr);
+    for (auto* v : {&c->ev_attn, &c->ev_sel})
+      for (auto& e : *v) {
+        const cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) return cuda_fail(r, "creating profiling events");
+      }
+  }
+  c->profiling = enable != 0;
+  if (enable) {
+    c->n_attn_pending = c->n_sel_pending = 0;
+    c->attn_ms = c->sel_ms = 0.0;
+    c->attn_launches = c->sel_launches = 0;
+  }
+  return SFI_OK;
+}
+
+sfi_status sfi_ctx_profile_read(sfi_ctx* c, double* attn_ms, int64_t* attn_launches,
+                                double* select_ms, int64_t* select_launches) {
+  if (!c || !attn_ms || !attn_launches || !select_ms || !select_launches)
+    return fail(SFI_ERR_INVALID_ARG, "ctx and every output must be set");
+  if (!c->ev_attn.empty()) {
+    cudaError_t e = flush_pairs(c->ev_attn, c->n_attn_pending, c->attn_ms);
+    if (e == cudaSuccess) e = flush_pairs(c->ev_sel, c->n_sel_pending, c->sel_ms);
+    if (e != cudaSuccess) return cuda_fail(e, "reading profiling events");
+  }
+  *attn_ms = c->attn_ms;
+  *attn_launches = c->attn_launches;
+  *select_ms = c->sel_ms;
+  *select_launches = c->sel_launches;
   return SFI_OK;
 }
 
@@ -190,8 +270,20 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   const long long total = (long long)d.n_kv_heads *
                           ((long long)n_slow * d.max_len + (long long)(d.batch - n_slow) * fast_bound);
   const int max_unit = n_slow ? d.max_len : fast_bound;
+  cudaError_t e = cudaSuccess;
+  if (c->profiling) e = record_pair(c->ev_attn, c->n_attn_pending, c->attn_ms, false, st);
+  if (e != cudaSuccess) return cuda_fail(e, "profiling event");
   if ((s = run_attn(a, &Lc, total, max_unit, st)) != SFI_OK) return s;
+  if (c->profiling) {
+    e = record_pair(c->ev_attn, c->n_attn_pending, c->attn_ms, true, st);
+    if (e != cudaSuccess) return cuda_fail(e, "profiling event");
+    c->attn_launches += 1;
+  }
   if (n_slow == 0) return SFI_OK;
+  if (c->profiling) {
+    e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, false, st);
+    if (e != cudaSuccess) return cuda_fail(e, "profiling event");
+  }
 
   FpassArgs fa{};
   fa.logits = a.logits;
@@ -204,7 +296,7 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   fa.max_len = d.max_len;
   fa.slow = a.slow;
   fa.status = a.status;
-  cudaError_t e = launch_fpass(fa, st);
+  e = launch_fpass(fa, st);
   if (e != cudaSuccess) return cuda_fail(e, "evidence pass launch");
 
   SelectArgs sa{};
@@ -226,6 +318,11 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   sa.status = a.status;
   e = launch_select(sa, st);
   if (e != cudaSuccess) return cuda_fail(e, "selector launch");
+  if (c->profiling) {
+    e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, true, st);
+    if (e != cudaSuccess) return cuda_fail(e, "profiling event");
+    c->sel_launches += 2;
+  }
   return SFI_OK;
 }
 
