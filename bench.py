@@ -486,6 +486,63 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+def run_kernel_cases(args):
+    """Each kernel of the path alone on one 128K layer (batch --case-batch),
+    timed with CUDA events over --steps repetitions after --warmup, with an L2
+    flush (a 512 MB write) between repetitions.  Also the driver for the ncu
+    captures (one launch of each kernel per repetition)."""
+    import torch
+    import slow_sparse_kv_gb300 as sfi
+    wl = W.cfg2(n_layers=1, n_steps=1)
+    wl.shape = W.Shape(args.case_batch, 32, 8, 128, "bf16")
+    wl.n0 = wl.n0[:args.case_batch]
+    wl.cap = wl.cap[:args.case_batch]
+    R = Cfg2Runner(wl, 0)
+    sh = wl.shape
+    B = sh.batch
+    lay = sfi.Layout(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16, R.offsets, wl.cap, wl.n0,
+                     R.max_len, device=R.dev)
+    ws = sfi.alloc_workspace(lay)
+    q = R.Q[0][0]
+    out = torch.empty(B, sh.n_q_heads, sh.head_dim, device=R.dev)
+    f = torch.empty(B, sh.n_kv_heads, R.max_len, device=R.dev)
+    kn = torch.empty_like(f)
+    idx = torch.empty(B, sh.n_kv_heads, wl.k, dtype=torch.int32, device=R.dev)
+    cnt = torch.empty(B, sh.n_kv_heads, dtype=torch.int32, device=R.dev)
+    prm = sfi.params(wl.n_sink, wl.window, wl.k, wl.lam)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=R.dev)
+    row = 2 * sh.n_kv_heads * sh.head_dim * 2
+    n = wl.n0[0]
+    cases = {
+        "dense": (lambda: sfi.sfi_slow_attn(lay, q, R.K[0], R.V[0], out, None, None, ws), B * n * row),
+        "slow": (lambda: sfi.sfi_slow_attn(lay, q, R.K[0], R.V[0], out, f, kn, ws), B * n * row),
+        "select": (lambda: sfi.sfi_select(lay, prm, f, kn, idx, cnt, None, ws),
+                   B * sh.n_kv_heads * n * 8),
+        "fast": (lambda: sfi.sfi_fast_attn(lay, prm, q, R.K[0], R.V[0], idx, cnt, out, ws),
+                 B * (wl.n_sink + wl.k + wl.window) * row),
+    }
+    res = {}
+    cases["slow"][0]()
+    cases["select"][0]()
+    torch.cuda.synchronize()
+    for name in args.kernel_case.split(","):
+        fn, nbytes = cases[name]
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        res[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / ms / 1e6, 1), "bytes": nbytes}
+    res["device_status"] = sfi.sfi_read_status(ws)
+    return {"kernel_cases": res, "batch": B, "context": n}
+
+
 def run_reference(args):
     """The fp64 oracle as it stands, timed on the host cores for the same
     workload, metric and unit (bounded sample per step)."""
@@ -528,10 +585,16 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=1.5, help="seconds per CPU worker")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast: time "
+                    "each kernel alone on one 128K layer instead of the decode benchmark")
+    ap.add_argument("--case-batch", type=int, default=2)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.kernel_case:
+        print(json.dumps(run_kernel_cases(args)), flush=True)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
