@@ -175,6 +175,33 @@ sfi_status sfi_fast_attn(const sfi_layout* layout, const sfi_params* params,
                          const int32_t* idx, const int32_t* count, float* out,
                          void* ws, size_t ws_bytes, sfi_stream stream);
 
+/* Fast step that allocates nothing and takes no workspace.  The pages have
+ * no counterpart to this call; it exists for callers that may not allocate
+ * device memory on the path that runs the step -- for example a plug-in
+ * interface that hands over only inputs and outputs, or a serving loop that
+ * promised to allocate nothing after start-up because cudaMalloc can
+ * synchronise the whole device.  It computes exactly what sfi_fast_attn
+ * computes (same arguments and layout, minus the workspace).
+ *  - Scratch: a fixed 16 MiB device array inside the library, kept by every
+ *    GPU that loads the library until the process exits.  It holds the
+ *    status word, one counter per (sequence, KV head) and the split partial
+ *    results of head_dim + 2 floats per query head and work piece.
+ *    Geometries whose B * H_kv units do not fit even one piece each are
+ *    rejected with SFI_ERR_CAPACITY and a message giving the bytes needed.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before capturing a stream
+ *    into a CUDA graph.
+ *  - Each call clears the status word and counters with cudaMemsetAsync on
+ *    `stream` and calls no allocating routine.
+ *  - All calls share the one array: calls that overlap on the GPU (other
+ *    streams, other threads) race on it and must be serialised by the caller.
+ *    The device status word of this call is not readable through
+ *    sfi_read_status (there is no workspace). */
+sfi_status sfi_fast_attn_noalloc(const sfi_layout* layout, const sfi_params* params,
+                                 const void* q, const void* k, const void* v,
+                                 const int32_t* idx, const int32_t* count, float* out,
+                                 sfi_stream stream);
+
 /* ---------------------------------------------------------------- decode driver */
 
 typedef struct sfi_ctx sfi_ctx;

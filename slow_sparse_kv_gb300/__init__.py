@@ -60,6 +60,8 @@ EXPORTS = {
     "sfi_fast_attn_workspace_size": (c_size_t, [_L, _P]),
     "sfi_fast_attn": (c_int32, [_L, _P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "sfi_fast_attn_noalloc": (c_int32, [_L, _P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p]),
     "sfi_ctx_create": (c_int32, [POINTER(sfi_ctx_desc), POINTER(c_void_p)]),
     "sfi_ctx_destroy": (c_int32, [c_void_p]),
     "sfi_decode_step": (c_int32, [c_void_p, c_int32, c_void_p, _L, c_void_p, c_void_p, c_void_p,
@@ -204,6 +206,15 @@ def sfi_schedule(is_boundary, have_sel, since, budget: int):
     _check("sfi_schedule", lib.sfi_schedule(B, int(budget), ib.ctypes.data, have_sel.ctypes.data,
                                             since.ctypes.data, out.ctypes.data))
     return out
+
+
+def sfi_fast_attn_noalloc(layout: Layout, prm: sfi_params, q, k, v, idx, count, out, stream=None):
+    """The fast step without a workspace (scratch in a fixed array inside the
+    library), for callers that may not allocate on the path that runs it."""
+    c = layout.c
+    _check("sfi_fast_attn_noalloc", lib.sfi_fast_attn_noalloc(
+        ctypes.byref(c), ctypes.byref(prm), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(count),
+        _ptr(out), _stream(stream)))
 
 
 def sfi_read_status(ws: torch.Tensor, stream=None) -> int:
