@@ -263,15 +263,19 @@ sfi_status sfi_select(const sfi_layout* L, const sfi_params* P, const float* evi
   if (P->mode == SFI_SELECT_FUSED && !knorm)
     return fail(SFI_ERR_INVALID_ARG, "fused selection needs the key norms");
   if ((s = check_ws(L, ws, ws_bytes)) != SFI_OK) return s;
+  if (L->max_len > kSelectMaxLen)
+    return fail(SFI_ERR_CAPACITY, "the selector holds at most %d positions per row (max_len %d)",
+                kSelectMaxLen, L->max_len);
   const WsPlan p = plan_workspace(L->batch, L->n_q_heads, L->n_kv_heads, L->head_dim, L->max_len);
   char* w = static_cast<char*>(ws);
   SelectArgs a{};
   a.evidence = evidence;
   a.knorm = knorm;
+  a.H_q = L->n_q_heads;
   a.len = L->len;
   a.idx = idx_out;
   a.count = count_out;
-  a.s = s_out ? s_out : reinterpret_cast<float*>(w + p.s_off);
+  a.s = s_out;
   a.B = L->batch;
   a.H_kv = L->n_kv_heads;
   a.max_len = L->max_len;

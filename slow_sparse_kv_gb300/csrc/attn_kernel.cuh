@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const Att
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
       mbar_init(bar_empty + 8 * s, C::NCW);
     }
     fence_mbar_init();
@@ -200,36 +200,57 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const Att
         const int nr = min(C::SR, I.r1 - c0);
         const int slot = stage % C::NS;
         const uint32_t ph = (stage / C::NS) & 1u;
+        // cache positions of this stage's rows (lane l: rows l, l + 32, ...)
+        int pos[(C::SR + 31) / 32];
+#pragma unroll
+        for (int j = 0; j < (C::SR + 31) / 32; ++j) {
+          const int r = lane + 32 * j;
+          const int lp = c0 + r;
+          int p = 0;
+          if (!I.slow && r < nr) {
+            if (lp < ns) {
+              p = lp;
+            } else if (lp < ns + cnt) {
+              p = __ldg(ix + (lp - ns));
+              if (p < 0 || p >= n) {
+                set_status(a.status, SFI_DEV_BAD_INDEX);
+                p = 0;
+              }
+            } else {
+              p = wlo + (lp - ns - cnt);
+            }
+          }
+          pos[j] = p;
+        }
         if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
-        __syncwarp();
         const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
         if (I.slow) {
+          // dense rows: one bulk copy of K and one of V for the whole stage
           if (lane == 0) {
+            mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
             bulk_g2s(kd, kb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
             bulk_g2s(vd, vb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
+          } else {
+            mbar_arrive(bar_full + 8 * slot);
           }
         } else {
-          for (int j = lane; j < nr; j += 32) {
-            const int lp = c0 + j;
-            int pos;
-            if (lp < ns) {
-              pos = lp;
-            } else if (lp < ns + cnt) {
-              pos = __ldg(ix + (lp - ns));
-              if (pos < 0 || pos >= n) {
-                set_status(a.status, SFI_DEV_BAD_INDEX);
-                pos = 0;
-              }
-            } else {
-              pos = wlo + (lp - ns - cnt);
+          // gathered rows: every lane copies 16 bytes of LPR-lane rows; the
+          // row positions were resolved before the wait (pos[]), lane l
+          // holding the rows l, l + 32, ...
+#pragma unroll
+          for (int i = 0; i < C::SR / C::RPI; ++i) {
+            const int r = i * C::RPI + lane / C::LPR;
+            const int p = __shfl_sync(kFull, pos[(i * C::RPI) / 32], r & 31);
+            if (r < nr) {
+              const size_t so = size_t(p) * C::ROWB + (lane % C::LPR) * 16;
+              cp_async16(kd + r * C::ROWB + (lane % C::LPR) * 16, kb + so, pol);
+              cp_async16(vd + r * C::ROWB + (lane % C::LPR) * 16, vb + so, pol);
             }
-            bulk_g2s(kd + j * C::ROWB, kb + size_t(pos) * C::ROWB, C::ROWB, bar_full + 8 * slot, pol);
-            bulk_g2s(vd + j * C::ROWB, vb + size_t(pos) * C::ROWB, C::ROWB, bar_full + 8 * slot, pol);
           }
+          cp_async_arrive_noinc(bar_full + 8 * slot);
         }
         ++stage;
       }

@@ -18,7 +18,6 @@ struct sfi_ctx {
   sfi::WsPlan plan;
   // device
   char* ws = nullptr;          // attention / selector workspace
-  float* f = nullptr;          // [B*H_kv][max_len]
   float* knorm = nullptr;      // [B*H_kv][max_len]
   int32_t* idx = nullptr;      // [L][B*H_kv][k]
   int32_t* count = nullptr;    // [L][B*H_kv]
@@ -43,7 +42,6 @@ void free_ctx(sfi_ctx* c) {
   for (cudaEvent_t e : c->ev_attn) cudaEventDestroy(e);
   for (cudaEvent_t e : c->ev_sel) cudaEventDestroy(e);
   cudaFree(c->ws);
-  cudaFree(c->f);
   cudaFree(c->knorm);
   cudaFree(c->idx);
   cudaFree(c->count);
@@ -102,6 +100,8 @@ sfi_status sfi_ctx_create(const sfi_ctx_desc* d, sfi_ctx** out) {
     return fail(SFI_ERR_INVALID_ARG, "the decode driver runs the fused (SFI) selector");
   if (d->n_layers < 1) return fail(SFI_ERR_INVALID_ARG, "n_layers must be >= 1");
   if (d->budget < 0) return fail(SFI_ERR_INVALID_ARG, "budget must be >= 0");
+  if (d->max_len > kSelectMaxLen)
+    return fail(SFI_ERR_CAPACITY, "the selector holds at most %d positions per row", kSelectMaxLen);
   sfi_ctx* c = new (std::nothrow) sfi_ctx();
   if (!c) return fail(SFI_ERR_CAPACITY, "out of host memory");
   c->desc = *d;
@@ -110,7 +110,6 @@ sfi_status sfi_ctx_create(const sfi_ctx_desc* d, sfi_ctx** out) {
   const size_t row = units * size_t(d->max_len) * sizeof(float);
   cudaError_t e = cudaMalloc(&c->ws, c->plan.total);
   if (e == cudaSuccess) e = cudaMemset(c->ws, 0, c->plan.total);
-  if (e == cudaSuccess) e = cudaMalloc(&c->f, row);
   if (e == cudaSuccess) e = cudaMalloc(&c->knorm, row);
   if (e == cudaSuccess)
     e = cudaMalloc(&c->idx, size_t(d->n_layers) * units * d->params.k * sizeof(int32_t));
@@ -285,27 +284,17 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
   }
 
-  FpassArgs fa{};
-  fa.logits = a.logits;
-  fa.stats = a.stats;
-  fa.len = Lc.len;
-  fa.f = c->f;
-  fa.B = d.batch;
-  fa.H_q = d.n_q_heads;
-  fa.H_kv = d.n_kv_heads;
-  fa.max_len = d.max_len;
-  fa.slow = a.slow;
-  fa.status = a.status;
-  e = launch_fpass(fa, st);
-  if (e != cudaSuccess) return cuda_fail(e, "evidence pass launch");
-
+  // Selector straight from the stored logits (the evidence f is formed on
+  // the fly; the decode path has no use for f itself).
   SelectArgs sa{};
-  sa.evidence = c->f;
+  sa.logits = a.logits;
+  sa.stats = a.stats;
+  sa.H_q = d.n_q_heads;
   sa.knorm = c->knorm;
   sa.len = Lc.len;
   sa.idx = idx;
   sa.count = count;
-  sa.s = reinterpret_cast<float*>(c->ws + c->plan.s_off);
+  sa.s = nullptr;
   sa.B = d.batch;
   sa.H_kv = d.n_kv_heads;
   sa.max_len = d.max_len;
@@ -321,7 +310,7 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   if (c->profiling) {
     e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, true, st);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
-    c->sel_launches += 2;
+    c->sel_launches += 1;
   }
   return SFI_OK;
 }

@@ -22,14 +22,26 @@
 // the lower position exactly as the definition says.  Histograms use
 // warp-aggregated shared-memory atomics (the score distribution is very
 // skewed, so many lanes hit the same bin).
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "common.cuh"
 
 namespace sfi {
 
-constexpr int kSelThreads = 1024;
 constexpr int kFpassThreads = 256;
+constexpr int kSelCluster = 8;   // CTAs per unit
+constexpr int kSelCT = 512;      // threads per selector CTA
+
+// f_i = (1/G) sum_h 2^(l_{h,i} - M_h) / Z_h, from log2-scaled logits.
+template <int G>
+__device__ __forceinline__ float evidence_from_logits(const float* l, const float (&M)[G],
+                                                      const float (&iz)[G]) {
+  float acc = 0.f;
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) acc = fmaf(exp2f(l[hh] - M[hh]), iz[hh], acc);
+  return acc * (1.0f / float(G));
+}
 
 template <int G>
 __global__ void __launch_bounds__(kFpassThreads) fpass_kernel(const FpassArgs a) {
@@ -45,15 +57,10 @@ __global__ void __launch_bounds__(kFpassThreads) fpass_kernel(const FpassArgs a)
     M[hh] = a.stats[qh * 2];
     iz[hh] = 1.0f / a.stats[qh * 2 + 1];
   }
-  const float inv_g = 1.0f / float(G);
   const float* lrow = a.logits + size_t(u) * a.max_len * G;
   float* frow = a.f + size_t(u) * a.max_len;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const float* l = lrow + size_t(i) * G;
-    float acc = 0.f;
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) acc = fmaf(exp2f(l[hh] - M[hh]), iz[hh], acc);
-    frow[i] = acc * inv_g;
+    frow[i] = evidence_from_logits<G>(lrow + size_t(i) * G, M, iz);
   }
 }
 
@@ -123,145 +130,206 @@ __device__ void pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_di
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
+// One cluster of kSelCluster CTAs per unit; CTA `rank` owns the positions
+// [rank * ch, (rank + 1) * ch) of [0, n) and keeps their scores in shared
+// memory.  Cluster-wide quantities (the key-norm sum over E, the radix
+// histograms, the compaction offsets) are exchanged through distributed
+// shared memory; every CTA takes the same decisions from the same data.
+// EV_G > 0: the evidence is computed here from the attention kernel's
+// log2-scaled logits [pos][EV_G] and per-head (M, Z) (decode path); EV_G == 0:
+// `evidence` holds f (or, per sequence, the per-KV-head logit sums).
+template <int EV_G>
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
+    select_cluster_kernel(const SelectArgs a) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  extern __shared__ __align__(16) unsigned char sel_smem[];
+  float* sc = reinterpret_cast<float*>(sel_smem);
   __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist_g[4][256];  // cluster totals, used in rank 0
   __shared__ float shf[33];
-  __shared__ unsigned long long scan_w[33];
+  __shared__ float part_nu;
+  __shared__ uint32_t cnt_gt, cnt_eq;
   __shared__ uint32_t sh_digit, sh_above;
+  __shared__ uint32_t warp_cnt[2][kSelCT / 32];
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int rank = int(cl.block_rank());
+  const int unit = blockIdx.x / kSelCluster;
   const bool per_seq = a.mode == SFI_SELECT_LOGIT_SUM_SEQ;
-  const int b = per_seq ? blockIdx.x : blockIdx.x / a.H_kv;
-  if (!seq_is_slow(a.active, b)) return;
-  const int u = per_seq ? b * a.H_kv : blockIdx.x;  // row of s / evidence used for scores
+  const int b = per_seq ? unit : unit / a.H_kv;
+  if (!seq_is_slow(a.active, b)) return;  // uniform over the cluster
+  const int u = per_seq ? b * a.H_kv : unit;
   const int n = a.len[b];
   if (n < 1 || n > a.max_len) {
-    if (tid == 0) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
-    return;
+    if (tid == 0 && rank == 0) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
+    return;  // uniform over the cluster
   }
   const int lo = per_seq ? 0 : a.n_sink;
   const int hi = max(lo, n - a.window);
   const int ne = hi - lo;
   const int keff = min(a.k, ne);
-  float* srow = a.s + size_t(u) * a.max_len;
-
-  // ---------------------------------------------------------------- scores
-  for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
-  float coef = 0.f;
-  if (!per_seq) {
-    const float* kn = a.knorm + size_t(u) * a.max_len;
-    float part = 0.f;
-    for (int i = lo + tid; i < hi; i += kSelThreads) part += kn[i];
-    const float tot = sel_block_sum(part, shf);
-    coef = tot > 0.f ? a.lambda / tot : 0.f;
-  }
-  __syncthreads();
+  const int n_sc = per_seq ? hi : n;  // positions that receive a score
+  const int ch = (n_sc + kSelCluster - 1) / kSelCluster;
+  const int p0 = min(n_sc, rank * ch), p1 = min(n_sc, p0 + ch);
   const bool need_radix = keff > 0 && keff < ne;
-  {
-    const float* ev = a.evidence + size_t(u) * a.max_len;
-    const float* kn = per_seq ? nullptr : a.knorm + size_t(u) * a.max_len;
-    const int n_s = per_seq ? hi : n;  // positions that get a score
-    const float w_f = 1.0f - a.lambda;
-    for (int base = 0; base < n_s; base += kSelThreads) {
-      const int i = base + tid;
-      const bool in = i < n_s;
-      float sc = 0.f;
-      if (in) {
-        if (per_seq) {
-          for (int g = 0; g < a.H_kv; ++g) sc += a.evidence[(size_t(b) * a.H_kv + g) * a.max_len + i];
-        } else {
-          sc = w_f * ev[i];
-          if (i >= lo && i < hi) sc = fmaf(coef, kn[i], sc);
-        }
-        srow[i] = sc;
-      }
-      if (need_radix) hist_add(hist, order_key(sc) >> 24, in && i >= lo && i < hi);
+  const float* kn = per_seq ? nullptr : a.knorm + size_t(u) * a.max_len;
+
+  // ---------------------------------------------------------------- evidence
+  float M[EV_G > 0 ? EV_G : 1], iz[EV_G > 0 ? EV_G : 1];
+  if constexpr (EV_G > 0) {
+#pragma unroll
+    for (int hh = 0; hh < EV_G; ++hh) {
+      const size_t qh = size_t(b) * a.H_q + size_t(unit % a.H_kv) * EV_G + hh;
+      M[hh] = a.stats[qh * 2];
+      iz[hh] = 1.0f / a.stats[qh * 2 + 1];
     }
   }
+  float part = 0.f;
+  for (int i = p0 + tid; i < p1; i += kSelCT) {
+    float ev;
+    if constexpr (EV_G > 0) {
+      ev = evidence_from_logits<EV_G>(a.logits + (size_t(u) * a.max_len + i) * EV_G, M, iz);
+    } else if (per_seq) {
+      ev = 0.f;
+      for (int g = 0; g < a.H_kv; ++g) ev += a.evidence[(size_t(b) * a.H_kv + g) * a.max_len + i];
+    } else {
+      ev = a.evidence[size_t(u) * a.max_len + i];
+    }
+    sc[i - p0] = ev;
+    if (!per_seq && i >= lo && i < hi) part += kn[i];
+  }
+  if (tid < 256) {
+    hist[tid] = 0;
+    if (rank == 0) {
+      for (int j = 0; j < 4; ++j) hist_g[j][tid] = 0;
+    }
+  }
+  if (!per_seq) {
+    const float t = sel_block_sum(part, shf);
+    if (tid == 0) part_nu = t;
+  }
+  cl.sync();  // partial norm sums and the zeroed cluster histograms are visible
+  float coef = 0.f;
+  if (!per_seq) {
+    float tot = 0.f;
+    for (int r = 0; r < kSelCluster; ++r) tot += *cl.map_shared_rank(&part_nu, r);
+    coef = tot > 0.f ? a.lambda / tot : 0.f;
+  }
+  // ---------------------------------------------------------------- scores
+  float* srow = a.s ? a.s + size_t(u) * a.max_len : nullptr;
+  const float w_f = per_seq ? 1.0f : 1.0f - a.lambda;
+  for (int base = p0; base < p1; base += kSelCT) {
+    const int i = base + tid;
+    const bool in = i < p1;
+    float v = 0.f;
+    if (in) {
+      v = w_f * sc[i - p0];
+      if (!per_seq && i >= lo && i < hi) v = fmaf(coef, kn[i], v);
+      sc[i - p0] = v;
+      if (srow) srow[i] = v;
+    }
+    if (need_radix) hist_add(hist, order_key(v) >> 24, in && i >= lo && i < hi);
+  }
   __syncthreads();
 
-  int32_t* out_idx = a.idx + size_t(blockIdx.x * (per_seq ? a.H_kv : 1)) * a.k;
-  if (!need_radix) {
-    // keep all of E (or nothing)
-    for (int j = tid; j < keff; j += kSelThreads) out_idx[j] = lo + j;
-  } else {
+  int32_t* out_idx = a.idx + size_t(per_seq ? b * a.H_kv : unit) * a.k;
+  if (need_radix) {
     // ------------------------------------------------------------ radix select
     uint32_t prefix = 0, krem = uint32_t(keff);
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       if (pass > 0) {
-        for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+        if (tid < 256) hist[tid] = 0;
         __syncthreads();
-        for (int base = lo; base < hi; base += kSelThreads) {
+        const int e0 = max(p0, lo), e1 = min(p1, hi);
+        for (int base = e0; base < e1; base += kSelCT) {
           const int i = base + tid;
-          const bool in = i < hi;
-          const uint32_t key = in ? order_key(srow[i]) : 0u;
-          const bool match = in && (key >> (shift + 8)) == prefix;
-          hist_add(hist, (key >> shift) & 255u, match);
+          const bool in = i < e1;
+          const uint32_t key = in ? order_key(sc[i - p0]) : 0u;
+          hist_add(hist, (key >> shift) & 255u, in && (key >> (shift + 8)) == prefix);
         }
         __syncthreads();
       }
+      if (tid < 256 && hist[tid]) atomicAdd(cl.map_shared_rank(&hist_g[pass][tid], 0), hist[tid]);
+      cl.sync();
+      if (tid < 256) hist[tid] = *cl.map_shared_rank(&hist_g[pass][tid], 0);
+      __syncthreads();
       if (tid < 32) pick_digit(hist, krem, &sh_digit, &sh_above);
       __syncthreads();
       prefix = (prefix << 8) | sh_digit;
       krem -= sh_above;
+    }
+    const uint32_t tau = prefix, take_eq = krem;
+    // ------------------------------------------------------------ compaction
+    const int e0 = max(p0, lo), e1 = min(p1, hi);
+    uint32_t g_loc = 0, q_loc = 0;
+    for (int i = e0 + tid; i < e1; i += kSelCT) {
+      const uint32_t key = order_key(sc[i - p0]);
+      g_loc += key > tau;
+      q_loc += key == tau;
+    }
+    const float gs = sel_block_sum(float(g_loc), shf);  // exact: counts < 2^24
+    const float qs = sel_block_sum(float(q_loc), shf);
+    if (tid == 0) {
+      cnt_gt = uint32_t(gs);
+      cnt_eq = uint32_t(qs);
+    }
+    cl.sync();
+    uint32_t gt_before = 0, eq_before = 0;
+    for (int r = 0; r < rank; ++r) {
+      gt_before += *cl.map_shared_rank(&cnt_gt, r);
+      eq_before += *cl.map_shared_rank(&cnt_eq, r);
+    }
+    for (int base = e0; base < e1; base += kSelCT) {
+      const int i = base + tid;
+      const bool in = i < e1;
+      const uint32_t key = in ? order_key(sc[i - p0]) : 0u;
+      const bool isg = in && key > tau, isq = in && key == tau;
+      const unsigned bg = __ballot_sync(kFull, isg), bq = __ballot_sync(kFull, isq);
+      const unsigned lt = (1u << lane) - 1u;
+      if (lane == 0) {
+        warp_cnt[0][w] = __popc(bg);
+        warp_cnt[1][w] = __popc(bq);
+      }
+      __syncthreads();
+      uint32_t wg = 0, wq = 0, tg = 0, tq = 0;
+      for (int j = 0; j < kSelCT / 32; ++j) {
+        const uint32_t cg_ = warp_cnt[0][j], cq_ = warp_cnt[1][j];
+        if (j < w) {
+          wg += cg_;
+          wq += cq_;
+        }
+        tg += cg_;
+        tq += cq_;
+      }
+      const uint32_t gb = gt_before + wg + __popc(bg & lt);
+      const uint32_t qb = eq_before + wq + __popc(bq & lt);
+      if (isg) out_idx[gb + min(qb, take_eq)] = i;
+      if (isq && qb < take_eq) out_idx[gb + qb] = i;
+      gt_before += tg;
+      eq_before += tq;
       __syncthreads();
     }
-    const uint32_t tau = prefix;
-    const uint32_t take_eq = krem;
-    // ------------------------------------------------------------ compaction
-    const int ch = (ne + kSelThreads - 1) / kSelThreads;
-    const int c0 = lo + tid * ch, c1 = min(hi, c0 + ch);
-    uint32_t cg = 0, ceq = 0;
-    for (int i = c0; i < c1; ++i) {
-      const uint32_t key = order_key(srow[i]);
-      cg += key > tau;
-      ceq += key == tau;
-    }
-    unsigned long long v = (static_cast<unsigned long long>(cg) << 32) | ceq;
-    const int lane = tid & 31, w = tid >> 5;
-    unsigned long long incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) scan_w[w] = incl;
-    __syncthreads();
-    if (tid == 0) {
-      unsigned long long s = 0;
-      for (int i = 0; i < kSelThreads / 32; ++i) {
-        const unsigned long long x = scan_w[i];
-        scan_w[i] = s;
-        s += x;
-      }
-    }
-    __syncthreads();
-    const unsigned long long ex = scan_w[w] + incl - v;
-    uint32_t gt_before = uint32_t(ex >> 32), eq_before = uint32_t(ex & 0xffffffffu);
-    for (int i = c0; i < c1; ++i) {
-      const uint32_t key = order_key(srow[i]);
-      if (key > tau) {
-        out_idx[gt_before + min(eq_before, take_eq)] = i;
-        ++gt_before;
-      } else if (key == tau) {
-        if (eq_before < take_eq) out_idx[gt_before + eq_before] = i;
-        ++eq_before;
-      }
-    }
+  } else {
+    // keep all of E (or nothing): position lo + j goes to slot j
+    const int e0 = max(p0, lo), e1 = min(min(p1, hi), lo + keff);
+    for (int i = e0 + tid; i < e1; i += kSelCT) out_idx[i - lo] = i;
   }
-  if (tid == 0) {
+  if (tid == 0 && rank == 0) {
     if (per_seq) {
       for (int g = 0; g < a.H_kv; ++g) a.count[b * a.H_kv + g] = keff;
     } else {
       a.count[u] = keff;
     }
   }
+  cl.sync();  // every CTA's set is written, and no CTA leaves while others read its memory
   if (per_seq && a.H_kv > 1) {
-    // every KV head of the sequence reads the same selected set
-    __syncthreads();
+    // every KV head of the sequence reads the same set; CTA `rank` copies its share
+    const int cs = (keff + kSelCluster - 1) / kSelCluster;
+    const int j0 = rank * cs, j1 = min(keff, j0 + cs);
     for (int g = 1; g < a.H_kv; ++g)
-      for (int j = tid; j < keff; j += kSelThreads) out_idx[size_t(g) * a.k + j] = out_idx[j];
+      for (int j = j0 + tid; j < j1; j += kSelCT) out_idx[size_t(g) * a.k + j] = out_idx[j];
   }
 }
 
@@ -283,10 +351,30 @@ cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
-  const int grid = a.mode == SFI_SELECT_LOGIT_SUM_SEQ ? a.B : a.B * a.H_kv;
-  select_kernel<<<grid, kSelThreads, 0, st>>>(a);
+size_t select_smem_bytes(int max_len) {
+  return size_t((max_len + kSelCluster - 1) / kSelCluster) * sizeof(float);
+}
+
+template <int EV_G>
+cudaError_t launch_select_t(const SelectArgs& a, cudaStream_t st) {
+  const size_t smem = select_smem_bytes(a.max_len);
+  cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel<EV_G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  const int units = a.mode == SFI_SELECT_LOGIT_SUM_SEQ ? a.B : a.B * a.H_kv;
+  select_cluster_kernel<EV_G><<<units * kSelCluster, kSelCT, smem, st>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
+  if (!a.logits) return launch_select_t<0>(a, st);
+  switch (a.H_q / a.H_kv) {
+    case 1: return launch_select_t<1>(a, st);
+    case 2: return launch_select_t<2>(a, st);
+    case 4: return launch_select_t<4>(a, st);
+    case 8: return launch_select_t<8>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace sfi

@@ -58,13 +58,18 @@ struct FpassArgs {
   uint32_t* status;
 };
 
+constexpr int kSelectMaxLen = 409600;  // per-position rows the cluster selector holds in shared memory
+
 struct SelectArgs {
   const float* evidence;  // f (fused mode) or per-KV-head logit sums (logit-sum mode)
+  const float* logits;    // if set: compute f from these log2-scaled logits [unit][pos][G]
+  const float* stats;     //   and these per-head (M, Z) instead of reading `evidence`
+  int32_t H_q;
   const float* knorm;
   const int32_t* len;
   int32_t* idx;    // [B*H_kv][k]
   int32_t* count;  // [B*H_kv]
-  float* s;        // [B*H_kv][max_len] fused scores (s_out or workspace)
+  float* s;        // [B*H_kv][max_len] fused scores (nullable)
   int32_t B, H_kv, max_len;
   int32_t n_sink, window, k;
   float lambda;
