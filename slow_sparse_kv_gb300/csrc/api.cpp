@@ -132,15 +132,35 @@ int stage_rows(int dtype, int D) {
   return dtype == SFI_F32 ? attn_stage_rows_f32(D) : attn_stage_rows_bf16(D);
 }
 
-int choose_rows_per_item(long long total_rows, int max_unit_rows, int sr, int grid) {
-  long long min_rpi = ceil_div(ceil_div(max_unit_rows, kItemSlotsPerUnit), sr) * sr;
+// Rows per work item for a launch whose units come in two classes (n_a units
+// of at most rows_a rows, n_b of at most rows_b).  Items are processed in
+// waves over `grid` CTAs; the estimate of a launch is waves * (stages per
+// item + a fixed per-item cost of about three stages), minimised over item
+// sizes that split either class evenly.  At most kItemSlotsPerUnit items per
+// unit (the workspace holds that many partials).
+int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid) {
+  const int rows_max = rows_a > rows_b ? rows_a : rows_b;
+  long long min_rpi = ceil_div(ceil_div(rows_max, kItemSlotsPerUnit), sr) * sr;
   if (min_rpi < sr) min_rpi = sr;
-  // items of at most ~4096 rows, as a whole number of waves over the grid
-  long long waves = ceil_div(total_rows, (long long)grid * 4096);
-  if (waves < 1) waves = 1;
-  long long rpi = ceil_div(ceil_div(total_rows, grid * waves), sr) * sr;
-  if (rpi < min_rpi) rpi = min_rpi;
-  return int(rpi);
+  const double c_item = 3.0;
+  long long best = min_rpi;
+  double best_cost = 1e300;
+  for (int cls = 0; cls < 2; ++cls) {
+    const int rows = cls == 0 ? rows_a : rows_b;
+    if (rows <= 0 || (cls == 0 ? n_a : n_b) == 0) continue;
+    for (int k = 1; k <= kItemSlotsPerUnit; ++k) {
+      long long rpi = ceil_div(ceil_div(rows, k), sr) * sr;
+      if (rpi < min_rpi) rpi = min_rpi;
+      const long long items = n_a * ceil_div(rows_a, rpi) + n_b * ceil_div(rows_b, rpi);
+      const long long waves = ceil_div(items, grid);
+      const double cost = double(waves) * (double(rpi) / sr + c_item);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = rpi;
+      }
+    }
+  }
+  return int(best);
 }
 
 void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const void* k,
@@ -166,12 +186,11 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
   a.stats = reinterpret_cast<float*>(ws + p.stats_off);
 }
 
-sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long total_rows, int max_unit_rows,
-                    cudaStream_t st) {
+sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,
+                    long long n_fast_units, int fast_rows, cudaStream_t st) {
   const int G = L->n_q_heads / L->n_kv_heads;
-  a.rows_per_item =
-      choose_rows_per_item(total_rows, max_unit_rows, stage_rows(L->dtype, L->head_dim),
-                           device_sm_count());
+  a.rows_per_item = choose_rows_per_item(n_slow_units, slow_rows, n_fast_units, fast_rows,
+                                         stage_rows(L->dtype, L->head_dim), device_sm_count());
   const cudaError_t e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st)
                                             : launch_attn_bf16(a, L->head_dim, G, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -232,8 +251,8 @@ sfi_status sfi_slow_attn(const sfi_layout* L, const void* q, const void* k, cons
   for (int b = 0; b < L->batch; ++b) a.slow.bits[b >> 5] |= 1u << (b & 31);
   a.emit = (f_out || knorm_out) ? 1 : 0;
   a.knorm = knorm_out;
-  const long long total = (long long)L->batch * L->n_kv_heads * L->max_len;
-  if ((s = run_attn(a, L, total, L->max_len, st)) != SFI_OK) return s;
+  if ((s = run_attn(a, L, (long long)L->batch * L->n_kv_heads, L->max_len, 0, 0, st)) != SFI_OK)
+    return s;
   if (f_out) {
     FpassArgs fa{};
     fa.logits = a.logits;
@@ -309,8 +328,8 @@ sfi_status sfi_fast_attn(const sfi_layout* L, const sfi_params* P, const void* q
   a.n_sink = P->n_sink;
   a.window = P->window;
   const int bound = fast_unit_rows_bound(L, P);
-  const long long total = (long long)L->batch * L->n_kv_heads * bound;
-  return run_attn(a, L, total, bound, static_cast<cudaStream_t>(stream));
+  return run_attn(a, L, 0, 0, (long long)L->batch * L->n_kv_heads, bound,
+                  static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

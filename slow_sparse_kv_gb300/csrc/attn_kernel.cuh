@@ -8,22 +8,29 @@
 // unit and [sinks | selected | window] for a fast one -- so one persistent
 // kernel serves a mixed batch.
 //
-// Design (GB300, HBM-bound matrix-vector work, G = H_q / H_kv query heads per
-// KV head, so no tensor-core contraction):
+// Design (GB300; the step is HBM-bound: G = H_q / H_kv query heads per KV
+// head read every K and V row once):
 //  * the rows of each unit are cut into equal work items; CTAs (one per SM)
 //    walk the items round-robin;
-//  * one producer warp streams K and V rows into a ring of shared-memory
-//    stages with bulk asynchronous copies (cp.async.bulk, completion on
-//    mbarriers): one copy per contiguous stage for dense rows, one 16-byte-
-//    aligned row copy per gathered row for the managed state;
-//  * eight consumer warps each take a slice of every stage: lanes are grouped
-//    LPR = row_bytes / 16 per row, each lane owns 16 bytes of the row, keeps
-//    its slice of the G query vectors in registers, and the per-row dot
-//    products are finished with a transpose-reduce across the group;
-//  * online softmax in the log2 domain (q is pre-scaled by log2(e)/sqrt(d)),
-//    fp32 accumulation of p.v per lane;
-//  * slow units also write their logits ([pos][G], contiguous per warp) and
-//    the key norms, which the evidence pass and the selector read back;
+//  * one producer warp streams K and V rows into a 4-deep ring of shared-
+//    memory stages with completion on mbarriers: every lane copies 16-byte
+//    pieces with cp.async (dense runs and gathered rows alike); fp32 dense
+//    runs use one bulk copy (cp.async.bulk) per stage instead;
+//  * bf16 caches: eight consumer warps, four per stage, 16 rows each.  The
+//    G query vectors sit in registers as the A operand of mma.sync m16n8k16
+//    (rows G..15 zero); S = Q K^T comes from ldmatrix'ed K rows (the stages
+//    are stored with a 16-byte-chunk XOR swizzle so ldmatrix is conflict-
+//    free), the online softmax runs on the accumulator fragments (one head
+//    per lane quad, log2 domain), and P is fed back as the A operand of
+//    O += P V with ldmatrix.trans'ed V rows (fp32 accumulation throughout;
+//    P is rounded to bf16 for the product).  ncu showed the CUDA-core
+//    version spending ~79 warp instructions per 256-byte row, which capped
+//    it at ~60% of HBM bandwidth; the tensor-core path needs ~6;
+//  * fp32 caches (kept exact to 2e-5): eight consumer warps share every
+//    stage on CUDA cores, 16-byte row slices per lane, per-row dots finished
+//    with a transpose-reduce across the lanes of a row;
+//  * slow units also write their logits ([pos][G], log2-scaled) and the key
+//    norms, which the evidence pass and the selector read back;
 //  * the consumer warps merge their states per item; a unit cut into several
 //    items writes per-item partials and the last CTA to finish a unit (an
 //    atomic counter per unit, reset after use) merges them into the output.
@@ -31,22 +38,32 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sfi {
 
 template <typename T, int D, int G>
 struct AttnCfg {
+  static constexpr bool MMA = std::is_same<T, bf16_t>::value;
   static constexpr int ES = sizeof(T);
   static constexpr int ROWB = D * ES;       // bytes per cache row
-  static constexpr int LPR = ROWB / 16;     // lanes per row
-  static constexpr int EPL = 16 / ES;       // elements per lane
-  static constexpr int RPI = 32 / LPR;      // rows per warp-wide 16-byte load
-  static constexpr int R = 4;               // rows per lane group per stage
-  static constexpr int RB = RPI * R;        // rows per warp per stage
+  static constexpr int LPR = ROWB / 16;     // 16-byte chunks (lanes) per row
+  static constexpr int EPL = 16 / ES;       // elements per chunk
+  static constexpr int RPI = 32 / LPR;      // rows per warp-wide 16-byte access
+  static constexpr int R = 4;               // SIMT: rows per lane group per stage
+  static constexpr int RB = RPI * R;        // SIMT: rows per warp per stage
   static constexpr int NCW = 8;             // consumer warps
-  static constexpr int SR = RB * NCW;       // rows per stage
-  static constexpr int NS = 4;              // pipeline depth
+  static constexpr int MW = 16;             // MMA: rows per consumer warp per stage
+  static constexpr int CPS = MMA ? 4 : NCW;  // consumer warps per stage
+  static constexpr int SR = MMA ? MW * CPS : RB * NCW;  // rows per stage
+  // pipeline depth: as many stages as shared memory allows (bytes in flight
+  // per SM are what keeps HBM busy), at most 6
+  static constexpr int NS_FIT =
+      int((227 * 1024 - 2048 - size_t(NCW) * G * (D + 2) * 4 - (size_t(kMaxUnits) + 1) * 4) /
+          (2 * size_t(SR) * ROWB));
+  static constexpr int NS = NS_FIT > 6 ? 6 : (NS_FIT < 2 ? 2 : NS_FIT);
   static constexpr int NT = (NCW + 1) * 32;
   static constexpr int STAGE_B = SR * ROWB;  // bytes of K (or V) per stage
   static constexpr int NE = (RB * G + 31) / 32;
@@ -54,15 +71,24 @@ struct AttnCfg {
   static constexpr int NV = V >= LPR ? V / LPR : 1;
   static_assert(LPR >= 8 && LPR <= 32, "row must be 128..512 bytes");
   static_assert(R < LPR, "norm reduction assumes one value per lane");
+  static_assert(!MMA || G <= 8, "MMA path keeps the heads in rows 0..7 of the tile");
   static constexpr size_t OFF_K = 0;
   static constexpr size_t OFF_V = OFF_K + size_t(NS) * STAGE_B;
   static constexpr size_t OFF_BAR = OFF_V + size_t(NS) * STAGE_B;
-  static constexpr size_t OFF_SL = OFF_BAR + 2 * NS * 8;
-  static constexpr size_t OFF_SN = OFF_SL + size_t(NCW) * RB * G * 4;
-  static constexpr size_t OFF_RED = OFF_SN + size_t(NCW) * RB * 4;
+  static constexpr size_t OFF_SL = OFF_BAR + 2 * NS * 8;                  // SIMT scratch
+  static constexpr size_t OFF_SN = OFF_SL + (MMA ? 0 : size_t(NCW) * RB * G * 4);
+  static constexpr size_t OFF_RED = OFF_SN + (MMA ? 0 : size_t(NCW) * RB * 4);
   static constexpr size_t OFF_MISC = OFF_RED + size_t(NCW) * G * (D + 2) * 4;
   static constexpr size_t OFF_UNITS = OFF_MISC + 64;
   static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1) * 4; }
+  static constexpr bool OFF_UNITS_MAX_CHECK() {
+    return OFF_UNITS + (size_t(kMaxUnits) + 1) * 4 <= size_t(227) * 1024;
+  }
+  static_assert(OFF_UNITS_MAX_CHECK(), "shared memory plan exceeds 227 KB");
+  // byte offset of 16-byte chunk c of stage row r (XOR swizzle on the MMA path)
+  static __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
+    return uint32_t(r * ROWB + ((MMA ? (c ^ (r & 7)) : c) << 4));
+  }
 };
 
 struct ItemInfo {
@@ -151,131 +177,21 @@ __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* u
   return I;
 }
 
+// Consumer warp, CUDA-core path: process this CTA's stages of one item and
+// leave the warp's (max, sum, p.v) state in red.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const AttnArgs a) {
+__device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo& I,
+                                               unsigned char* smem, uint32_t bar_full,
+                                               uint32_t bar_empty, volatile int* abort_flag,
+                                               uint32_t& stage, int warp, int lane, float* red) {
   using C = AttnCfg<T, D, G>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_units = a.B * a.H_kv;
-  int* units = reinterpret_cast<int*>(smem + C::OFF_UNITS);
-  int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
-  const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
-  const uint32_t bar_empty = bar_full + C::NS * 8;
-
-  attn_build_units<C::NT>(a, units, n_units, misc);
-  const int total = units[n_units];
-  if (total > a.max_items) {
-    if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
-    return;
-  }
-  if (blockIdx.x >= total) return;
-  volatile int* abort_flag = misc + 12;
-  if (tid == 0) {
-    *abort_flag = 0;
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
-      mbar_init(bar_empty + 8 * s, C::NCW);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == C::NCW) {
-    // ------------------------------------------------------------ producer
-    const uint64_t pol = l2_evict_first_policy();
-    const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
-    uint32_t stage = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      const ItemInfo I = attn_resolve(a, units, n_units, it);
-      const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
-      const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
-      const char* vb = reinterpret_cast<const char*>(a.v) + head0 * C::ES;
-      const int n = I.n;
-      const int ns = min(a.n_sink, n);
-      const int cnt = I.slow ? 0 : min(max(a.count[I.u], 0), a.idx_stride);
-      const int wlo = max(a.n_sink, n - a.window);
-      const int32_t* ix = I.slow ? nullptr : a.idx + size_t(I.u) * a.idx_stride;
-      for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
-        const int nr = min(C::SR, I.r1 - c0);
-        const int slot = stage % C::NS;
-        const uint32_t ph = (stage / C::NS) & 1u;
-        // cache positions of this stage's rows (lane l: rows l, l + 32, ...)
-        int pos[(C::SR + 31) / 32];
-#pragma unroll
-        for (int j = 0; j < (C::SR + 31) / 32; ++j) {
-          const int r = lane + 32 * j;
-          const int lp = c0 + r;
-          int p = 0;
-          if (!I.slow && r < nr) {
-            if (lp < ns) {
-              p = lp;
-            } else if (lp < ns + cnt) {
-              p = __ldg(ix + (lp - ns));
-              if (p < 0 || p >= n) {
-                set_status(a.status, SFI_DEV_BAD_INDEX);
-                p = 0;
-              }
-            } else {
-              p = wlo + (lp - ns - cnt);
-            }
-          }
-          pos[j] = p;
-        }
-        if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
-        if (I.slow) {
-          // dense rows: one bulk copy of K and one of V for the whole stage
-          if (lane == 0) {
-            mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
-            bulk_g2s(kd, kb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
-            bulk_g2s(vd, vb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
-          } else {
-            mbar_arrive(bar_full + 8 * slot);
-          }
-        } else {
-          // gathered rows: every lane copies 16 bytes of LPR-lane rows; the
-          // row positions were resolved before the wait (pos[]), lane l
-          // holding the rows l, l + 32, ...
-#pragma unroll
-          for (int i = 0; i < C::SR / C::RPI; ++i) {
-            const int r = i * C::RPI + lane / C::LPR;
-            const int p = __shfl_sync(kFull, pos[(i * C::RPI) / 32], r & 31);
-            if (r < nr) {
-              const size_t so = size_t(p) * C::ROWB + (lane % C::LPR) * 16;
-              cp_async16(kd + r * C::ROWB + (lane % C::LPR) * 16, kb + so, pol);
-              cp_async16(vd + r * C::ROWB + (lane % C::LPR) * 16, vb + so, pol);
-            }
-          }
-          cp_async_arrive_noinc(bar_full + 8 * slot);
-        }
-        ++stage;
-      }
-    }
-    // Let every copy that was issued land before the CTA can exit.
-    const uint32_t first = stage > uint32_t(C::NS) ? stage - C::NS : 0u;
-    for (uint32_t s = first; s < stage; ++s) mbar_wait(bar_full + 8 * (s % C::NS), (s / C::NS) & 1u);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
   const int li = lane % C::LPR, lg = lane / C::LPR;
   const int hl = lane % G;  // head of this lane's softmax entries
   float* sl = reinterpret_cast<float*>(smem + C::OFF_SL) + warp * C::RB * G;
   float* sn = reinterpret_cast<float*>(smem + C::OFF_SN) + warp * C::RB;
-  float* red_all = reinterpret_cast<float*>(smem + C::OFF_RED);
   const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
-  const int nct = C::NCW * 32;
-  uint32_t stage = 0;
-
-  for (int it = blockIdx.x; it < total; it += gridDim.x) {
-    const ItemInfo I = attn_resolve(a, units, n_units, it);
-    const bool emit = a.emit && I.slow;
-    const bool emit_norm = emit && a.knorm != nullptr;
-
+  const bool emit = a.emit && I.slow;
+  const bool emit_norm = emit && a.knorm != nullptr;
     float qf[G][C::EPL];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -424,7 +340,6 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const Att
         for (int e = 0; e < C::EPL; ++e) acc[hh][e] += __shfl_xor_sync(kFull, acc[hh][e], o);
 #pragma unroll
     for (int o = G; o < 32; o <<= 1) zl += __shfl_xor_sync(kFull, zl, o);
-    float* red = red_all + warp * G * (D + 2);
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
       if (lane == hh) {
@@ -437,6 +352,306 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const Att
       for (int hh = 0; hh < G; ++hh)
 #pragma unroll
         for (int e = 0; e < C::EPL; ++e) red[hh * (D + 2) + 2 + li * C::EPL + e] = acc[hh][e];
+    }
+}
+
+// Consumer warp, tensor-core path (bf16): warp `warp` takes rows
+// [16 * (warp % 4), +16) of every stage whose index has parity warp / 4.
+template <int D, int G>
+__device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo& I,
+                                              unsigned char* smem, uint32_t bar_full,
+                                              uint32_t bar_empty, volatile int* abort_flag,
+                                              uint32_t& stage, int warp, int lane, float* red) {
+  using C = AttnCfg<bf16_t, D, G>;
+  constexpr int KS = D / 16;  // k-steps of QK
+  constexpr int NTD = D / 8;  // 8-column output tiles of PV
+  const int g4 = lane >> 2, t4 = lane & 3;
+  const int wslot = warp & 3, wpar = warp >> 2;
+  const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
+  const bool emit = a.emit && I.slow;
+  const bool emit_norm = emit && a.knorm != nullptr;
+  const float qs = a.qscale;
+
+  // A operand: q of head g4 (zero for padding heads), bf16 pairs.
+  uint32_t qa[KS][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(a.q) +
+                           ((size_t(I.b) * a.H_q + size_t(I.g) * G + (g4 < G ? g4 : 0)) * D) / 2;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = g4 < G ? __ldg(qrow + ks * 8 + t4) : 0u;
+      qa[ks][1] = g4 < G ? __ldg(qrow + ks * 8 + 4 + t4) : 0u;
+    }
+  }
+  float acc[NTD][2];
+#pragma unroll
+  for (int c = 0; c < NTD; ++c) acc[c][0] = acc[c][1] = 0.f;
+  float m = -INFINITY, zl = 0.f;
+
+  for (int c0 = I.r0; c0 < I.r1; c0 += C::SR, ++stage) {
+    if (int(stage & 1u) != wpar) continue;
+    const int nr = min(C::SR, I.r1 - c0);
+    const int slot = stage % C::NS;
+    const uint32_t ph = (stage / C::NS) & 1u;
+    const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
+    const int r0 = wslot * C::MW;
+    const int nw = min(C::MW, nr - r0);  // valid rows of this warp (may be <= 0)
+    if (have && nw > 0) {
+      const uint32_t kst = kbase + slot * C::STAGE_B;
+      const uint32_t vst = vbase + slot * C::STAGE_B;
+      // ---- S = Q K^T over the warp's 16 rows (two 8-row column tiles)
+      float sacc[2][2];
+      float nsq[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = 0.f;
+        const int row = r0 + nt * 8 + (lane & 7);
+#pragma unroll
+        for (int kp = 0; kp < KS / 2; ++kp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kst + C::chunk_off(row, kp * 4 + (lane >> 3)), b0, b1, b2, b3);
+          mma_bf16_top8(sacc[nt][0], sacc[nt][1], qa[2 * kp][0], qa[2 * kp][1], b0, b1);
+          mma_bf16_top8(sacc[nt][0], sacc[nt][1], qa[2 * kp + 1][0], qa[2 * kp + 1][1], b2, b3);
+          if (emit_norm) {
+            const uint32_t bb[4] = {b0, b1, b2, b3};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = __uint_as_float(bb[j] << 16), hi = __uint_as_float(bb[j] & 0xffff0000u);
+              nsq[nt] = fmaf(lo, lo, fmaf(hi, hi, nsq[nt]));
+            }
+          }
+        }
+      }
+      // this lane's logits: head g4, rows r0 + 8 nt + 2 t4 + j (log2 domain)
+      float l[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int rr = nt * 8 + 2 * t4 + j;
+          l[nt * 2 + j] = rr < nw ? sacc[nt][j] * qs : -INFINITY;
+        }
+      if (emit) {
+        if (g4 < G) {
+          float* lo = a.logits + (size_t(I.u) * a.max_len + c0 + r0) * G + g4;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int rr = nt * 8 + 2 * t4 + j;
+              if (rr < nw) lo[rr * G] = l[nt * 2 + j];
+            }
+        }
+        if (emit_norm) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            float v = nsq[nt];
+            v += __shfl_xor_sync(kFull, v, 1);
+            v += __shfl_xor_sync(kFull, v, 2);
+            const int rr = nt * 8 + g4;
+            if (t4 == 0 && rr < nw) a.knorm[size_t(I.u) * a.max_len + c0 + r0 + rr] = sqrtf(v);
+          }
+        }
+      }
+      // ---- online softmax for head g4 (the quad shares the head)
+      float tmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
+      if (tmax > m) {
+        const float al = exp2f(m - tmax);
+#pragma unroll
+        for (int c = 0; c < NTD; ++c) {
+          acc[c][0] *= al;
+          acc[c][1] *= al;
+        }
+        zl *= al;
+        m = tmax;
+      }
+      float p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        p[j] = exp2f(l[j] - m);
+        zl += p[j];
+      }
+      const uint32_t pa_lo = pack_bf16x2(p[0], p[1]);  // rows 2t4, 2t4+1
+      const uint32_t pa_hi = pack_bf16x2(p[2], p[3]);  // rows 8+2t4, 9+2t4
+      // rows past the valid ones hold stale or unset data: zero their V
+      uint32_t m_lo = 0xffffffffu, m_hi = 0xffffffffu;
+      if (nw < C::MW) {
+        m_lo = (2 * t4 < nw ? 0x0000ffffu : 0u) | (2 * t4 + 1 < nw ? 0xffff0000u : 0u);
+        m_hi = (8 + 2 * t4 < nw ? 0x0000ffffu : 0u) | (9 + 2 * t4 < nw ? 0xffff0000u : 0u);
+      }
+      // ---- O += P V
+      const int vrow = r0 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(vst + C::chunk_off(vrow, 2 * dp + (lane >> 4)), b0, b1, b2, b3);
+        b0 &= m_lo;
+        b1 &= m_hi;
+        b2 &= m_lo;
+        b3 &= m_hi;
+        mma_bf16_top8(acc[2 * dp][0], acc[2 * dp][1], pa_lo, pa_hi, b0, b1);
+        mma_bf16_top8(acc[2 * dp + 1][0], acc[2 * dp + 1][1], pa_lo, pa_hi, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+  }
+  // ---- warp state: one head per quad
+  zl += __shfl_xor_sync(kFull, zl, 1);
+  zl += __shfl_xor_sync(kFull, zl, 2);
+  if (g4 < G) {
+    float* rw = red + g4 * (D + 2);
+    if (t4 == 0) {
+      rw[0] = m;
+      rw[1] = zl;
+    }
+#pragma unroll
+    for (int c = 0; c < NTD; ++c) {
+      rw[2 + 8 * c + 2 * t4] = acc[c][0];
+      rw[2 + 8 * c + 2 * t4 + 1] = acc[c][1];
+    }
+  }
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const AttnArgs a) {
+  using C = AttnCfg<T, D, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_units = a.B * a.H_kv;
+  int* units = reinterpret_cast<int*>(smem + C::OFF_UNITS);
+  int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
+  const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
+  const uint32_t bar_empty = bar_full + C::NS * 8;
+
+  attn_build_units<C::NT>(a, units, n_units, misc);
+  const int total = units[n_units];
+  if (total > a.max_items) {
+    if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
+    return;
+  }
+  if (blockIdx.x >= total) return;
+  volatile int* abort_flag = misc + 12;
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
+      mbar_init(bar_empty + 8 * s, C::CPS);  // one arrival per consuming warp
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == C::NCW) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = l2_evict_first_policy();
+    const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
+    uint32_t stage = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      const ItemInfo I = attn_resolve(a, units, n_units, it);
+      const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
+      const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
+      const char* vb = reinterpret_cast<const char*>(a.v) + head0 * C::ES;
+      const int n = I.n;
+      const int ns = min(a.n_sink, n);
+      const int cnt = I.slow ? 0 : min(max(a.count[I.u], 0), a.idx_stride);
+      const int wlo = max(a.n_sink, n - a.window);
+      const int32_t* ix = I.slow ? nullptr : a.idx + size_t(I.u) * a.idx_stride;
+      // Row positions of stage c0 (lane l: rows l, l + 32, ...).  Gathered
+      // positions come from the index list in global memory, so the loads
+      // for the next stage are issued one stage ahead of their use.
+      auto resolve_pos = [&](int c0s, int (&out)[(C::SR + 31) / 32]) {
+        const int nrs = min(C::SR, I.r1 - c0s);
+#pragma unroll
+        for (int j = 0; j < (C::SR + 31) / 32; ++j) {
+          const int r = lane + 32 * j;
+          const int lp = c0s + r;
+          int p = I.slow ? lp : 0;  // rows past the stage are never copied
+          if (!I.slow && r < nrs) {
+            if (lp < ns) {
+              p = lp;
+            } else if (lp < ns + cnt) {
+              p = __ldg(ix + (lp - ns));
+            } else {
+              p = wlo + (lp - ns - cnt);
+            }
+          }
+          out[j] = p;
+        }
+      };
+      int pos_next[(C::SR + 31) / 32];
+      resolve_pos(I.r0, pos_next);
+      for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
+        const int nr = min(C::SR, I.r1 - c0);
+        const int slot = stage % C::NS;
+        const uint32_t ph = (stage / C::NS) & 1u;
+        int pos[(C::SR + 31) / 32];
+#pragma unroll
+        for (int j = 0; j < (C::SR + 31) / 32; ++j) {
+          int p = pos_next[j];
+          if (!I.slow && (p < 0 || p >= n)) {
+            set_status(a.status, SFI_DEV_BAD_INDEX);
+            p = 0;
+          }
+          pos[j] = p;
+        }
+        if (c0 + C::SR < I.r1) resolve_pos(c0 + C::SR, pos_next);
+        if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
+        if (!C::MMA && I.slow) {
+          // dense rows: one bulk copy of K and one of V for the whole stage
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
+            bulk_g2s(kd, kb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
+            bulk_g2s(vd, vb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
+          } else {
+            mbar_arrive(bar_full + 8 * slot);
+          }
+        } else {
+          // row by row: every lane copies one 16-byte chunk of a row; the
+          // row positions were resolved before the wait (pos[]), lane l
+          // holding the rows l, l + 32, ...
+#pragma unroll
+          for (int i = 0; i < C::SR / C::RPI; ++i) {
+            const int r = i * C::RPI + lane / C::LPR;
+            const int c = lane % C::LPR;
+            const int p = __shfl_sync(kFull, pos[(i * C::RPI) / 32], r & 31);
+            if (r < nr) {
+              const size_t so = size_t(p) * C::ROWB + c * 16;
+              cp_async16(kd + C::chunk_off(r, c), kb + so, pol);
+              cp_async16(vd + C::chunk_off(r, c), vb + so, pol);
+            }
+          }
+          cp_async_arrive_noinc(bar_full + 8 * slot);
+        }
+        ++stage;
+      }
+    }
+    // Let every copy that was issued land before the CTA can exit.
+    const uint32_t first = stage > uint32_t(C::NS) ? stage - C::NS : 0u;
+    for (uint32_t s = first; s < stage; ++s) mbar_wait(bar_full + 8 * (s % C::NS), (s / C::NS) & 1u);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  float* red_all = reinterpret_cast<float*>(smem + C::OFF_RED);
+  const int nct = C::NCW * 32;
+  uint32_t stage = 0;
+
+  for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    const ItemInfo I = attn_resolve(a, units, n_units, it);
+    const bool emit = a.emit && I.slow;
+    float* red = red_all + warp * G * (D + 2);
+    if constexpr (C::MMA) {
+      attn_item_mma<D, G>(a, I, smem, bar_full, bar_empty, abort_flag, stage, warp, lane, red);
+    } else {
+      attn_item_simt<T, D, G>(a, I, smem, bar_full, bar_empty, abort_flag, stage, warp, lane, red);
     }
     named_bar_sync(1, nct);
 
@@ -480,15 +695,25 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const Att
         __threadfence();
         for (int j = tid; j < G * D; j += nct) {
           const int hh = j / D, dim = j % D;
-          float M = -INFINITY, A = 0.f, Z = 0.f;
-          for (int i = 0; i < I.n_items; ++i) {
-            const float* p = a.partials + (size_t(I.first + i) * G + hh) * (D + 2);
-            const float pm = __ldcg(p), pz = __ldcg(p + 1), pa = __ldcg(p + 2 + dim);
-            const float M2 = fmaxf(M, pm);
-            const float s0 = exp2f(M - M2), s1 = exp2f(pm - M2);
-            A = A * s0 + pa * s1;
-            Z = Z * s0 + pz * s1;
-            M = M2;
+          const float* pbase = a.partials + (size_t(I.first) * G + hh) * (D + 2);
+          const size_t pstride = size_t(G) * (D + 2);
+          // pass 1: the global max (independent loads)
+          float M = -INFINITY;
+          int i = 0;
+          for (; i + 4 <= I.n_items; i += 4) {
+            const float m0 = __ldcg(pbase + (i + 0) * pstride), m1 = __ldcg(pbase + (i + 1) * pstride);
+            const float m2 = __ldcg(pbase + (i + 2) * pstride), m3 = __ldcg(pbase + (i + 3) * pstride);
+            M = fmaxf(M, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+          }
+          for (; i < I.n_items; ++i) M = fmaxf(M, __ldcg(pbase + i * pstride));
+          // pass 2: rescaled sums
+          float A = 0.f, Z = 0.f;
+#pragma unroll 4
+          for (i = 0; i < I.n_items; ++i) {
+            const float* p = pbase + i * pstride;
+            const float sc = exp2f(__ldcg(p) - M);
+            Z = fmaf(__ldcg(p + 1), sc, Z);
+            A = fmaf(__ldcg(p + 2 + dim), sc, A);
           }
           const size_t qh = size_t(I.b) * a.H_q + size_t(I.g) * G + hh;
           a.out[qh * D + dim] = A / Z;

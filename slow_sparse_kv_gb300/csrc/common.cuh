@@ -130,6 +130,45 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// ldmatrix: four 8x8 b16 matrices; lanes 8j..8j+7 give the row addresses of
+// matrix j, register j receives this lane's two elements of matrix j.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A * B + D for one m16n8k16 bf16 tile with fp32 accumulation, where rows
+// 8..15 of A are zero: a0 holds A[g][2t..2t+1], a2 holds A[g][2t+8..2t+9]
+// (g = lane / 4, t = lane % 4); d0, d1 are D[g][2t..2t+1].  Rows 8..15 of D
+// are not kept.
+__device__ __forceinline__ void mma_bf16_top8(float& d0, float& d1, uint32_t a0, uint32_t a2,
+                                              uint32_t b0, uint32_t b1) {
+  float x2, x3;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d0), "=f"(d1), "=f"(x2), "=f"(x3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(0.f),
+        "f"(0.f));
+  (void)x2;
+  (void)x3;
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // 16 bytes of storage -> fp32 elements.
 template <typename T>
 struct Unpack;

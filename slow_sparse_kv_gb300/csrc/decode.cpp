@@ -266,13 +266,12 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   a.n_sink = d.params.n_sink;
   a.window = d.params.window;
   const int fast_bound = fast_unit_rows_bound(&Lc, &d.params);
-  const long long total = (long long)d.n_kv_heads *
-                          ((long long)n_slow * d.max_len + (long long)(d.batch - n_slow) * fast_bound);
-  const int max_unit = n_slow ? d.max_len : fast_bound;
   cudaError_t e = cudaSuccess;
   if (c->profiling) e = record_pair(c->ev_attn, c->n_attn_pending, c->attn_ms, false, st);
   if (e != cudaSuccess) return cuda_fail(e, "profiling event");
-  if ((s = run_attn(a, &Lc, total, max_unit, st)) != SFI_OK) return s;
+  if ((s = run_attn(a, &Lc, (long long)n_slow * d.n_kv_heads, d.max_len,
+                    (long long)(d.batch - n_slow) * d.n_kv_heads, fast_bound, st)) != SFI_OK)
+    return s;
   if (c->profiling) {
     e = record_pair(c->ev_attn, c->n_attn_pending, c->attn_ms, true, st);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");

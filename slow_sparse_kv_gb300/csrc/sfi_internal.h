@@ -97,8 +97,8 @@ sfi_status check_layout(const sfi_layout* L);
 sfi_status check_params(const sfi_params* P, bool for_select);
 void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const void* k,
                       const void* v, float* out, char* ws, const WsPlan& p);
-sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long total_rows, int max_unit_rows,
-                    cudaStream_t st);
+sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,
+                    long long n_fast_units, int fast_rows, cudaStream_t st);
 int fast_unit_rows_bound(const sfi_layout* L, const sfi_params* P);
 sfi_status fail(sfi_status s, const char* fmt, ...);
 sfi_status cuda_fail(cudaError_t e, const char* what);

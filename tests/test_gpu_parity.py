@@ -112,7 +112,8 @@ def test_fast_all_positions_equals_dense(sfi):
     out2 = torch.empty_like(torch.from_numpy(out)).cuda()
     sfi.sfi_fast_attn(lay, prm, qd, dl.k, dl.v, idx, cnt, out2, ws)
     torch.cuda.synchronize()
-    assert float((out2.cpu() - torch.from_numpy(out)).abs().max()) <= 1e-5
+    # same rows, different split points and P rounding: equal within the bf16 parity bar
+    assert float((out2.cpu() - torch.from_numpy(out)).abs().max()) <= O_TOL["bf16"]
 
 
 def test_ties_go_to_lower_positions(sfi):
