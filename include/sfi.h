@@ -175,6 +175,36 @@ sfi_status sfi_fast_attn(const sfi_layout* layout, const sfi_params* params,
                          const int32_t* idx, const int32_t* count, float* out,
                          void* ws, size_t ws_bytes, sfi_stream stream);
 
+/* ---------------------------------------------------------------- Vegas verify */
+
+/* Verification attention with collected logit sums (Vegas, gist.science
+ * 2602.07223: section 2 "Verification phase" -- dense attention with the
+ * gamma + 1 rows of the draft chain; section 2.A -- the selected prefix set
+ * maximises the attention logits summed over the collected rows and all
+ * query heads; section 2.B "Collect-2-Query" -- collect only the first draft
+ * row and the bonus row).
+ *
+ * n_b = len[b] includes the n_rows chain tokens; the prefix is
+ * P = [0, n_b - n_rows).  Row t (0 <= t < n_rows) of sequence b sits at
+ * position n_b - n_rows + t and attends to [0, n_b - n_rows + t]:
+ *   out[b][t][h] = softmax-weighted sum of v over those positions (fp32).
+ * If logitsum_out is not NULL, for every KV head g and prefix position i:
+ *   logitsum_out[b][g][i] = sum over t in collect_rows, h in group g of
+ *                           q_{t,h} . k_{g,i} / sqrt(d)      (natural units);
+ * summing those rows over g gives the aggregated logits the selector's
+ * SFI_SELECT_LOGIT_SUM_SEQ mode ranks (with window = n_rows, n_sink = 0).
+ * q: [B][n_rows][H_q][d] bf16; out: [B][n_rows][H_q][d] fp32;
+ * collect_rows: host array of n_collect distinct rows.
+ * Limits (SFI_ERR_UNSUPPORTED beyond them): bf16 only; n_rows <= 8;
+ * n_rows * G <= 32; n_collect * G <= 16.  The workspace is sized by
+ * sfi_verify_attn_workspace_size (it holds n_rows * G partial rows per
+ * work item). */
+size_t sfi_verify_attn_workspace_size(const sfi_layout* layout, int32_t n_rows);
+sfi_status sfi_verify_attn(const sfi_layout* layout, int32_t n_rows, const int32_t* collect_rows,
+                           int32_t n_collect, const void* q, const void* k, const void* v,
+                           float* out, float* logitsum_out, void* ws, size_t ws_bytes,
+                           sfi_stream stream);
+
 /* Fast step that allocates nothing and takes no workspace.  The pages have
  * no counterpart to this call; it exists for callers that may not allocate
  * device memory on the path that runs the step -- for example a plug-in

@@ -60,6 +60,9 @@ EXPORTS = {
     "sfi_fast_attn_workspace_size": (c_size_t, [_L, _P]),
     "sfi_fast_attn": (c_int32, [_L, _P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "sfi_verify_attn_workspace_size": (c_size_t, [_L, c_int32]),
+    "sfi_verify_attn": (c_int32, [_L, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "sfi_fast_attn_noalloc": (c_int32, [_L, _P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_void_p]),
     "sfi_ctx_create": (c_int32, [POINTER(sfi_ctx_desc), POINTER(c_void_p)]),
@@ -206,6 +209,25 @@ def sfi_schedule(is_boundary, have_sel, since, budget: int):
     _check("sfi_schedule", lib.sfi_schedule(B, int(budget), ib.ctypes.data, have_sel.ctypes.data,
                                             since.ctypes.data, out.ctypes.data))
     return out
+
+
+def verify_workspace(layout: Layout, n_rows: int) -> torch.Tensor:
+    """A zero-filled workspace for sfi_verify_attn with n_rows chain rows."""
+    c = layout.c
+    n = int(lib.sfi_verify_attn_workspace_size(ctypes.byref(c), int(n_rows)))
+    if n == 0:
+        raise SfiError("sfi_verify_attn_workspace_size", SFI_ERR_INVALID_ARG)
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def sfi_verify_attn(layout: Layout, n_rows: int, collect_rows, q, k, v, out, logitsum_out=None,
+                    ws=None, stream=None):
+    rows = list(collect_rows or [])
+    arr = (c_int32 * max(1, len(rows)))(*rows)
+    c = layout.c
+    _check("sfi_verify_attn", lib.sfi_verify_attn(
+        ctypes.byref(c), int(n_rows), arr, len(rows), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+        _ptr(logitsum_out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def sfi_fast_attn_noalloc(layout: Layout, prm: sfi_params, q, k, v, idx, count, out, stream=None):

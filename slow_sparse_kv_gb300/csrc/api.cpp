@@ -332,4 +332,67 @@ sfi_status sfi_fast_attn(const sfi_layout* L, const sfi_params* P, const void* q
                   static_cast<cudaStream_t>(stream));
 }
 
+size_t sfi_verify_attn_workspace_size(const sfi_layout* L, int32_t n_rows) {
+  if (check_layout(L) != SFI_OK || n_rows < 1 || n_rows > 8) return 0;
+  return plan_workspace(L->batch, L->n_kv_heads * n_rows * (L->n_q_heads / L->n_kv_heads),
+                        L->n_kv_heads, L->head_dim, L->max_len)
+      .total;
+}
+
+sfi_status sfi_verify_attn(const sfi_layout* L, int32_t n_rows, const int32_t* collect_rows,
+                           int32_t n_collect, const void* q, const void* k, const void* v,
+                           float* out, float* logitsum_out, void* ws, size_t ws_bytes,
+                           sfi_stream stream) {
+  sfi_status s = check_layout(L);
+  if (s != SFI_OK) return s;
+  if (!q || !k || !v || !out) return fail(SFI_ERR_INVALID_ARG, "q, k, v and out must be set");
+  if (L->dtype != SFI_BF16) return fail(SFI_ERR_UNSUPPORTED, "verify attention takes bf16 caches");
+  const int G = L->n_q_heads / L->n_kv_heads;
+  if (n_rows < 1 || n_rows > 8 || n_rows * G > 32)
+    return fail(SFI_ERR_UNSUPPORTED, "verify rows: need 1 <= n_rows <= 8 and n_rows * G <= 32 (got %d, G %d)",
+                n_rows, G);
+  int8_t order[8];
+  int n_ord = 0;
+  bool used[8] = {false, false, false, false, false, false, false, false};
+  if (logitsum_out) {
+    if (n_collect < 0 || n_collect > n_rows || (n_collect > 0 && !collect_rows))
+      return fail(SFI_ERR_INVALID_ARG, "collect_rows must list 0..n_rows distinct rows");
+    if (n_collect * G > 16)
+      return fail(SFI_ERR_UNSUPPORTED, "n_collect * G must be <= 16 (got %d)", n_collect * G);
+    for (int i = 0; i < n_collect; ++i) {
+      const int t = collect_rows[i];
+      if (t < 0 || t >= n_rows || used[t])
+        return fail(SFI_ERR_INVALID_ARG, "collect row %d invalid or repeated", t);
+      used[t] = true;
+      order[n_ord++] = int8_t(t);
+    }
+  } else {
+    n_collect = 0;
+  }
+  for (int t = 0; t < n_rows; ++t)
+    if (!used[t]) order[n_ord++] = int8_t(t);
+  const int QR = n_rows * G;
+  const WsPlan p = plan_workspace(L->batch, L->n_kv_heads * QR, L->n_kv_heads, L->head_dim, L->max_len);
+  if (!ws) return fail(SFI_ERR_WORKSPACE, "workspace is NULL");
+  if (ws_bytes < p.total)
+    return fail(SFI_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu required",
+                ws_bytes, p.total);
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+    return fail(SFI_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  VerifyArgs va;
+  std::memset(&va, 0, sizeof(va));
+  fill_attn_common(va.base, L, q, k, v, out, static_cast<char*>(ws), p);
+  for (int b = 0; b < L->batch; ++b) va.base.slow.bits[b >> 5] |= 1u << (b & 31);
+  va.base.rows_per_item = choose_rows_per_item((long long)L->batch * L->n_kv_heads, L->max_len, 0,
+                                               0, verify_stage_rows(), device_sm_count());
+  va.R = n_rows;
+  va.ncg = n_collect * G;
+  for (int i = 0; i < n_ord; ++i) va.t_of_slot[i] = order[i];
+  va.lsum = logitsum_out;
+  va.lscale = float(1.0 / std::sqrt(double(L->head_dim)));
+  const cudaError_t e = launch_verify(va, L->head_dim, G, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "verify attention launch");
+  return SFI_OK;
+}
+
 }  // extern "C"

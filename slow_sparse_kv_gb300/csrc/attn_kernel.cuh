@@ -47,6 +47,7 @@ namespace sfi {
 template <typename T, int D, int G>
 struct AttnCfg {
   static constexpr bool MMA = std::is_same<T, bf16_t>::value;
+  static constexpr int DIM = D;
   static constexpr int ES = sizeof(T);
   static constexpr int ROWB = D * ES;       // bytes per cache row
   static constexpr int LPR = ROWB / 16;     // 16-byte chunks (lanes) per row
@@ -175,6 +176,109 @@ __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* u
   I.n = a.len[I.b];
   I.slow = seq_is_slow(a.slow, I.b);
   return I;
+}
+
+// Producer warp: walks this CTA's items in order and fills the stage ring.
+// Dense rows and gathered rows are copied the same way: each lane moves
+// 16-byte chunks with cp.async (XOR-swizzled destination on the tensor-core
+// path) and arrives on the stage's mbarrier when its copies land; fp32 dense
+// stages use one bulk copy per operand instead.
+template <class C>
+__device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units, int n_units,
+                                             int total, unsigned char* smem, uint32_t bar_full,
+                                             uint32_t bar_empty, volatile int* abort_flag,
+                                             int lane) {
+  constexpr int D = C::DIM;
+  const uint64_t pol = l2_evict_first_policy();
+  const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
+  uint32_t stage = 0;
+  bool ok = true;
+  for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+    const ItemInfo I = attn_resolve(a, units, n_units, it);
+    const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
+    const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
+    const char* vb = reinterpret_cast<const char*>(a.v) + head0 * C::ES;
+    const int n = I.n;
+    const int ns = min(a.n_sink, n);
+    const int cnt = I.slow ? 0 : min(max(a.count[I.u], 0), a.idx_stride);
+    const int wlo = max(a.n_sink, n - a.window);
+    const int32_t* ix = I.slow ? nullptr : a.idx + size_t(I.u) * a.idx_stride;
+    // Row positions of stage c0 (lane l: rows l, l + 32, ...).  Gathered
+    // positions come from the index list in global memory, so the loads
+    // for the next stage are issued one stage ahead of their use.
+    auto resolve_pos = [&](int c0s, int (&out)[(C::SR + 31) / 32]) {
+      const int nrs = min(C::SR, I.r1 - c0s);
+#pragma unroll
+      for (int j = 0; j < (C::SR + 31) / 32; ++j) {
+        const int r = lane + 32 * j;
+        const int lp = c0s + r;
+        int p = I.slow ? lp : 0;  // rows past the stage are never copied
+        if (!I.slow && r < nrs) {
+          if (lp < ns) {
+            p = lp;
+          } else if (lp < ns + cnt) {
+            p = __ldg(ix + (lp - ns));
+          } else {
+            p = wlo + (lp - ns - cnt);
+          }
+        }
+        out[j] = p;
+      }
+    };
+    int pos_next[(C::SR + 31) / 32];
+    resolve_pos(I.r0, pos_next);
+    for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
+      const int nr = min(C::SR, I.r1 - c0);
+      const int slot = stage % C::NS;
+      const uint32_t ph = (stage / C::NS) & 1u;
+      int pos[(C::SR + 31) / 32];
+#pragma unroll
+      for (int j = 0; j < (C::SR + 31) / 32; ++j) {
+        int p = pos_next[j];
+        if (!I.slow && (p < 0 || p >= n)) {
+          set_status(a.status, SFI_DEV_BAD_INDEX);
+          p = 0;
+        }
+        pos[j] = p;
+      }
+      if (c0 + C::SR < I.r1) resolve_pos(c0 + C::SR, pos_next);
+      if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
+      if (!C::MMA && I.slow) {
+        // dense rows: one bulk copy of K and one of V for the whole stage
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
+          bulk_g2s(kd, kb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
+          bulk_g2s(vd, vb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
+        } else {
+          mbar_arrive(bar_full + 8 * slot);
+        }
+      } else {
+        // row by row: every lane copies one 16-byte chunk of a row; the
+        // row positions were resolved before the wait (pos[]), lane l
+        // holding the rows l, l + 32, ...
+#pragma unroll
+        for (int i = 0; i < C::SR / C::RPI; ++i) {
+          const int r = i * C::RPI + lane / C::LPR;
+          const int c = lane % C::LPR;
+          const int p = __shfl_sync(kFull, pos[(i * C::RPI) / 32], r & 31);
+          if (r < nr) {
+            const size_t so = size_t(p) * C::ROWB + c * 16;
+            cp_async16(kd + C::chunk_off(r, c), kb + so, pol);
+            cp_async16(vd + C::chunk_off(r, c), vb + so, pol);
+          }
+        }
+        cp_async_arrive_noinc(bar_full + 8 * slot);
+      }
+      ++stage;
+    }
+  }
+  // Let every copy that was issued land before the CTA can exit.
+  const uint32_t first = stage > uint32_t(C::NS) ? stage - C::NS : 0u;
+  for (uint32_t s = first; s < stage; ++s) mbar_wait(bar_full + 8 * (s % C::NS), (s / C::NS) & 1u);
 }
 
 // Consumer warp, CUDA-core path: process this CTA's stages of one item and
@@ -545,97 +649,7 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const Att
   __syncthreads();
 
   if (warp == C::NCW) {
-    // ------------------------------------------------------------ producer
-    const uint64_t pol = l2_evict_first_policy();
-    const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
-    uint32_t stage = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      const ItemInfo I = attn_resolve(a, units, n_units, it);
-      const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
-      const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
-      const char* vb = reinterpret_cast<const char*>(a.v) + head0 * C::ES;
-      const int n = I.n;
-      const int ns = min(a.n_sink, n);
-      const int cnt = I.slow ? 0 : min(max(a.count[I.u], 0), a.idx_stride);
-      const int wlo = max(a.n_sink, n - a.window);
-      const int32_t* ix = I.slow ? nullptr : a.idx + size_t(I.u) * a.idx_stride;
-      // Row positions of stage c0 (lane l: rows l, l + 32, ...).  Gathered
-      // positions come from the index list in global memory, so the loads
-      // for the next stage are issued one stage ahead of their use.
-      auto resolve_pos = [&](int c0s, int (&out)[(C::SR + 31) / 32]) {
-        const int nrs = min(C::SR, I.r1 - c0s);
-#pragma unroll
-        for (int j = 0; j < (C::SR + 31) / 32; ++j) {
-          const int r = lane + 32 * j;
-          const int lp = c0s + r;
-          int p = I.slow ? lp : 0;  // rows past the stage are never copied
-          if (!I.slow && r < nrs) {
-            if (lp < ns) {
-              p = lp;
-            } else if (lp < ns + cnt) {
-              p = __ldg(ix + (lp - ns));
-            } else {
-              p = wlo + (lp - ns - cnt);
-            }
-          }
-          out[j] = p;
-        }
-      };
-      int pos_next[(C::SR + 31) / 32];
-      resolve_pos(I.r0, pos_next);
-      for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
-        const int nr = min(C::SR, I.r1 - c0);
-        const int slot = stage % C::NS;
-        const uint32_t ph = (stage / C::NS) & 1u;
-        int pos[(C::SR + 31) / 32];
-#pragma unroll
-        for (int j = 0; j < (C::SR + 31) / 32; ++j) {
-          int p = pos_next[j];
-          if (!I.slow && (p < 0 || p >= n)) {
-            set_status(a.status, SFI_DEV_BAD_INDEX);
-            p = 0;
-          }
-          pos[j] = p;
-        }
-        if (c0 + C::SR < I.r1) resolve_pos(c0 + C::SR, pos_next);
-        if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
-        if (!C::MMA && I.slow) {
-          // dense rows: one bulk copy of K and one of V for the whole stage
-          if (lane == 0) {
-            mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
-            bulk_g2s(kd, kb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
-            bulk_g2s(vd, vb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
-          } else {
-            mbar_arrive(bar_full + 8 * slot);
-          }
-        } else {
-          // row by row: every lane copies one 16-byte chunk of a row; the
-          // row positions were resolved before the wait (pos[]), lane l
-          // holding the rows l, l + 32, ...
-#pragma unroll
-          for (int i = 0; i < C::SR / C::RPI; ++i) {
-            const int r = i * C::RPI + lane / C::LPR;
-            const int c = lane % C::LPR;
-            const int p = __shfl_sync(kFull, pos[(i * C::RPI) / 32], r & 31);
-            if (r < nr) {
-              const size_t so = size_t(p) * C::ROWB + c * 16;
-              cp_async16(kd + C::chunk_off(r, c), kb + so, pol);
-              cp_async16(vd + C::chunk_off(r, c), vb + so, pol);
-            }
-          }
-          cp_async_arrive_noinc(bar_full + 8 * slot);
-        }
-        ++stage;
-      }
-    }
-    // Let every copy that was issued land before the CTA can exit.
-    const uint32_t first = stage > uint32_t(C::NS) ? stage - C::NS : 0u;
-    for (uint32_t s = first; s < stage; ++s) mbar_wait(bar_full + 8 * (s % C::NS), (s / C::NS) & 1u);
+    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, abort_flag, lane);
     return;
   }
 

@@ -33,9 +33,51 @@ constexpr int kFpassThreads = 256;
 constexpr int kSelCluster = 8;   // CTAs per unit
 constexpr int kSelCT = 512;      // threads per selector CTA
 
+constexpr int kSelU = 8;         // positions in flight per selector thread
+constexpr int kRadixPasses = 3;  // digits of 11, 11 and 10 bits
+constexpr int kRadixBins = 2048;
+constexpr int kRadixShift0 = 21;
+constexpr int kRadixShift1 = 10;
+
+// Eight consecutive scores sc[o .. o+7] (o a multiple of 8, scores past `lim`
+// read as 0); two 16-byte shared-memory loads when the block is in range.
+__device__ __forceinline__ void load8(const float* sc, int o, int lim, float (&v)[8]) {
+  if (o + 8 <= lim) {
+    const float4 a = *reinterpret_cast<const float4*>(sc + o);
+    const float4 b = *reinterpret_cast<const float4*>(sc + o + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = o + j < lim ? sc[o + j] : 0.f;
+  }
+}
+
+// The G logits of one position ([pos][G] rows are 4*G-byte aligned).
+template <int G>
+__device__ __forceinline__ void load_row(const float* p, float (&l)[G]) {
+  if constexpr (G % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < G; j += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(p + j);
+      l[j] = x.x;
+      l[j + 1] = x.y;
+      l[j + 2] = x.z;
+      l[j + 3] = x.w;
+    }
+  } else if constexpr (G == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(p);
+    l[0] = x.x;
+    l[1] = x.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < G; ++j) l[j] = p[j];
+  }
+}
+
 // f_i = (1/G) sum_h 2^(l_{h,i} - M_h) / Z_h, from log2-scaled logits.
 template <int G>
-__device__ __forceinline__ float evidence_from_logits(const float* l, const float (&M)[G],
+__device__ __forceinline__ float evidence_from_logits(const float (&l)[G], const float (&M)[G],
                                                       const float (&iz)[G]) {
   float acc = 0.f;
 #pragma unroll
@@ -60,7 +102,9 @@ __global__ void __launch_bounds__(kFpassThreads) fpass_kernel(const FpassArgs a)
   const float* lrow = a.logits + size_t(u) * a.max_len * G;
   float* frow = a.f + size_t(u) * a.max_len;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    frow[i] = evidence_from_logits<G>(lrow + size_t(i) * G, M, iz);
+    float l[G];
+    load_row<G>(lrow + size_t(i) * G, l);
+    frow[i] = evidence_from_logits<G>(l, M, iz);
   }
 }
 
@@ -98,17 +142,14 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool acti
 }
 
 // Pick the digit d with above(d) < krem <= above(d) + hist[d], where
-// above(d) counts keys in higher bins.  Warp 0 only.
+// above(d) counts keys in higher bins (NB bins).  Warp 0 only.
+template <int NB>
 __device__ void pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_digit,
                            uint32_t* out_above) {
+  constexpr int PER = NB / 32;
   const int lane = threadIdx.x & 31;
-  uint32_t c[8];
   uint32_t sum = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    c[j] = hist[255 - 8 * lane - j];
-    sum += c[j];
-  }
+  for (int j = 0; j < PER; ++j) sum += hist[NB - 1 - PER * lane - j];
   uint32_t incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -118,16 +159,47 @@ __device__ void pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_di
   const uint32_t excl = incl - sum;
   if (excl < krem && krem <= incl) {
     uint32_t accum = excl;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (accum + c[j] >= krem) {
-        *out_digit = uint32_t(255 - 8 * lane - j);
+    for (int j = 0; j < PER; ++j) {
+      const uint32_t c = hist[NB - 1 - PER * lane - j];
+      if (accum + c >= krem) {
+        *out_digit = uint32_t(NB - 1 - PER * lane - j);
         *out_above = accum;
         break;
       }
-      accum += c[j];
+      accum += c;
     }
   }
+}
+
+// Exclusive block scan of one packed (gt << 16 | eq) count per thread; also
+// returns the block total.  Two barriers.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    uint32_t x = lane < nw ? sh[lane] : 0u;
+    uint32_t xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, xi, o);
+      if (lane >= o) xi += y;
+    }
+    if (lane < nw) sh[lane] = xi - x;
+    if (lane == nw - 1) sh[32] = xi;
+  }
+  __syncthreads();
+  total = sh[32];
+  const uint32_t r = sh[w] + incl - v;
+  __syncthreads();
+  return r;
 }
 
 // One cluster of kSelCluster CTAs per unit; CTA `rank` owns the positions
@@ -145,15 +217,15 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char sel_smem[];
   float* sc = reinterpret_cast<float*>(sel_smem);
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t hist_g[4][256];  // cluster totals, used in rank 0
+  __shared__ uint32_t hist[kRadixBins];
+  __shared__ uint32_t hist_g[kRadixPasses][kRadixBins];  // cluster totals, used in rank 0
   __shared__ float shf[33];
   __shared__ float part_nu;
   __shared__ uint32_t cnt_gt, cnt_eq;
   __shared__ uint32_t sh_digit, sh_above;
-  __shared__ uint32_t warp_cnt[2][kSelCT / 32];
+  __shared__ uint32_t scan_sh[33];
 
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int tid = threadIdx.x;
   const int rank = int(cl.block_rank());
   const int unit = blockIdx.x / kSelCluster;
   const bool per_seq = a.mode == SFI_SELECT_LOGIT_SUM_SEQ;
@@ -185,24 +257,43 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       iz[hh] = 1.0f / a.stats[qh * 2 + 1];
     }
   }
+  // Positions are processed kSelU at a time per thread with every load
+  // issued before any is used, so the loop is bound by bandwidth, not by the
+  // latency of one load after another.
   float part = 0.f;
-  for (int i = p0 + tid; i < p1; i += kSelCT) {
-    float ev;
-    if constexpr (EV_G > 0) {
-      ev = evidence_from_logits<EV_G>(a.logits + (size_t(u) * a.max_len + i) * EV_G, M, iz);
-    } else if (per_seq) {
-      ev = 0.f;
-      for (int g = 0; g < a.H_kv; ++g) ev += a.evidence[(size_t(b) * a.H_kv + g) * a.max_len + i];
-    } else {
-      ev = a.evidence[size_t(u) * a.max_len + i];
+  for (int base = p0; base < p1; base += kSelCT * kSelU) {
+    float lg[kSelU][EV_G > 0 ? EV_G : 1];
+    float ev[kSelU], kv[kSelU];
+#pragma unroll
+    for (int j = 0; j < kSelU; ++j) {
+      const int i = base + j * kSelCT + tid;
+      ev[j] = 0.f;
+      kv[j] = 0.f;
+      if (i < p1) {
+        if constexpr (EV_G > 0) {
+          load_row<EV_G>(a.logits + (size_t(u) * a.max_len + i) * EV_G, lg[j]);
+        } else if (per_seq) {
+          for (int g = 0; g < a.H_kv; ++g) ev[j] += a.evidence[(size_t(b) * a.H_kv + g) * a.max_len + i];
+        } else {
+          ev[j] = a.evidence[size_t(u) * a.max_len + i];
+        }
+        if (!per_seq && i >= lo && i < hi) kv[j] = kn[i];
+      }
     }
-    sc[i - p0] = ev;
-    if (!per_seq && i >= lo && i < hi) part += kn[i];
+#pragma unroll
+    for (int j = 0; j < kSelU; ++j) {
+      const int i = base + j * kSelCT + tid;
+      if (i < p1) {
+        if constexpr (EV_G > 0) ev[j] = evidence_from_logits<EV_G>(lg[j], M, iz);
+        sc[i - p0] = ev[j];
+        part += kv[j];
+      }
+    }
   }
-  if (tid < 256) {
-    hist[tid] = 0;
+  for (int i = tid; i < kRadixBins; i += kSelCT) {
+    hist[i] = 0;
     if (rank == 0) {
-      for (int j = 0; j < 4; ++j) hist_g[j][tid] = 0;
+      for (int j = 0; j < kRadixPasses; ++j) hist_g[j][i] = 0;
     }
   }
   if (!per_seq) {
@@ -219,55 +310,87 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   // ---------------------------------------------------------------- scores
   float* srow = a.s ? a.s + size_t(u) * a.max_len : nullptr;
   const float w_f = per_seq ? 1.0f : 1.0f - a.lambda;
-  for (int base = p0; base < p1; base += kSelCT) {
-    const int i = base + tid;
-    const bool in = i < p1;
-    float v = 0.f;
-    if (in) {
-      v = w_f * sc[i - p0];
-      if (!per_seq && i >= lo && i < hi) v = fmaf(coef, kn[i], v);
-      sc[i - p0] = v;
-      if (srow) srow[i] = v;
+  for (int base = p0; base < p1; base += kSelCT * kSelU) {
+    float kv[kSelU];
+#pragma unroll
+    for (int j = 0; j < kSelU; ++j) {
+      const int i = base + j * kSelCT + tid;
+      kv[j] = (!per_seq && i < p1 && i >= lo && i < hi) ? kn[i] : 0.f;
     }
-    if (need_radix) hist_add(hist, order_key(v) >> 24, in && i >= lo && i < hi);
+#pragma unroll
+    for (int j = 0; j < kSelU; ++j) {
+      const int i = base + j * kSelCT + tid;
+      const bool in = i < p1;
+      float v = 0.f;
+      if (in) {
+        v = w_f * sc[i - p0];
+        if (!per_seq && i >= lo && i < hi) v = fmaf(coef, kv[j], v);
+        sc[i - p0] = v;
+        if (srow) srow[i] = v;
+      }
+      if (need_radix) hist_add(hist, order_key(v) >> kRadixShift0, in && i >= lo && i < hi);
+    }
   }
   __syncthreads();
 
   int32_t* out_idx = a.idx + size_t(per_seq ? b * a.H_kv : unit) * a.k;
   if (need_radix) {
     // ------------------------------------------------------------ radix select
+    // Three passes of 11, 11 and 10 bits over the order keys of E.  Shared-
+    // memory reads go 8 positions per thread (two 16-byte loads) in tiles
+    // aligned to the CTA's first position.
     uint32_t prefix = 0, krem = uint32_t(keff);
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
+    const int e0 = max(p0, lo), e1 = min(p1, hi);
+    for (int pass = 0; pass < kRadixPasses; ++pass) {
+      const int shift = pass == 0 ? kRadixShift0 : (pass == 1 ? kRadixShift1 : 0);
+      const int width = pass == 0 ? 32 - kRadixShift0 : (pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1);
+      const uint32_t dmask = (1u << width) - 1u;
       if (pass > 0) {
-        if (tid < 256) hist[tid] = 0;
+        for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = 0;
         __syncthreads();
-        const int e0 = max(p0, lo), e1 = min(p1, hi);
-        for (int base = e0; base < e1; base += kSelCT) {
-          const int i = base + tid;
-          const bool in = i < e1;
-          const uint32_t key = in ? order_key(sc[i - p0]) : 0u;
-          hist_add(hist, (key >> shift) & 255u, in && (key >> (shift + 8)) == prefix);
+        const int hs = shift + width;
+        for (int tb = p0; tb < e1; tb += kSelCT * 8) {
+          const int i0 = tb + tid * 8;
+          float v8[8];
+          load8(sc, i0 - p0, p1 - p0, v8);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = i0 + j;
+            const uint32_t key = order_key(v8[j]);
+            const bool m = i >= e0 && i < e1 && (key >> hs) == prefix;
+            hist_add(hist, (key >> shift) & dmask, m);
+          }
         }
         __syncthreads();
       }
-      if (tid < 256 && hist[tid]) atomicAdd(cl.map_shared_rank(&hist_g[pass][tid], 0), hist[tid]);
+      for (int i = tid; i < kRadixBins; i += kSelCT)
+        if (hist[i]) atomicAdd(cl.map_shared_rank(&hist_g[pass][i], 0), hist[i]);
       cl.sync();
-      if (tid < 256) hist[tid] = *cl.map_shared_rank(&hist_g[pass][tid], 0);
+      for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = *cl.map_shared_rank(&hist_g[pass][i], 0);
       __syncthreads();
-      if (tid < 32) pick_digit(hist, krem, &sh_digit, &sh_above);
+      if (tid < 32) {
+        if (width == 11) pick_digit<2048>(hist, krem, &sh_digit, &sh_above);
+        else pick_digit<1024>(hist, krem, &sh_digit, &sh_above);
+      }
       __syncthreads();
-      prefix = (prefix << 8) | sh_digit;
+      prefix = (prefix << width) | sh_digit;
       krem -= sh_above;
     }
     const uint32_t tau = prefix, take_eq = krem;
     // ------------------------------------------------------------ compaction
-    const int e0 = max(p0, lo), e1 = min(p1, hi);
     uint32_t g_loc = 0, q_loc = 0;
-    for (int i = e0 + tid; i < e1; i += kSelCT) {
-      const uint32_t key = order_key(sc[i - p0]);
-      g_loc += key > tau;
-      q_loc += key == tau;
+    for (int tb = p0; tb < e1; tb += kSelCT * 8) {
+      const int i0 = tb + tid * 8;
+      float v8[8];
+      load8(sc, i0 - p0, p1 - p0, v8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j;
+        const uint32_t key = order_key(v8[j]);
+        const bool in = i >= e0 && i < e1;
+        g_loc += in && key > tau;
+        q_loc += in && key == tau;
+      }
     }
     const float gs = sel_block_sum(float(g_loc), shf);  // exact: counts < 2^24
     const float qs = sel_block_sum(float(q_loc), shf);
@@ -281,35 +404,36 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       gt_before += *cl.map_shared_rank(&cnt_gt, r);
       eq_before += *cl.map_shared_rank(&cnt_eq, r);
     }
-    for (int base = e0; base < e1; base += kSelCT) {
-      const int i = base + tid;
-      const bool in = i < e1;
-      const uint32_t key = in ? order_key(sc[i - p0]) : 0u;
-      const bool isg = in && key > tau, isq = in && key == tau;
-      const unsigned bg = __ballot_sync(kFull, isg), bq = __ballot_sync(kFull, isq);
-      const unsigned lt = (1u << lane) - 1u;
-      if (lane == 0) {
-        warp_cnt[0][w] = __popc(bg);
-        warp_cnt[1][w] = __popc(bq);
+    for (int tb = p0; tb < e1; tb += kSelCT * 8) {
+      const int i0 = tb + tid * 8;
+      float v8[8];
+      load8(sc, i0 - p0, p1 - p0, v8);
+      uint32_t fg = 0, fq = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j;
+        const uint32_t key = order_key(v8[j]);
+        const bool in = i >= e0 && i < e1;
+        fg |= uint32_t(in && key > tau) << j;
+        fq |= uint32_t(in && key == tau) << j;
       }
-      __syncthreads();
-      uint32_t wg = 0, wq = 0, tg = 0, tq = 0;
-      for (int j = 0; j < kSelCT / 32; ++j) {
-        const uint32_t cg_ = warp_cnt[0][j], cq_ = warp_cnt[1][j];
-        if (j < w) {
-          wg += cg_;
-          wq += cq_;
+      uint32_t tile_tot;
+      const uint32_t ex = block_excl_scan((uint32_t(__popc(fg)) << 16) | uint32_t(__popc(fq)),
+                                          scan_sh, tile_tot);
+      uint32_t gb = gt_before + (ex >> 16), qb = eq_before + (ex & 0xffffu);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j;
+        if ((fg >> j) & 1u) {
+          out_idx[gb + min(qb, take_eq)] = i;
+          ++gb;
+        } else if ((fq >> j) & 1u) {
+          if (qb < take_eq) out_idx[gb + qb] = i;
+          ++qb;
         }
-        tg += cg_;
-        tq += cq_;
       }
-      const uint32_t gb = gt_before + wg + __popc(bg & lt);
-      const uint32_t qb = eq_before + wq + __popc(bq & lt);
-      if (isg) out_idx[gb + min(qb, take_eq)] = i;
-      if (isq && qb < take_eq) out_idx[gb + qb] = i;
-      gt_before += tg;
-      eq_before += tq;
-      __syncthreads();
+      gt_before += tile_tot >> 16;
+      eq_before += tile_tot & 0xffffu;
     }
   } else {
     // keep all of E (or nothing): position lo + j goes to slot j

@@ -58,7 +58,7 @@ struct FpassArgs {
   uint32_t* status;
 };
 
-constexpr int kSelectMaxLen = 409600;  // per-position rows the cluster selector holds in shared memory
+constexpr int kSelectMaxLen = 327680;  // per-position rows the cluster selector holds in shared memory
 
 struct SelectArgs {
   const float* evidence;  // f (fused mode) or per-KV-head logit sums (logit-sum mode)
@@ -77,6 +77,18 @@ struct SelectArgs {
   SeqMask active;
   uint32_t* status;
 };
+
+// Verification attention (Vegas): R chain rows per head, collected logit sums.
+struct VerifyArgs {
+  AttnArgs base;         // q: [B][R][H_q][D]; out: [B][R][H_q][D]; all units dense
+  int32_t R;             // verify rows per sequence
+  int32_t ncg;           // collected rows * G (tile rows 0..ncg-1 are collected)
+  int8_t t_of_slot[8];   // chain row of each tile slot (slot = tile row / G)
+  float* lsum;           // [B*H_kv][max_len] or null
+  float lscale;          // 1 / sqrt(D)
+};
+cudaError_t launch_verify(const VerifyArgs& va, int D, int G, cudaStream_t st);
+int verify_stage_rows();
 
 // Workspace plan: one layout serves every call of a given geometry.
 struct WsPlan {
@@ -100,6 +112,7 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
 sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,
                     long long n_fast_units, int fast_rows, cudaStream_t st);
 int fast_unit_rows_bound(const sfi_layout* L, const sfi_params* P);
+int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid);
 sfi_status fail(sfi_status s, const char* fmt, ...);
 sfi_status cuda_fail(cudaError_t e, const char* what);
 

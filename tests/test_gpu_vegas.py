@@ -1,0 +1,110 @@
+"""GPU parity of the Vegas path: verification attention with a causal tail,
+Collect-2 logit sums, per-sequence aggregated selection and the draft steps,
+against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.sfi_oracle as O
+import sfi_workloads as W
+from tests.sfi_testlib import DeviceLayer, O_TOL, check_selection, load_sfi, max_abs, storage_to_torch
+
+pytestmark = pytest.mark.gpu
+
+# Collected logit sums: each is a sum of 2*G logits of size O(1), accumulated
+# in fp32 on the tensor cores from exact bf16 products; 1e-4 * (1 + |L|)
+# bounds that accumulation with a wide margin.  The selection tie band is the
+# same absolute term: positions closer than that to the k-th sum are ambiguous.
+L_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def sfi():
+    assert torch.cuda.is_available()
+    return load_sfi()
+
+
+def run_vegas(sfi, wl, n_pre, gamma, k, collect):
+    sh = wl.shape
+    B, R = sh.batch, gamma + 1
+    dl = DeviceLayer.build(wl)
+    lens = [n + R for n in n_pre]
+    lay = dl.layout(sfi, lens)
+    ws = sfi.verify_workspace(lay, R)
+    q_st = [[wl.q_storage(0, 0, b, t) for t in range(R)] for b in range(B)]
+    q = torch.stack([torch.stack([storage_to_torch(q_st[b][t], sh.dtype) for t in range(R)])
+                     for b in range(B)]).cuda()
+    q64 = [np.stack([W.storage_to_f64(q_st[b][t], sh.dtype) for t in range(R)]) for b in range(B)]
+    out = torch.full((B, R, sh.n_q_heads, sh.head_dim), float("nan"), device="cuda")
+    lsum = torch.full((B, sh.n_kv_heads, lay.max_len), -7.0, device="cuda")
+    sfi.sfi_verify_attn(lay, R, collect, q, dl.k, dl.v, out, lsum, ws)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws) == 0
+    out, lsum_np = out.cpu().numpy(), lsum.cpu().numpy()
+    # selection: per-sequence top-k of the head-summed logit sums
+    prm = sfi.params(0, R, k, 0.0, mode=sfi.SFI_SELECT_LOGIT_SUM_SEQ)
+    idx = torch.full((B, sh.n_kv_heads, k), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, sh.n_kv_heads), -1, dtype=torch.int32, device="cuda")
+    s_out = torch.full((B, sh.n_kv_heads, lay.max_len), -7.0, device="cuda")
+    ws2 = sfi.alloc_workspace(lay)
+    sfi.sfi_select(lay, prm, lsum, None, idx, cnt, s_out, ws2)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws2) == 0
+    idx, cnt, s_np = idx.cpu().numpy(), cnt.cpu().numpy(), s_out.cpu().numpy()
+    T = []
+    for b in range(B):
+        o_ref, logits = O.verify_attention(q64[b], dl.K64[b], dl.V64[b], n_pre[b])
+        assert max_abs(out[b], o_ref) <= O_TOL[sh.dtype], max_abs(out[b], o_ref)
+        Lg = O.collected_logit_sum(logits, collect, n_pre[b], n_kv_heads=sh.n_kv_heads)
+        got = lsum_np[b, :, :n_pre[b]]
+        assert np.all(np.abs(got - Lg) <= L_TOL * (1 + np.abs(Lg))), float(np.max(np.abs(got - Lg)))
+        assert np.all(lsum_np[b, :, n_pre[b]:] == -7.0), "wrote past the prefix"
+        L = Lg.sum(0)
+        ke = min(k, n_pre[b])
+        assert np.all(cnt[b] == ke)
+        sel = idx[b, 0, :ke]
+        for g in range(1, sh.n_kv_heads):
+            assert np.array_equal(idx[b, g, :ke], sel)
+        check_selection(sel, L, 0, n_pre[b], k, rtol=1e-6, atol=L_TOL * (1 + np.abs(L).max()))
+        assert np.array_equal(sel, O.top_k(s_np[b, 0].astype(np.float64), 0, n_pre[b], k))
+        T.append(sel.astype(np.int64))
+    # draft steps j = 1..gamma at length n_pre + gamma + j: T plus the tail since the prefix
+    for j in range(1, gamma + 1):
+        lens_j = [n + gamma + j for n in n_pre]
+        lay_j = dl.layout(sfi, lens_j)
+        qd, qf = dl.queries(10 + j)
+        o = torch.empty(B, sh.n_q_heads, sh.head_dim, device="cuda")
+        tail = gamma + j
+        # one window for the batch: sequences share the draft position
+        prm_d = sfi.params(0, tail, k, 0.0)
+        sfi.sfi_fast_attn(lay_j, prm_d, qd, dl.k, dl.v, torch.from_numpy(idx).cuda(),
+                          torch.from_numpy(cnt).cuda(), o, ws2)
+        torch.cuda.synchronize()
+        assert sfi.sfi_read_status(ws2) == 0
+        o = o.cpu().numpy()
+        for b in range(B):
+            ref = O.draft_step(qf[b], dl.K64[b], dl.V64[b], n_pre[b], lens_j[b], T[b])
+            assert max_abs(o[b], ref) <= O_TOL[sh.dtype], (j, b, max_abs(o[b], ref))
+
+
+def test_vegas_small(sfi):
+    n_pre = [3000, 1234]
+    wl = W.small(2, 32, 8, 128, "bf16", [n + 5 for n in n_pre], seed=31, k=200)
+    run_vegas(sfi, wl, n_pre, gamma=4, k=200, collect=[0, 4])
+
+
+def test_vegas_other_shapes(sfi):
+    # d = 64, G = 8 (collected rows fill tile 0), three chain rows
+    n_pre = [700, 2049, 64]
+    wl = W.small(3, 16, 2, 64, "bf16", [n + 3 for n in n_pre], seed=32, k=50)
+    run_vegas(sfi, wl, n_pre, gamma=2, k=50, collect=[0, 2])
+    # G = 4 with all five rows in two tiles, collecting three rows
+    n_pre = [1500]
+    wl = W.small(1, 8, 2, 128, "bf16", [n + 5 for n in n_pre], seed=33, k=1500)
+    run_vegas(sfi, wl, n_pre, gamma=4, k=1500, collect=[1, 3, 4])
+
+
+def test_vegas_cfg3_full_size(sfi):
+    """Batch 4, prefix 65536, gamma 4, Collect-2 rows {0, 4}, k = 2048."""
+    wl = W.cfg3()
+    run_vegas(sfi, wl, wl.n0, gamma=wl.gamma, k=wl.k, collect=[0, wl.gamma])
