@@ -1,7 +1,9 @@
 // C ABI of libsfi: host-side validation, workspace planning and kernel
 // dispatch for the slow step, the selector and the fast step.  Every check
 // happens before anything is enqueued; errors carry a thread-local message.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cmath>
 #include <cstdarg>
@@ -163,6 +165,44 @@ int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, i
   return int(best);
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// K (or V) as a 2-D tensor of bf16 rows: dim 0 = D elements, dim 1 = rows.
+// The row extent is the largest the descriptor allows; the kernel only ever
+// asks for full 64-row boxes that lie inside a (sequence, KV head) slab.
+bool encode_rows(CUtensorMap* m, const void* base, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(1) << 31};
+  const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+void attach_tensor_maps(AttnArgs& a, const sfi_layout* L) {
+  a.use_tma = 0;
+  if (L->dtype != SFI_BF16) return;
+  if (reinterpret_cast<uintptr_t>(a.k) % 16 || reinterpret_cast<uintptr_t>(a.v) % 16) return;
+  if (encode_rows(&a.tmk, a.k, L->head_dim) && encode_rows(&a.tmv, a.v, L->head_dim)) a.use_tma = 1;
+}
+
 void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const void* k,
                       const void* v, float* out, char* ws, const WsPlan& p) {
   std::memset(&a, 0, sizeof(a));
@@ -184,6 +224,7 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
   a.status = reinterpret_cast<uint32_t*>(ws + p.status_off);
   a.logits = reinterpret_cast<float*>(ws + p.logits_off);
   a.stats = reinterpret_cast<float*>(ws + p.stats_off);
+  attach_tensor_maps(a, L);
 }
 
 sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,

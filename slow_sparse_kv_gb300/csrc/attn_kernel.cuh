@@ -86,9 +86,16 @@ struct AttnCfg {
     return OFF_UNITS + (size_t(kMaxUnits) + 1) * 4 <= size_t(227) * 1024;
   }
   static_assert(OFF_UNITS_MAX_CHECK(), "shared memory plan exceeds 227 KB");
-  // byte offset of 16-byte chunk c of stage row r (XOR swizzle on the MMA path)
+  // Byte offset of 16-byte chunk c of stage row r.  Tensor-core path: the
+  // stage is stored as 64-element column halves [c / 8][row][128 bytes] with
+  // the 128-byte swizzle (chunk c % 8 stored at (c % 8) ^ (row % 8)), the
+  // layout a 64 x 64 TMA box with CU_TENSOR_MAP_SWIZZLE_128B produces; rows
+  // copied with cp.async use the same addresses.  SIMT path: plain rows.
   static __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
-    return uint32_t(r * ROWB + ((MMA ? (c ^ (r & 7)) : c) << 4));
+    if constexpr (MMA)
+      return uint32_t((c >> 3) * (SR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    else
+      return uint32_t(r * ROWB + (c << 4));
   }
 };
 
@@ -189,6 +196,8 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
                                              uint32_t bar_empty, volatile int* abort_flag,
                                              int lane) {
   constexpr int D = C::DIM;
+  // the swizzle pattern assumes 1024-byte aligned stage buffers
+  const bool tma_ok = (smem_addr(smem) & 1023u) == 0;
   const uint64_t pol = l2_evict_first_policy();
   const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
   uint32_t stage = 0;
@@ -203,6 +212,15 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
     const int cnt = I.slow ? 0 : min(max(a.count[I.u], 0), a.idx_stride);
     const int wlo = max(a.n_sink, n - a.window);
     const int32_t* ix = I.slow ? nullptr : a.idx + size_t(I.u) * a.idx_stride;
+    // TMA rows of this unit: K viewed as [rows][D]; usable when the slab
+    // starts on a whole row and its rows fit the descriptor
+    long long row0 = 0;
+    bool tma_unit = false;
+    if constexpr (C::MMA) {
+      const long long off = a.kv_offset[I.b];
+      row0 = off / D + (long long)I.g * a.kv_cap[I.b];
+      tma_unit = a.use_tma && tma_ok && I.slow && off % D == 0 && row0 + I.r1 < (1LL << 31);
+    }
     // Row positions of stage c0 (lane l: rows l, l + 32, ...).  Gathered
     // positions come from the index list in global memory, so the loads
     // for the next stage are issued one stage ahead of their use.
@@ -247,7 +265,19 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
         break;
       }
       const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
-      if (!C::MMA && I.slow) {
+      if (tma_unit && nr == C::SR) {
+        // full dense stage: 64-row TMA boxes, one per 64-column half
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(C::SR) * C::ROWB * 2u);
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_2d(kd + h * (C::SR * 128), &a.tmk, h * 64, int(row0 + c0), bar_full + 8 * slot, pol);
+            tma_load_2d(vd + h * (C::SR * 128), &a.tmv, h * 64, int(row0 + c0), bar_full + 8 * slot, pol);
+          }
+        } else {
+          mbar_arrive(bar_full + 8 * slot);
+        }
+      } else if (!C::MMA && I.slow) {
         // dense rows: one bulk copy of K and one of V for the whole stage
         if (lane == 0) {
           mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
@@ -620,9 +650,10 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
+    attn_kernel(const __grid_constant__ AttnArgs a) {
   using C = AttnCfg<T, D, G>;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_units = a.B * a.H_kv;
   int* units = reinterpret_cast<int*>(smem + C::OFF_UNITS);

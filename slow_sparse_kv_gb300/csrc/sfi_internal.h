@@ -2,6 +2,7 @@
 // decode.cpp) and the CUDA kernels.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -22,6 +23,11 @@ struct SeqMask {
 // Split-K attention over either the whole cache (slow sequences) or the
 // managed sparse state (fast sequences) of every (sequence, KV head) unit.
 struct AttnArgs {
+  // 2-D TMA descriptors of K and V viewed as [rows][D] bf16 rows with a
+  // 128-byte swizzle and 64 x 64 boxes (used when use_tma is set).
+  CUtensorMap tmk;
+  CUtensorMap tmv;
+  int32_t use_tma;
   const void* q;  // [B][H_q][D]
   const void* k;
   const void* v;
@@ -113,6 +119,9 @@ sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, in
                     long long n_fast_units, int fast_rows, cudaStream_t st);
 int fast_unit_rows_bound(const sfi_layout* L, const sfi_params* P);
 int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid);
+// Fill a.tmk / a.tmv for bf16 caches (sets a.use_tma; leaves it 0 if the
+// driver entry point is unavailable).
+void attach_tensor_maps(AttnArgs& a, const sfi_layout* L);
 sfi_status fail(sfi_status s, const char* fmt, ...);
 sfi_status cuda_fail(cudaError_t e, const char* what);
 

@@ -51,7 +51,7 @@ struct VerifyCfg {
   static constexpr size_t OFF_UNITS = OFF_MISC + 64;
   static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1) * 4; }
   static __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
-    return uint32_t(r * ROWB + ((c ^ (r & 7)) << 4));
+    return uint32_t((c >> 3) * (SR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
   }
 };
 
@@ -222,10 +222,11 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(VerifyCfg<D>::NT, 1) verify_kernel(const VerifyArgs va) {
+__global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
+    verify_kernel(const __grid_constant__ VerifyArgs va) {
   using C = VerifyCfg<D>;
   const AttnArgs& a = va.base;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_units = a.B * a.H_kv;
   int* units = reinterpret_cast<int*>(smem + C::OFF_UNITS);
