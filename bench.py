@@ -240,24 +240,25 @@ class Cfg2Runner:
         B, L, T = sh.batch, wl.n_layers, wl.n_steps
         dt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
         dcode = 1 if sh.dtype == "bf16" else 0
-        per_seq = sh.n_kv_heads * wl.cap[0] * sh.head_dim
-        self.offsets = [b * per_seq for b in range(B)]
+        per = [sh.n_kv_heads * c * sh.head_dim for c in wl.cap]  # ragged: one slab per sequence
+        self.offsets = [int(sum(per[:b])) for b in range(B)]
+        total = int(sum(per))
         st = self.stream.cuda_stream
         self.K, self.V, self.Q = [], [], []
         for l in range(L):
             u = wl.u_vec(l)
             u3 = torch.tensor(3.0 * u, dtype=torch.float64, device=self.dev)
             u2 = torch.tensor(2.0 * u, dtype=torch.float64, device=self.dev)
-            kt = torch.empty(B * per_seq, dtype=dt, device=self.dev)
-            vt = torch.empty(B * per_seq, dtype=dt, device=self.dev)
+            kt = torch.empty(total, dtype=dt, device=self.dev)
+            vt = torch.empty(total, dtype=dt, device=self.dev)
             for b in range(B):
                 mask = torch.from_numpy(wl.heavy_mask(l, b).astype(np.uint8)).to(self.dev)
                 cap = wl.cap[b]
                 r = gen.sfigen_fill(kt.data_ptr() + self.offsets[b] * kt.element_size(), dcode,
-                                    wl.key(W.T_K, l, b), 0, per_seq, sh.head_dim, cap,
+                                    wl.key(W.T_K, l, b), 0, per[b], sh.head_dim, cap,
                                     mask.data_ptr(), u3.data_ptr(), st)
                 r |= gen.sfigen_fill(vt.data_ptr() + self.offsets[b] * vt.element_size(), dcode,
-                                     wl.key(W.T_V, l, b), 0, per_seq, sh.head_dim, cap, None, None, st)
+                                     wl.key(W.T_V, l, b), 0, per[b], sh.head_dim, cap, None, None, st)
                 assert r == 0, "generator launch failed"
             qt = torch.empty(T, B, sh.n_q_heads, sh.head_dim, dtype=dt, device=self.dev)
             nq = sh.n_q_heads * sh.head_dim
@@ -543,6 +544,56 @@ def run_kernel_cases(args):
     return {"kernel_cases": res, "batch": B, "context": n}
 
 
+def run_ragged_sweep(args):
+    """Ragged serving batch (32 sequences, contexts log-uniform in [4096, 262144],
+    25% at a boundary): per (k, window) point, an untimed all-slow step at n - 1
+    builds every selection, then one mixed step at n -- 8 slow and 24 fast
+    sequences in one attention launch plus the selector -- is timed."""
+    import torch
+    import slow_sparse_kv_gb300 as sfi
+    base = W.cfg4()
+    R = Cfg2Runner(base, 0)
+    sh = base.shape
+    slow_set = set(int(x) for x in W.cfg4_slow_set())
+    bnd1 = (ctypes.c_uint8 * sh.batch)(*[1 if b in slow_set else 0 for b in range(sh.batch)])
+    row = 2 * sh.n_kv_heads * sh.head_dim * sh.esize
+    lens = [n + 1 for n in base.n0]
+    points = []
+    for k in (1024, 4096, 16384):
+        for win in (128, 256, 512):
+            ctx = sfi.DecodeContext(sh.batch, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16,
+                                    R.max_len, 1, sfi.params(base.n_sink, win, k, base.lam), 0)
+            times = []
+            for rep in range(args.warmup + args.steps):
+                ctx.reset()
+                r = sfi.lib.sfi_decode_step(ctx.h, 0, R.bnd[0], R.layouts[0], R.Q[0][0].data_ptr(), R.kp[0],
+                                            R.vp[0], R.op[0], R.stream.cuda_stream)
+                assert r == 0
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                r = sfi.lib.sfi_decode_step(ctx.h, 0, bnd1, R.layouts[1], R.Q[0][1].data_ptr(), R.kp[0],
+                                            R.vp[0], R.op[0], R.stream.cuda_stream)
+                e1.record()
+                assert r == 0
+                torch.cuda.synchronize()
+                if rep >= args.warmup:
+                    times.append(e0.elapsed_time(e1))
+            ctx.close()
+            nbytes = 0
+            for b in range(sh.batch):
+                n = lens[b]
+                if b in slow_set:
+                    nbytes += n * row
+                else:
+                    e = max(0, (n - 1) - win - base.n_sink)
+                    nbytes += (min(base.n_sink, n) + min(k, e) + (n - max(base.n_sink, n - win))) * row
+            ms = statistics.median(times)
+            points.append({"k": k, "window": win, "ms": round(ms, 4), "alg_bytes": nbytes,
+                           "GB/s": round(nbytes / ms / 1e6, 1)})
+    return {"ragged_sweep": points, "sequences": sh.batch, "slow": sorted(slow_set),
+            "contexts": lens, "kv_gb": round(sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9, 2)}
+
+
 def run_reference(args):
     """The fp64 oracle as it stands, timed on the host cores for the same
     workload, metric and unit (bounded sample per step)."""
@@ -588,10 +639,15 @@ def main():
     ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast: time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
     ap.add_argument("--case-batch", type=int, default=2)
+    ap.add_argument("--ragged-sweep", action="store_true", help="time one mixed slow/fast step of "
+                    "the 32-sequence ragged batch for k in {1024, 4096, 16384} x window in {128, 256, 512}")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.ragged_sweep:
+        print(json.dumps(run_ragged_sweep(args)), flush=True)
+        return
     if args.kernel_case:
         print(json.dumps(run_kernel_cases(args)), flush=True)
         return

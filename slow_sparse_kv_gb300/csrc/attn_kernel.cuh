@@ -65,7 +65,9 @@ struct AttnCfg {
       int((227 * 1024 - 2048 - size_t(NCW) * G * (D + 2) * 4 - (size_t(kMaxUnits) + 1) * 4) /
           (2 * size_t(SR) * ROWB));
   static constexpr int NS = NS_FIT > 6 ? 6 : (NS_FIT < 2 ? 2 : NS_FIT);
-  static constexpr int NT = (NCW + 1) * 32;
+  static constexpr int PW = 4;              // producer warps (each copies SR / PW rows)
+  static_assert(SR % (PW * RPI) == 0, "stage rows split evenly over the producer warps");
+  static constexpr int NT = (NCW + 4) * 32;  // consumers + producer warps
   static constexpr int STAGE_B = SR * ROWB;  // bytes of K (or V) per stage
   static constexpr int NE = (RB * G + 31) / 32;
   static constexpr int V = G * R;
@@ -194,8 +196,11 @@ template <class C>
 __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units, int n_units,
                                              int total, unsigned char* smem, uint32_t bar_full,
                                              uint32_t bar_empty, volatile int* abort_flag,
-                                             int lane) {
+                                             int pw, int lane) {
   constexpr int D = C::DIM;
+  constexpr int RPW = C::SR / C::PW;        // rows of a stage per producer warp
+  constexpr int PJ = (RPW + 31) / 32;       // positions per lane
+  const int rbase = pw * RPW;               // this warp's first row of every stage
   // the swizzle pattern assumes 1024-byte aligned stage buffers
   const bool tma_ok = (smem_addr(smem) & 1023u) == 0;
   const uint64_t pol = l2_evict_first_policy();
@@ -224,14 +229,14 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
     // Row positions of stage c0 (lane l: rows l, l + 32, ...).  Gathered
     // positions come from the index list in global memory, so the loads
     // for the next stage are issued one stage ahead of their use.
-    auto resolve_pos = [&](int c0s, int (&out)[(C::SR + 31) / 32]) {
+    auto resolve_pos = [&](int c0s, int (&out)[PJ]) {
       const int nrs = min(C::SR, I.r1 - c0s);
 #pragma unroll
-      for (int j = 0; j < (C::SR + 31) / 32; ++j) {
-        const int r = lane + 32 * j;
+      for (int j = 0; j < PJ; ++j) {
+        const int r = rbase + lane + 32 * j;
         const int lp = c0s + r;
         int p = I.slow ? lp : 0;  // rows past the stage are never copied
-        if (!I.slow && r < nrs) {
+        if (!I.slow && r < nrs && lane + 32 * j < RPW) {
           if (lp < ns) {
             p = lp;
           } else if (lp < ns + cnt) {
@@ -243,15 +248,15 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
         out[j] = p;
       }
     };
-    int pos_next[(C::SR + 31) / 32];
+    int pos_next[PJ];
     resolve_pos(I.r0, pos_next);
     for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
       const int nr = min(C::SR, I.r1 - c0);
       const int slot = stage % C::NS;
       const uint32_t ph = (stage / C::NS) & 1u;
-      int pos[(C::SR + 31) / 32];
+      int pos[PJ];
 #pragma unroll
-      for (int j = 0; j < (C::SR + 31) / 32; ++j) {
+      for (int j = 0; j < PJ; ++j) {
         int p = pos_next[j];
         if (!I.slow && (p < 0 || p >= n)) {
           set_status(a.status, SFI_DEV_BAD_INDEX);
@@ -267,7 +272,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
       const uint32_t kd = kbase + slot * C::STAGE_B, vd = vbase + slot * C::STAGE_B;
       if (tma_unit && nr == C::SR) {
         // full dense stage: 64-row TMA boxes, one per 64-column half
-        if (lane == 0) {
+        if (pw == 0 && lane == 0) {
           mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(C::SR) * C::ROWB * 2u);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h) {
@@ -279,7 +284,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
         }
       } else if (!C::MMA && I.slow) {
         // dense rows: one bulk copy of K and one of V for the whole stage
-        if (lane == 0) {
+        if (pw == 0 && lane == 0) {
           mbar_arrive_expect_tx(bar_full + 8 * slot, uint32_t(nr) * C::ROWB * 2u);
           bulk_g2s(kd, kb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
           bulk_g2s(vd, vb + size_t(c0) * C::ROWB, uint32_t(nr) * C::ROWB, bar_full + 8 * slot, pol);
@@ -289,12 +294,13 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
       } else {
         // row by row: every lane copies one 16-byte chunk of a row; the
         // row positions were resolved before the wait (pos[]), lane l
-        // holding the rows l, l + 32, ...
+        // holding this warp's rows l, l + 32, ...
 #pragma unroll
-        for (int i = 0; i < C::SR / C::RPI; ++i) {
-          const int r = i * C::RPI + lane / C::LPR;
+        for (int i = 0; i < RPW / C::RPI; ++i) {
+          const int rl = i * C::RPI + lane / C::LPR;
+          const int r = rbase + rl;
           const int c = lane % C::LPR;
-          const int p = __shfl_sync(kFull, pos[(i * C::RPI) / 32], r & 31);
+          const int p = __shfl_sync(kFull, pos[(i * C::RPI) / 32], rl & 31);
           if (r < nr) {
             const size_t so = size_t(p) * C::ROWB + c * 16;
             cp_async16(kd + C::chunk_off(r, c), kb + so, pol);
@@ -668,19 +674,20 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
     return;
   }
   if (blockIdx.x >= total) return;
-  volatile int* abort_flag = misc + 12;
+  volatile int* abort_flag = misc + 14;  // misc[0..12]: unit-table scan scratch
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
+      mbar_init(bar_full + 8 * s, 32 * C::PW);  // one arrival per producer lane
       mbar_init(bar_empty + 8 * s, C::CPS);  // one arrival per consuming warp
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == C::NCW) {
-    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, abort_flag, lane);
+  if (warp >= C::NCW) {
+    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, abort_flag, warp - C::NCW,
+                    lane);
     return;
   }
 
@@ -734,9 +741,9 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
     if (!single) {
       __threadfence();
       named_bar_sync(1, nct);
-      if (tid == 0) misc[13] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
+      if (tid == 0) misc[15] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
       named_bar_sync(1, nct);
-      if (misc[13]) {
+      if (misc[15]) {
         __threadfence();
         for (int j = tid; j < G * D; j += nct) {
           const int hh = j / D, dim = j % D;

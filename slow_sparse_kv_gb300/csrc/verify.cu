@@ -36,7 +36,8 @@ struct VerifyCfg {
   static constexpr int MW = 16;
   static constexpr int CPS = NCW;  // both tiles read every stage
   static constexpr int SR = MW * 4;
-  static constexpr int NT = (NCW + 1) * 32;
+  static constexpr int PW = 4;  // producer warps
+  static constexpr int NT = (NCW + PW) * 32;
   static constexpr int STAGE_B = SR * ROWB;
   static constexpr size_t RED_B = size_t(NCW) * 16 * (D + 2) * 4;
   static constexpr int NS_FIT =
@@ -240,18 +241,19 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
     return;
   }
   if (blockIdx.x >= total) return;
-  volatile int* abort_flag = misc + 12;
+  volatile int* abort_flag = misc + 14;  // misc[0..12]: unit-table scan scratch
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(bar_full + 8 * s, 32);
+      mbar_init(bar_full + 8 * s, 32 * C::PW);
       mbar_init(bar_empty + 8 * s, C::CPS);
     }
     fence_mbar_init();
   }
   __syncthreads();
-  if (warp == C::NCW) {
-    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, abort_flag, lane);
+  if (warp >= C::NCW) {
+    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, abort_flag, warp - C::NCW,
+                    lane);
     return;
   }
   float* red_all = reinterpret_cast<float*>(smem + C::OFF_RED);
@@ -294,9 +296,9 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
     if (!single) {
       __threadfence();
       named_bar_sync(1, nct);
-      if (tid == 0) misc[13] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
+      if (tid == 0) misc[15] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
       named_bar_sync(1, nct);
-      if (misc[13]) {
+      if (misc[15]) {
         __threadfence();
         for (int j = tid; j < QR * D; j += nct) {
           const int qr = j / D, dim = j % D;
