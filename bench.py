@@ -236,6 +236,9 @@ class Cfg2Runner:
         gen.sfigen_fill.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_int64,
                                     ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_void_p]
+        gen.sfigen_fill_rows.restype = ctypes.c_int
+        gen.sfigen_fill_rows.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         self.gen = gen
         B, L, T = sh.batch, wl.n_layers, wl.n_steps
         dt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
@@ -262,11 +265,11 @@ class Cfg2Runner:
                 assert r == 0, "generator launch failed"
             qt = torch.empty(T, B, sh.n_q_heads, sh.head_dim, dtype=dt, device=self.dev)
             nq = sh.n_q_heads * sh.head_dim
-            for t in range(T):
-                for b in range(B):
-                    r = gen.sfigen_fill(qt[t, b].data_ptr(), dcode, wl.key(W.T_Q, l, b, t, 0), 0, nq,
-                                        sh.head_dim, 1, None, u2.data_ptr(), st)
-                    assert r == 0
+            keys = torch.tensor([wl.key(W.T_Q, l, b, t, 0) - (1 << 64 if wl.key(W.T_Q, l, b, t, 0) >= 1 << 63 else 0)
+                                 for t in range(T) for b in range(B)], dtype=torch.int64, device=self.dev)
+            r = gen.sfigen_fill_rows(qt.data_ptr(), dcode, keys.data_ptr(), T * B, nq, sh.head_dim,
+                                     u2.data_ptr(), st)
+            assert r == 0, "generator launch failed"
             self.K.append(kt)
             self.V.append(vt)
             self.Q.append(qt)

@@ -52,7 +52,41 @@ __global__ void fill_kernel(void* dst, int dtype, uint64_t key, int64_t start, i
   }
 }
 
+// Row r of dst (row_len elements) is stream keys[r] at elements [0, row_len),
+// plus add[j] (j = element % d) when add is not NULL.
+__global__ void fill_rows_kernel(void* dst, int dtype, const uint64_t* keys, int64_t rows,
+                                 int64_t row_len, int d, const double* add) {
+  const int64_t count = rows * row_len;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < count;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / row_len;
+    const uint64_t e = uint64_t(i - r * row_len);
+    double z = normal_at(keys[r], e);
+    if (add) z = z + add[int(e % uint64_t(d))];
+    const float f = __double2float_rn(z);
+    if (dtype == 0) {
+      static_cast<float*>(dst)[i] = f;
+    } else {
+      static_cast<__nv_bfloat16*>(dst)[i] = __float2bfloat16_rn(f);
+    }
+  }
+}
+
 }  // namespace
+
+extern "C" int sfigen_fill_rows(void* dst, int dtype, const uint64_t* keys, int64_t rows,
+                                int64_t row_len, int d, const double* add, void* stream) {
+  if (!dst || !keys || rows < 0 || row_len < 1 || d < 1) return 1;
+  if (rows == 0) return 0;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (rows * row_len + 255) / 256;
+  if (blocks > int64_t(sms) * 16) blocks = int64_t(sms) * 16;
+  fill_rows_kernel<<<int(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(dst, dtype, keys, rows,
+                                                                             row_len, d, add);
+  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
 
 extern "C" int sfigen_fill(void* dst, int dtype, uint64_t key, int64_t start, int64_t count, int d,
                            int cap, const uint8_t* rows_mask, const double* add, void* stream) {

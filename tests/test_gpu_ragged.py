@@ -37,10 +37,14 @@ def test_ragged_mixed_step():
         kd = R.K[0][R.offsets[b]:R.offsets[b] + per].view(torch.int16).cpu().numpy().view(np.uint16)
         vd = R.V[0][R.offsets[b]:R.offsets[b] + per].view(torch.int16).cpu().numpy().view(np.uint16)
         assert int(np.sum(kd != k_st.reshape(-1))) <= 2 and int(np.sum(vd != v_st.reshape(-1))) <= 2
-        q = [W.storage_to_f64(R.Q[0][t][b].view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
-             for t in range(2)]
-        inp[b] = (W.storage_to_f64(kd.reshape(k_st.shape), "bf16"),
-                  W.storage_to_f64(vd.reshape(v_st.shape), "bf16"), q)
+        q = []
+        for t in range(2):
+            q_st = base.q_storage(0, t, b)
+            qd = R.Q[0][t][b].view(torch.int16).cpu().numpy().view(np.uint16)
+            assert int(np.sum(qd != q_st)) <= 1
+            q.append(W.storage_to_f64(q_st, "bf16"))
+        # the oracle reads the CPU generator's values only
+        inp[b] = (W.storage_to_f64(k_st, "bf16"), W.storage_to_f64(v_st, "bf16"), q)
     bnd1 = (ctypes.c_uint8 * sh.batch)(*[1 if b in slow_set else 0 for b in range(sh.batch)])
     for k, win in POINTS:
         ctx = sfi.DecodeContext(sh.batch, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16,
