@@ -223,7 +223,7 @@ class ClockSampler:
 class Cfg2Runner:
     """Device-resident decode workload driven through sfi_decode_step."""
 
-    def __init__(self, wl: W.Workload, device: int):
+    def __init__(self, wl: W.Workload, device: int, async_select: bool = True):
         import torch
         import slow_sparse_kv_gb300 as sfi
         self.torch, self.sfi, self.wl = torch, sfi, wl
@@ -288,7 +288,8 @@ class Cfg2Runner:
         self.trace = wl.boundary_trace()
         self.bnd = [(ctypes.c_uint8 * B)(*[int(x) for x in self.trace[t]]) for t in range(T)]
         self.ctx = sfi.DecodeContext(B, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dt, self.max_len, L,
-                                     sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget)
+                                     sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget,
+                                     async_select=async_select)
         self.slow_masks = None
         self.kp = [t.data_ptr() for t in self.K]
         self.vp = [t.data_ptr() for t in self.V]
@@ -343,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         wl.seed = rank_seed(wl.seed, rank)
     t_setup = time.perf_counter()
-    R = Cfg2Runner(wl, local_rank)
+    R = Cfg2Runner(wl, local_rank, async_select=not args.sync_select)
     setup_s = time.perf_counter() - t_setup
     sfi = R.sfi
     sh = wl.shape
@@ -457,6 +458,7 @@ def run_ours(args, rank, world, local_rank):
             "l2": "inputs larger than L2 (%.1f GB of KV per GPU)" % (
                 sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9),
             "parallelism": f"dp{world} (independent sequences per GPU)",
+            "selector": "in line" if args.sync_select else "overlapped with the next layer",
         },
         "tokens_per_s": round(steps_per_s * sh.batch, 1),
         "breakdown": {
@@ -499,8 +501,8 @@ def run_kernel_cases(args):
     import slow_sparse_kv_gb300 as sfi
     wl = W.cfg2(n_layers=1, n_steps=1)
     wl.shape = W.Shape(args.case_batch, 32, 8, 128, "bf16")
-    wl.n0 = wl.n0[:args.case_batch]
-    wl.cap = wl.cap[:args.case_batch]
+    wl.n0 = [wl.n0[i % len(wl.n0)] for i in range(args.case_batch)]
+    wl.cap = [wl.cap[i % len(wl.cap)] for i in range(args.case_batch)]
     R = Cfg2Runner(wl, 0)
     sh = wl.shape
     B = sh.batch
@@ -639,6 +641,9 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=1.5, help="seconds per CPU worker")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sync-select", action="store_true",
+                    help="run each layer's selector on the decode stream instead of overlapping it "
+                         "with the next layer's attention")
     ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast: time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
     ap.add_argument("--case-batch", type=int, default=2)

@@ -17,8 +17,10 @@
  *    than sfi_ctx_create allocate nothing; scratch comes from a caller-owned
  *    device workspace whose size the matching *_workspace_size call returns.
  *    A workspace must be zero-filled (cudaMemsetAsync) before its first use;
- *    every call that returns SFI_OK leaves it ready for the next call.  Calls
- *    that share one workspace must not overlap on the GPU.
+ *    every call that returns SFI_OK and whose device status (sfi_read_status)
+ *    stays 0 leaves it ready for the next call.  After a nonzero device
+ *    status, zero-fill it again: its work and merge counters may be left
+ *    mid-count.  Calls that share one workspace must not overlap on the GPU.
  *  - Asynchrony: every call only enqueues kernels on `stream` (a
  *    cudaStream_t; NULL is the legacy default stream) and returns.
  *  - Errors: arguments are validated on the host before anything is
@@ -242,10 +244,17 @@ typedef struct {
   int32_t n_layers; /* each layer keeps its own selection */
   sfi_params params;
   int32_t budget;   /* fast steps allowed between refreshes; 0 = unlimited */
+  /* != 0: overlap each layer's selector with the next layer's attention (SFI
+   * pages, "System design": selection runs asynchronously beside decoding).
+   * The selector then runs on a high-priority stream of the context, with a
+   * second set of evidence buffers; the caller's stream joins it at the last
+   * layer of each step.  0: the selector runs on the caller's stream. */
+  int32_t async_select;
 } sfi_ctx_desc;
 
 /* Create a decode context: allocates (with cudaMalloc, once) each layer's
- * selection buffers and the shared evidence/workspace buffers. */
+ * selection buffers and the shared evidence/workspace buffers (two sets when
+ * async_select != 0), and with async_select its stream and events. */
 sfi_status sfi_ctx_create(const sfi_ctx_desc* desc, sfi_ctx** ctx_out);
 sfi_status sfi_ctx_destroy(sfi_ctx* ctx);
 
@@ -258,7 +267,13 @@ sfi_status sfi_ctx_destroy(sfi_ctx* ctx);
  * then runs one mixed launch (dense rows for slow sequences, managed-state
  * rows for fast ones); for slow sequences it also computes f and the key
  * norms and refreshes the layer's selection.  is_boundary_host is read only
- * when layer == 0.  q: [B][H_q][d]; out: [B][H_q][d] fp32. */
+ * when layer == 0.  q: [B][H_q][d]; out: [B][H_q][d] fp32.
+ * With async_select, the selector of a layer below the last may still run
+ * after the caller's stream has passed this call; the step of the last layer
+ * orders every selector before later work on `stream`, and
+ * sfi_ctx_selection / sfi_ctx_read_status order themselves after them.  The
+ * layout's device arrays need stay valid only until this call's attention
+ * has run (the selector reads a copy of len). */
 sfi_status sfi_decode_step(sfi_ctx* ctx, int32_t layer, const uint8_t* is_boundary_host,
                            const sfi_layout* layout, const void* q, const void* k,
                            const void* v, float* out, sfi_stream stream);
@@ -272,7 +287,10 @@ sfi_status sfi_schedule(int32_t batch, int32_t budget, const uint8_t* is_boundar
                         uint8_t* have_sel, int32_t* since, uint8_t* slow_out);
 
 /* Forget the schedule state (every sequence starts again without a
- * selection, so its next step is slow).  Host only. */
+ * selection, so its next step is slow) and zero-fill the context's
+ * workspace, clearing its device status.  Synchronous: waits for the
+ * device (cudaMemset), so no decode step of this context may be in flight
+ * on another thread. */
 sfi_status sfi_ctx_reset(sfi_ctx* ctx);
 
 /* Device-time profiling of sfi_decode_step (off by default).  enable != 0
@@ -285,11 +303,17 @@ sfi_status sfi_ctx_profile(sfi_ctx* ctx, int32_t enable);
 sfi_status sfi_ctx_profile_read(sfi_ctx* ctx, double* attn_ms, int64_t* attn_launches,
                                 double* select_ms, int64_t* select_launches);
 
+/* OR of the device status words of the context's workspaces (the bits
+ * SFI_DEV_*), cleared; waits for `stream` after ordering it behind every
+ * selector enqueued so far.  Returns SFI_ERR_CUDA if a copy fails. */
+sfi_status sfi_ctx_read_status(sfi_ctx* ctx, uint32_t* status_host, sfi_stream stream);
+
 /* The current step's decision (host [B], 1 = slow). */
 sfi_status sfi_ctx_slow_mask(const sfi_ctx* ctx, uint8_t* slow_host);
 
 /* Copy a layer's current selection into caller device buffers idx_out
- * ([B][H_kv][k] int32) and count_out ([B][H_kv] int32), enqueued on stream. */
+ * ([B][H_kv][k] int32) and count_out ([B][H_kv] int32), enqueued on stream
+ * behind every selector enqueued so far. */
 sfi_status sfi_ctx_selection(const sfi_ctx* ctx, int32_t layer, int32_t* idx_out,
                              int32_t* count_out, sfi_stream stream);
 

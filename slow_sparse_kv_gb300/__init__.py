@@ -41,7 +41,8 @@ class sfi_params(ctypes.Structure):
 class sfi_ctx_desc(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32),
                 ("head_dim", c_int32), ("dtype", c_int32), ("max_len", c_int32),
-                ("n_layers", c_int32), ("params", sfi_params), ("budget", c_int32)]
+                ("n_layers", c_int32), ("params", sfi_params), ("budget", c_int32),
+                ("async_select", c_int32)]
 
 
 _L = POINTER(sfi_layout)
@@ -71,6 +72,7 @@ EXPORTS = {
                                   c_void_p, c_void_p]),
     "sfi_schedule": (c_int32, [c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "sfi_ctx_reset": (c_int32, [c_void_p]),
+    "sfi_ctx_read_status": (c_int32, [c_void_p, POINTER(c_uint32), c_void_p]),
     "sfi_ctx_profile": (c_int32, [c_void_p, c_int32]),
     "sfi_ctx_profile_read": (c_int32, [c_void_p, POINTER(ctypes.c_double), POINTER(ctypes.c_int64),
                                        POINTER(ctypes.c_double), POINTER(ctypes.c_int64)]),
@@ -249,9 +251,10 @@ class DecodeContext:
     """sfi_ctx wrapper: per-layer selections plus the slow/fast schedule."""
 
     def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, dtype: torch.dtype,
-                 max_len: int, n_layers: int, prm: sfi_params, budget: int):
+                 max_len: int, n_layers: int, prm: sfi_params, budget: int,
+                 async_select: bool = True):
         desc = sfi_ctx_desc(batch, n_q_heads, n_kv_heads, head_dim, dtype_code(dtype), max_len,
-                            n_layers, prm, budget)
+                            n_layers, prm, budget, int(bool(async_select)))
         h = c_void_p()
         _check("sfi_ctx_create", lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)))
         self.h = h
@@ -291,6 +294,13 @@ class DecodeContext:
         _check("sfi_ctx_profile_read", lib.sfi_ctx_profile_read(
             self.h, ctypes.byref(am), ctypes.byref(al), ctypes.byref(sm), ctypes.byref(sl)))
         return am.value, al.value, sm.value, sl.value
+
+    def read_status(self, stream=None) -> int:
+        """OR of the context's device status words (cleared); waits for the stream."""
+        v = c_uint32(0)
+        _check("sfi_ctx_read_status", lib.sfi_ctx_read_status(self.h, ctypes.byref(v),
+                                                              _stream(stream)))
+        return int(v.value)
 
     def slow_mask(self):
         buf = (ctypes.c_uint8 * self.batch)()

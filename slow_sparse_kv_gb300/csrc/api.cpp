@@ -64,7 +64,7 @@ WsPlan plan_workspace(int B, int H_q, int H_kv, int D, int max_len) {
   p.status_off = off;
   off += 256;
   p.counters_off = off;
-  off += align256(units * 4);
+  off += align256((units + 2) * 4);  // merge counters + the two work-distribution counters
   p.partials_off = off;
   off += align256(size_t(p.max_items) * G * (D + 2) * 4);
   p.logits_off = off;
@@ -135,27 +135,41 @@ int stage_rows(int dtype, int D) {
 }
 
 // Rows per work item for a launch whose units come in two classes (n_a units
-// of at most rows_a rows, n_b of at most rows_b).  Items are processed in
-// waves over `grid` CTAs; the estimate of a launch is waves * (stages per
-// item + a fixed per-item cost of about three stages), minimised over item
-// sizes that split either class evenly.  At most kItemSlotsPerUnit items per
-// unit (the workspace holds that many partials).
+// of at most rows_a rows, n_b of at most rows_b).  CTAs take items
+// dynamically, each paying a fixed cost of about 3 stages per item.  When
+// every item has the same size (one class) the launch lasts
+// ceil(items / grid) items; with two classes it lasts about the total work
+// / grid plus half the largest item.  The size minimises that estimate over
+// sizes that split either class evenly, with at most kItemSlotsPerUnit items
+// per unit (the workspace holds that many partials).
 int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid) {
+  if (n_a == 0 || rows_a <= 0) n_a = 0, rows_a = 0;
+  if (n_b == 0 || rows_b <= 0) n_b = 0, rows_b = 0;
   const int rows_max = rows_a > rows_b ? rows_a : rows_b;
   long long min_rpi = ceil_div(ceil_div(rows_max, kItemSlotsPerUnit), sr) * sr;
   if (min_rpi < sr) min_rpi = sr;
   const double c_item = 3.0;
+  const bool one_class = n_a == 0 || n_b == 0 || rows_a == rows_b;
   long long best = min_rpi;
   double best_cost = 1e300;
   for (int cls = 0; cls < 2; ++cls) {
     const int rows = cls == 0 ? rows_a : rows_b;
-    if (rows <= 0 || (cls == 0 ? n_a : n_b) == 0) continue;
+    if (rows <= 0) continue;
     for (int k = 1; k <= kItemSlotsPerUnit; ++k) {
       long long rpi = ceil_div(ceil_div(rows, k), sr) * sr;
       if (rpi < min_rpi) rpi = min_rpi;
-      const long long items = n_a * ceil_div(rows_a, rpi) + n_b * ceil_div(rows_b, rpi);
-      const long long waves = ceil_div(items, grid);
-      const double cost = double(waves) * (double(rpi) / sr + c_item);
+      const long long ia = n_a ? ceil_div(rows_a, rpi) : 0, ib = n_b ? ceil_div(rows_b, rpi) : 0;
+      const long long items = n_a * ia + n_b * ib;
+      double cost;
+      if (one_class) {
+        // equal items (the last of a unit may be shorter): whole rounds of the grid
+        cost = double(ceil_div(items, grid)) * (double(rpi) / sr + c_item);
+      } else {
+        const double stages =
+            double(n_a) * ceil_div(rows_a, sr) + double(n_b) * ceil_div(rows_b, sr);
+        const long long big = (ia > 1 || ib > 1) ? rpi : (rows_a > rows_b ? rows_a : rows_b);
+        cost = (stages + c_item * double(items)) / grid + 0.5 * (double(big) / sr + c_item);
+      }
       if (cost < best_cost) {
         best_cost = cost;
         best = rpi;
@@ -221,6 +235,7 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
   a.qscale = float(1.4426950408889634 / std::sqrt(double(L->head_dim)));
   a.partials = reinterpret_cast<float*>(ws + p.partials_off);
   a.counters = reinterpret_cast<int32_t*>(ws + p.counters_off);
+  a.work_ctr = reinterpret_cast<uint32_t*>(a.counters + size_t(L->batch) * L->n_kv_heads);
   a.status = reinterpret_cast<uint32_t*>(ws + p.status_off);
   a.logits = reinterpret_cast<float*>(ws + p.logits_off);
   a.stats = reinterpret_cast<float*>(ws + p.stats_off);

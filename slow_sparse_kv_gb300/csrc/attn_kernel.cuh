@@ -44,6 +44,17 @@
 
 namespace sfi {
 
+// Dynamic work distribution.  A CTA's first producer warp takes item ids
+// from a global counter (a.work_ctr[0]) as it starts each item and publishes
+// them through a small ring in shared memory (slot mbarriers: `full` with one
+// arrival, `empty` with one arrival from each of the other producer warps and
+// from consumer warp 0).  CTAs that start late -- for example on SMs that a
+// concurrently running kernel held -- simply take fewer items.  The last CTA
+// to finish fetching resets the counters for the next launch.
+constexpr int kItemRing = 4;
+// misc[] words of the CTA's shared scratch
+constexpr int kMiscAbort = 14, kMiscLast = 15, kMiscRing = 16, kMiscCurItem = 24;
+
 template <typename T, int D, int G>
 struct AttnCfg {
   static constexpr bool MMA = std::is_same<T, bf16_t>::value;
@@ -61,9 +72,11 @@ struct AttnCfg {
   static constexpr int SR = MMA ? MW * CPS : RB * NCW;  // rows per stage
   // pipeline depth: as many stages as shared memory allows (bytes in flight
   // per SM are what keeps HBM busy), at most 6
-  static constexpr int NS_FIT =
-      int((227 * 1024 - 2048 - size_t(NCW) * G * (D + 2) * 4 - (size_t(kMaxUnits) + 1) * 4) /
-          (2 * size_t(SR) * ROWB));
+  static constexpr size_t FIXED_B = (2 * 6 + 2 * kItemRing) * 8 +                   // mbarriers
+                                    (MMA ? 0 : size_t(NCW) * RB * (G + 1) * 4) +  // SIMT scratch
+                                    size_t(NCW) * G * (D + 2) * 4 + 128 +          // reduce + misc
+                                    (size_t(kMaxUnits) + 1) * 4;                   // unit table
+  static constexpr int NS_FIT = int((227 * 1024 - FIXED_B) / (2 * size_t(SR) * ROWB));
   static constexpr int NS = NS_FIT > 6 ? 6 : (NS_FIT < 2 ? 2 : NS_FIT);
   static constexpr int PW = 4;              // producer warps (each copies SR / PW rows)
   static_assert(SR % (PW * RPI) == 0, "stage rows split evenly over the producer warps");
@@ -78,11 +91,11 @@ struct AttnCfg {
   static constexpr size_t OFF_K = 0;
   static constexpr size_t OFF_V = OFF_K + size_t(NS) * STAGE_B;
   static constexpr size_t OFF_BAR = OFF_V + size_t(NS) * STAGE_B;
-  static constexpr size_t OFF_SL = OFF_BAR + 2 * NS * 8;                  // SIMT scratch
+  static constexpr size_t OFF_SL = OFF_BAR + (2 * NS + 2 * kItemRing) * 8;  // SIMT scratch
   static constexpr size_t OFF_SN = OFF_SL + (MMA ? 0 : size_t(NCW) * RB * G * 4);
   static constexpr size_t OFF_RED = OFF_SN + (MMA ? 0 : size_t(NCW) * RB * 4);
   static constexpr size_t OFF_MISC = OFF_RED + size_t(NCW) * G * (D + 2) * 4;
-  static constexpr size_t OFF_UNITS = OFF_MISC + 64;
+  static constexpr size_t OFF_UNITS = OFF_MISC + 128;
   static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1) * 4; }
   static constexpr bool OFF_UNITS_MAX_CHECK() {
     return OFF_UNITS + (size_t(kMaxUnits) + 1) * 4 <= size_t(227) * 1024;
@@ -100,6 +113,55 @@ struct AttnCfg {
       return uint32_t(r * ROWB + (c << 4));
   }
 };
+
+struct ItemRing {
+  uint32_t full, empty;  // mbarrier addresses of slot 0
+  volatile int* slot;    // kItemRing item ids
+};
+
+// Fetch the next item id for this CTA and publish it (first producer warp).
+__device__ __forceinline__ int ring_fetch_publish(const AttnArgs& a, int total, const ItemRing& r,
+                                                  uint32_t seq, volatile int* abort_flag,
+                                                  int lane) {
+  int it = -1;
+  bool fetched_end = false;
+  if (lane == 0) {
+    const unsigned x = atomicAdd(a.work_ctr, 1u);
+    if (x < unsigned(total)) {
+      it = int(x);
+    } else {
+      fetched_end = true;
+    }
+  }
+  it = __shfl_sync(kFull, it, 0);
+  if (lane == 0 && fetched_end) {
+    // every CTA fetches past the end exactly once; the last one resets
+    if (atomicAdd(a.work_ctr + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.work_ctr, 0u);
+      atomicExch(a.work_ctr + 1, 0u);
+    }
+  }
+  const int slot = seq % kItemRing;
+  const uint32_t ph = (seq / kItemRing) & 1u;
+  if (!warp_pipe_wait(r.empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) it = -1;
+  if (lane == 0) {
+    r.slot[slot] = it;
+    mbar_arrive(r.full + 8 * slot);
+  }
+  return it;
+}
+
+// Read the next published item id (other producer warps, consumer warp 0).
+__device__ __forceinline__ int ring_read(const AttnArgs& a, const ItemRing& r, uint32_t seq,
+                                         volatile int* abort_flag, int lane) {
+  const int slot = seq % kItemRing;
+  const uint32_t ph = (seq / kItemRing) & 1u;
+  int it = -1;
+  if (warp_pipe_wait(r.full + 8 * slot, ph, abort_flag, a.status)) it = r.slot[slot];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(r.empty + 8 * slot);
+  return it;
+}
 
 struct ItemInfo {
   int u, b, g, r0, r1, n, first, n_items;
@@ -195,8 +257,8 @@ __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* u
 template <class C>
 __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units, int n_units,
                                              int total, unsigned char* smem, uint32_t bar_full,
-                                             uint32_t bar_empty, volatile int* abort_flag,
-                                             int pw, int lane) {
+                                             uint32_t bar_empty, const ItemRing& ring,
+                                             volatile int* abort_flag, int pw, int lane) {
   constexpr int D = C::DIM;
   constexpr int RPW = C::SR / C::PW;        // rows of a stage per producer warp
   constexpr int PJ = (RPW + 31) / 32;       // positions per lane
@@ -207,7 +269,10 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
   const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
   uint32_t stage = 0;
   bool ok = true;
-  for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+  for (uint32_t iseq = 0; ok; ++iseq) {
+    const int it = pw == 0 ? ring_fetch_publish(a, total, ring, iseq, abort_flag, lane)
+                           : ring_read(a, ring, iseq, abort_flag, lane);
+    if (it < 0) break;
     const ItemInfo I = attn_resolve(a, units, n_units, it);
     const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
     const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
@@ -667,27 +732,36 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
   const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
   const uint32_t bar_empty = bar_full + C::NS * 8;
 
+  if (a.len_copy && blockIdx.x == 0)
+    for (int b = tid; b < a.B; b += C::NT) a.len_copy[b] = a.len[b];
   attn_build_units<C::NT>(a, units, n_units, misc);
   const int total = units[n_units];
   if (total > a.max_items) {
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
     return;
   }
-  if (blockIdx.x >= total) return;
-  volatile int* abort_flag = misc + 14;  // misc[0..12]: unit-table scan scratch
+  volatile int* abort_flag = misc + kMiscAbort;  // misc[0..12]: unit-table scan scratch
+  ItemRing ring;
+  ring.full = bar_empty + C::NS * 8;
+  ring.empty = ring.full + kItemRing * 8;
+  ring.slot = misc + kMiscRing;
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(bar_full + 8 * s, 32 * C::PW);  // one arrival per producer lane
       mbar_init(bar_empty + 8 * s, C::CPS);  // one arrival per consuming warp
     }
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(ring.full + 8 * s, 1);
+      mbar_init(ring.empty + 8 * s, C::PW);  // other producer warps + consumer warp 0
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
   if (warp >= C::NCW) {
-    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, abort_flag, warp - C::NCW,
-                    lane);
+    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, ring, abort_flag,
+                    warp - C::NCW, lane);
     return;
   }
 
@@ -696,10 +770,25 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
   const int nct = C::NCW * 32;
   uint32_t stage = 0;
 
-  for (int it = blockIdx.x; it < total; it += gridDim.x) {
+  volatile int* cur_item = misc + kMiscCurItem;
+  for (uint32_t iseq = 0;; ++iseq) {
+    // consumer warp 0 takes the item id from the ring and shares it
+    if (warp == 0) {
+      const int x = ring_read(a, ring, iseq, abort_flag, lane);
+      if (lane == 0) *cur_item = x;
+    }
+    named_bar_sync(1, nct);
+    const int it = *cur_item;
+    named_bar_sync(1, nct);
+    if (it < 0) break;
     const ItemInfo I = attn_resolve(a, units, n_units, it);
     const bool emit = a.emit && I.slow;
     float* red = red_all + warp * G * (D + 2);
+    // Tensor-core warps split stages by the parity of the CTA's running stage
+    // count, so which group holds the item's even stages depends on the
+    // CTA's earlier items; merging the groups in item order keeps the result
+    // independent of which CTA ran the item.
+    const int wflip = C::MMA ? int(stage & 1u) * 4 : 0;
     if constexpr (C::MMA) {
       attn_item_mma<D, G>(a, I, smem, bar_full, bar_empty, abort_flag, stage, warp, lane, red);
     } else {
@@ -718,7 +807,7 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
       float A = 0.f, Z = 0.f;
 #pragma unroll
       for (int w = 0; w < C::NCW; ++w) {
-        const float* rw = red_all + (w * G + hh) * (D + 2);
+        const float* rw = red_all + ((w ^ wflip) * G + hh) * (D + 2);
         const float sc = exp2f(rw[0] - M);
         Z = fmaf(rw[1], sc, Z);
         A = fmaf(rw[2 + dim], sc, A);
@@ -741,9 +830,9 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
     if (!single) {
       __threadfence();
       named_bar_sync(1, nct);
-      if (tid == 0) misc[15] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
+      if (tid == 0) misc[kMiscLast] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
       named_bar_sync(1, nct);
-      if (misc[15]) {
+      if (misc[kMiscLast]) {
         __threadfence();
         for (int j = tid; j < G * D; j += nct) {
           const int hh = j / D, dim = j % D;

@@ -13,14 +13,28 @@
 
 #include "sfi_internal.h"
 
+// Overlapped selection (desc.async_select != 0): the selector of layer l runs
+// on a high-priority side stream while the caller's stream goes on to layer
+// l + 1.  The buffers the selector reads (logits and statistics in the
+// workspace, key norms, a copy of len) come in two sets, used by layers of
+// even and odd index; a launch that rewrites set p first waits for the last
+// selector that read it (event sel_done[p]), which on the in-order side
+// stream also orders every earlier selector, including the one that wrote
+// the selection the launch reads.  At the last layer the caller's stream
+// joins the side stream, so a token's work is complete when the step of its
+// last layer is.
 struct sfi_ctx {
   sfi_ctx_desc desc;
   sfi::WsPlan plan;
-  // device
-  char* ws = nullptr;          // attention / selector workspace
-  float* knorm = nullptr;      // [B*H_kv][max_len]
+  // device, per buffer set
+  char* ws[2] = {nullptr, nullptr};        // attention / selector workspace
+  float* knorm[2] = {nullptr, nullptr};    // [B*H_kv][max_len]
+  int32_t* len_copy[2] = {nullptr, nullptr};  // [B]
   int32_t* idx = nullptr;      // [L][B*H_kv][k]
   int32_t* count = nullptr;    // [L][B*H_kv]
+  int n_sets = 1;
+  cudaStream_t side = nullptr;
+  cudaEvent_t attn_done[2] = {nullptr, nullptr}, sel_done[2] = {nullptr, nullptr};
   // host schedule state
   std::vector<uint8_t> have_sel, slow;
   std::vector<int32_t> since;
@@ -39,10 +53,17 @@ constexpr size_t kProfPairs = 4096;
 
 void free_ctx(sfi_ctx* c) {
   if (!c) return;
+  if (c->side) cudaStreamSynchronize(c->side);
   for (cudaEvent_t e : c->ev_attn) cudaEventDestroy(e);
   for (cudaEvent_t e : c->ev_sel) cudaEventDestroy(e);
-  cudaFree(c->ws);
-  cudaFree(c->knorm);
+  for (int p = 0; p < 2; ++p) {
+    if (c->attn_done[p]) cudaEventDestroy(c->attn_done[p]);
+    if (c->sel_done[p]) cudaEventDestroy(c->sel_done[p]);
+    cudaFree(c->ws[p]);
+    cudaFree(c->knorm[p]);
+    cudaFree(c->len_copy[p]);
+  }
+  if (c->side) cudaStreamDestroy(c->side);
   cudaFree(c->idx);
   cudaFree(c->count);
   delete c;
@@ -106,11 +127,23 @@ sfi_status sfi_ctx_create(const sfi_ctx_desc* d, sfi_ctx** out) {
   if (!c) return fail(SFI_ERR_CAPACITY, "out of host memory");
   c->desc = *d;
   c->plan = plan_workspace(d->batch, d->n_q_heads, d->n_kv_heads, d->head_dim, d->max_len);
+  c->n_sets = d->async_select ? 2 : 1;
   const size_t units = size_t(d->batch) * d->n_kv_heads;
   const size_t row = units * size_t(d->max_len) * sizeof(float);
-  cudaError_t e = cudaMalloc(&c->ws, c->plan.total);
-  if (e == cudaSuccess) e = cudaMemset(c->ws, 0, c->plan.total);
-  if (e == cudaSuccess) e = cudaMalloc(&c->knorm, row);
+  cudaError_t e = cudaSuccess;
+  for (int p = 0; p < c->n_sets && e == cudaSuccess; ++p) {
+    e = cudaMalloc(&c->ws[p], c->plan.total);
+    if (e == cudaSuccess) e = cudaMemset(c->ws[p], 0, c->plan.total);
+    if (e == cudaSuccess) e = cudaMalloc(&c->knorm[p], row);
+    if (e == cudaSuccess) e = cudaMalloc(&c->len_copy[p], size_t(d->batch) * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->attn_done[p], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->sel_done[p], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess && d->async_select) {
+    int lo = 0, hi = 0;  // numerically lowest value = highest priority
+    e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, hi);
+  }
   if (e == cudaSuccess)
     e = cudaMalloc(&c->idx, size_t(d->n_layers) * units * d->params.k * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&c->count, size_t(d->n_layers) * units * sizeof(int32_t));
@@ -154,6 +187,26 @@ sfi_status sfi_ctx_reset(sfi_ctx* c) {
   std::fill(c->since.begin(), c->since.end(), 0);
   std::fill(c->slow.begin(), c->slow.end(), 0);
   c->decided = false;
+  cudaError_t e = c->side ? cudaStreamSynchronize(c->side) : cudaSuccess;
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  for (int p = 0; p < c->n_sets && e == cudaSuccess; ++p) e = cudaMemset(c->ws[p], 0, c->plan.total);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "zero-filling the context workspace");
+  return SFI_OK;
+}
+
+sfi_status sfi_ctx_read_status(sfi_ctx* c, uint32_t* status_host, sfi_stream stream) {
+  if (!c || !status_host) return fail(SFI_ERR_INVALID_ARG, "ctx and status_host must be set");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  *status_host = 0;
+  for (int p = 0; p < c->n_sets; ++p) {
+    cudaError_t e = cudaStreamWaitEvent(st, c->sel_done[p], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "ordering the status read");
+    uint32_t v = 0;
+    const sfi_status s = sfi_read_status(c->ws[p], &v, stream);
+    if (s != SFI_OK) return s;
+    *status_host |= v;
+  }
   return SFI_OK;
 }
 
@@ -208,7 +261,11 @@ sfi_status sfi_ctx_selection(const sfi_ctx* c, int32_t layer, int32_t* idx_out,
   const size_t units = size_t(c->desc.batch) * c->desc.n_kv_heads;
   const size_t ni = units * c->desc.params.k;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(idx_out, c->idx + size_t(layer) * ni, ni * sizeof(int32_t),
+  cudaError_t e = cudaSuccess;
+  for (int p = 0; p < c->n_sets && e == cudaSuccess; ++p)
+    e = cudaStreamWaitEvent(st, c->sel_done[p], 0);  // the latest selectors
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(idx_out, c->idx + size_t(layer) * ni, ni * sizeof(int32_t),
                                   cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(count_out, c->count + size_t(layer) * units, units * sizeof(int32_t),
@@ -250,8 +307,14 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   int32_t* idx = c->idx + size_t(layer) * units * d.params.k;
   int32_t* count = c->count + size_t(layer) * units;
 
+  const int p = c->n_sets == 2 ? (layer & 1) : 0;
+  cudaError_t e = cudaSuccess;
+  // the last selector that read this buffer set (and every earlier one) is done
+  if (c->side) e = cudaStreamWaitEvent(st, c->sel_done[p], 0);
+  if (e != cudaSuccess) return cuda_fail(e, "ordering after the selector");
   AttnArgs a;
-  fill_attn_common(a, &Lc, q, k, v, out, c->ws, c->plan);
+  fill_attn_common(a, &Lc, q, k, v, out, c->ws[p], c->plan);
+  a.len_copy = c->len_copy[p];
   int n_slow = 0;
   for (int b = 0; b < d.batch; ++b)
     if (c->slow[b]) {
@@ -259,14 +322,13 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
       ++n_slow;
     }
   a.emit = 1;
-  a.knorm = c->knorm;
+  a.knorm = c->knorm[p];
   a.idx = idx;
   a.count = count;
   a.idx_stride = d.params.k;
   a.n_sink = d.params.n_sink;
   a.window = d.params.window;
   const int fast_bound = fast_unit_rows_bound(&Lc, &d.params);
-  cudaError_t e = cudaSuccess;
   if (c->profiling) e = record_pair(c->ev_attn, c->n_attn_pending, c->attn_ms, false, st);
   if (e != cudaSuccess) return cuda_fail(e, "profiling event");
   if ((s = run_attn(a, &Lc, (long long)n_slow * d.n_kv_heads, d.max_len,
@@ -278,8 +340,15 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
     c->attn_launches += 1;
   }
   if (n_slow == 0) return SFI_OK;
+  cudaStream_t ss = st;  // stream of the selector
+  if (c->side) {
+    ss = c->side;
+    e = cudaEventRecord(c->attn_done[p], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, c->attn_done[p], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "forking the selector stream");
+  }
   if (c->profiling) {
-    e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, false, st);
+    e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, false, ss);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
   }
 
@@ -289,8 +358,8 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   sa.logits = a.logits;
   sa.stats = a.stats;
   sa.H_q = d.n_q_heads;
-  sa.knorm = c->knorm;
-  sa.len = Lc.len;
+  sa.knorm = c->knorm[p];
+  sa.len = c->len_copy[p];
   sa.idx = idx;
   sa.count = count;
   sa.s = nullptr;
@@ -304,12 +373,18 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   sa.mode = SFI_SELECT_FUSED;
   sa.active = a.slow;
   sa.status = a.status;
-  e = launch_select(sa, st);
+  e = launch_select(sa, ss);
   if (e != cudaSuccess) return cuda_fail(e, "selector launch");
   if (c->profiling) {
-    e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, true, st);
+    e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, true, ss);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");
     c->sel_launches += 1;
+  }
+  if (c->side) {
+    e = cudaEventRecord(c->sel_done[p], ss);
+    // join at the last layer: the token's work ends on the caller's stream
+    if (e == cudaSuccess && layer == d.n_layers - 1) e = cudaStreamWaitEvent(st, c->sel_done[p], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "joining the selector stream");
   }
   return SFI_OK;
 }

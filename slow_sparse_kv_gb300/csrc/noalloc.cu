@@ -71,7 +71,7 @@ extern "C" sfi_status sfi_fast_attn_noalloc(const sfi_layout* L, const sfi_param
     return fail(SFI_ERR_INVALID_ARG, "q, k, v, idx, count and out must be set");
   const int G = L->n_q_heads / L->n_kv_heads;
   const long long units = (long long)L->batch * L->n_kv_heads;
-  const size_t counters_bytes = round256(size_t(units) * 4);
+  const size_t counters_bytes = round256(size_t(units + 2) * 4);  // + work-distribution counters
   const size_t item_bytes = size_t(G) * (L->head_dim + 2) * 4;
   const size_t avail = kNoAllocScratchBytes - kHeaderBytes - counters_bytes;
   const long long max_items = (long long)(avail / item_bytes);
@@ -111,6 +111,7 @@ extern "C" sfi_status sfi_fast_attn_noalloc(const sfi_layout* L, const sfi_param
   a.qscale = float(1.4426950408889634 / std::sqrt(double(L->head_dim)));
   a.status = reinterpret_cast<uint32_t*>(w);
   a.counters = reinterpret_cast<int32_t*>(w + kHeaderBytes);
+  a.work_ctr = reinterpret_cast<uint32_t*>(a.counters + units);
   a.partials = reinterpret_cast<float*>(w + kHeaderBytes + counters_bytes);
   a.max_items = int(max_items < 0x7fffffff ? max_items : 0x7fffffff);
   // Work items: every unit's rows in at most max_items / units pieces.

@@ -51,6 +51,8 @@ struct AttnArgs {
   SeqMask slow;
   float* partials;     // [max_items][G][D + 2]
   int32_t* counters;   // [B*H_kv], zero between launches
+  uint32_t* work_ctr;  // [2]: next item, CTAs done fetching; zero between launches
+  int32_t* len_copy;   // optional [B]: the kernel copies len here (for a later selector)
   uint32_t* status;
 };
 

@@ -47,9 +47,9 @@ struct VerifyCfg {
   static constexpr size_t OFF_K = 0;
   static constexpr size_t OFF_V = OFF_K + size_t(NS) * STAGE_B;
   static constexpr size_t OFF_BAR = OFF_V + size_t(NS) * STAGE_B;
-  static constexpr size_t OFF_RED = OFF_BAR + 2 * NS * 8;
+  static constexpr size_t OFF_RED = OFF_BAR + (2 * NS + 2 * kItemRing) * 8;
   static constexpr size_t OFF_MISC = OFF_RED + RED_B;
-  static constexpr size_t OFF_UNITS = OFF_MISC + 64;
+  static constexpr size_t OFF_UNITS = OFF_MISC + 128;
   static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1) * 4; }
   static __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
     return uint32_t((c >> 3) * (SR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
@@ -240,27 +240,43 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
     return;
   }
-  if (blockIdx.x >= total) return;
-  volatile int* abort_flag = misc + 14;  // misc[0..12]: unit-table scan scratch
+  volatile int* abort_flag = misc + kMiscAbort;  // misc[0..12]: unit-table scan scratch
+  ItemRing ring;
+  ring.full = bar_empty + C::NS * 8;
+  ring.empty = ring.full + kItemRing * 8;
+  ring.slot = misc + kMiscRing;
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(bar_full + 8 * s, 32 * C::PW);
       mbar_init(bar_empty + 8 * s, C::CPS);
     }
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(ring.full + 8 * s, 1);
+      mbar_init(ring.empty + 8 * s, C::PW);
+    }
     fence_mbar_init();
   }
   __syncthreads();
   if (warp >= C::NCW) {
-    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, abort_flag, warp - C::NCW,
-                    lane);
+    attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, ring, abort_flag,
+                    warp - C::NCW, lane);
     return;
   }
   float* red_all = reinterpret_cast<float*>(smem + C::OFF_RED);
   const int nct = C::NCW * 32;
   const int QR = va.R * G;
   uint32_t stage = 0;
-  for (int it = blockIdx.x; it < total; it += gridDim.x) {
+  volatile int* cur_item = misc + kMiscCurItem;
+  for (uint32_t iseq = 0;; ++iseq) {
+    if (warp == 0) {
+      const int x = ring_read(a, ring, iseq, abort_flag, lane);
+      if (lane == 0) *cur_item = x;
+    }
+    named_bar_sync(1, nct);
+    const int it = *cur_item;
+    named_bar_sync(1, nct);
+    if (it < 0) break;
     const ItemInfo I = attn_resolve(a, units, n_units, it);
     verify_item<D, G>(va, I, smem, bar_full, bar_empty, abort_flag, stage, warp, lane,
                       red_all + warp * 16 * (D + 2));
@@ -296,9 +312,9 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
     if (!single) {
       __threadfence();
       named_bar_sync(1, nct);
-      if (tid == 0) misc[15] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
+      if (tid == 0) misc[kMiscLast] = atomicAdd(a.counters + I.u, 1) == I.n_items - 1;
       named_bar_sync(1, nct);
-      if (misc[15]) {
+      if (misc[kMiscLast]) {
         __threadfence();
         for (int j = tid; j < QR * D; j += nct) {
           const int qr = j / D, dim = j % D;

@@ -168,7 +168,8 @@ def test_length_over_capacity_is_flagged(sfi):
     assert sfi.sfi_read_status(ws) & sfi.SFI_DEV_LEN_OVER_CAP
 
 
-def test_decode_loop_cfg0(sfi):
+@pytest.mark.parametrize("async_select", [False, True])
+def test_decode_loop_cfg0(sfi, async_select):
     """The decode driver over the 17-step fp32 workload (1 slow + 16 fast)."""
     wl = W.cfg0()
     sh = wl.shape
@@ -176,7 +177,8 @@ def test_decode_loop_cfg0(sfi):
     trace = wl.boundary_trace()
     slow_ref = O.schedule(trace, wl.budget)
     ctx = sfi.DecodeContext(sh.batch, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.float32,
-                            max(wl.cap), 1, sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget)
+                            max(wl.cap), 1, sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget,
+                            async_select=async_select)
     lay = dl.layout(sfi, wl.n0)
     qs64 = []
     outs = []
@@ -203,6 +205,7 @@ def test_decode_loop_cfg0(sfi):
         else:
             exp = O.fast_step(qs64[t], dl.K64[0], dl.V64[0], wl.n0[0] + t, sel, wl.n_sink, wl.window)
         assert max_abs(outs[t], exp) <= O_TOL["f32"], (t, max_abs(outs[t], exp))
+    assert ctx.read_status() == 0
     ctx.close()
 
 
