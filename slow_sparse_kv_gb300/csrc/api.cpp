@@ -5,12 +5,16 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <queue>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "sfi_internal.h"
 
@@ -134,48 +138,120 @@ int stage_rows(int dtype, int D) {
   return dtype == SFI_F32 ? attn_stage_rows_f32(D) : attn_stage_rows_bf16(D);
 }
 
+namespace {
+
+// Length of a launch, in stage times of a CTA streaming at its fair share of
+// HBM, when `grid` CTAs take items in order (n_a units of rows_a rows, then
+// n_b units of rows_b rows, each split into items of rpi rows).  While items
+// remain every CTA is busy and all stream at the same rate (list scheduling
+// with a min-heap of the CTAs' free times).  Once the last item is taken the
+// CTAs that are still busy share HBM among fewer streams and speed up, each
+// to at most kCtaCap times its fair share (the stages a CTA keeps in
+// flight bound its own rate).  Each item also costs kItemCost stage times
+// (its epilogue, and its share of the merge of split units).
+double simulate_launch(long long n_a, int rows_a, long long n_b, int rows_b, long long rpi, int sr,
+                       int grid) {
+  constexpr double kItemCost = 3.0;
+  constexpr double kCtaCap = 1.3;
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < grid; ++i) free_at.push(0.0);
+  double t_last = 0.0;
+  auto take = [&](double cost) {
+    const double t = free_at.top();
+    free_at.pop();
+    t_last = t;
+    free_at.push(t + cost);
+  };
+  for (int cls = 0; cls < 2; ++cls) {
+    const long long n = cls == 0 ? n_a : n_b;
+    const int rows = cls == 0 ? rows_a : rows_b;
+    if (n <= 0 || rows <= 0) continue;
+    const long long full = rows / rpi, rem = rows - full * rpi;
+    const double c_full = double(ceil_div(rpi, sr)) + kItemCost;
+    const double c_rem = double(ceil_div(rem, sr)) + kItemCost;
+    for (long long u = 0; u < n; ++u) {
+      for (long long i = 0; i < full; ++i) take(c_full);
+      if (rem > 0) take(c_rem);
+    }
+  }
+  // the tail: remaining work of every CTA after the last item was taken
+  double t = t_last, done = 0.0;
+  int active = grid;
+  while (!free_at.empty()) {
+    const double r = free_at.top() - t_last;  // ascending
+    free_at.pop();
+    if (r > done) {
+      const double rate = std::min(double(grid) / active, kCtaCap);
+      t += (r - done) / rate;
+      done = r;
+    }
+    --active;
+  }
+  return t;
+}
+
+struct RpiKey {
+  long long n_a, n_b;
+  int rows_a, rows_b, sr, grid;
+  bool operator==(const RpiKey& o) const {
+    return n_a == o.n_a && n_b == o.n_b && rows_a == o.rows_a && rows_b == o.rows_b &&
+           sr == o.sr && grid == o.grid;
+  }
+};
+
+}  // namespace
+
 // Rows per work item for a launch whose units come in two classes (n_a units
-// of at most rows_a rows, n_b of at most rows_b).  CTAs take items
-// dynamically, each paying a fixed cost of about 3 stages per item.  When
-// every item has the same size (one class) the launch lasts
-// ceil(items / grid) items; with two classes it lasts about the total work
-// / grid plus half the largest item.  The size minimises that estimate over
-// sizes that split either class evenly, with at most kItemSlotsPerUnit items
-// per unit (the workspace holds that many partials).
+// of at most rows_a rows, taken first, then n_b of at most rows_b): the
+// candidate that splits either class into 1..kItemSlotsPerUnit even items
+// with the shortest simulated launch, among those that give every CTA an
+// item when any does and the launch is long (at most kItemSlotsPerUnit items per unit: the
+// workspace holds that many partials).  Results are cached per
+// launch shape; a decode loop meets only a handful of shapes.
 int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid) {
-  if (n_a == 0 || rows_a <= 0) n_a = 0, rows_a = 0;
-  if (n_b == 0 || rows_b <= 0) n_b = 0, rows_b = 0;
+  if (n_a <= 0 || rows_a <= 0) n_a = 0, rows_a = 0;
+  if (n_b <= 0 || rows_b <= 0) n_b = 0, rows_b = 0;
+  const RpiKey key{n_a, n_b, rows_a, rows_b, sr, grid};
+  static std::mutex mu;
+  static std::vector<std::pair<RpiKey, int>> cache;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const auto& e : cache)
+      if (e.first == key) return e.second;
+  }
   const int rows_max = rows_a > rows_b ? rows_a : rows_b;
   long long min_rpi = ceil_div(ceil_div(rows_max, kItemSlotsPerUnit), sr) * sr;
   if (min_rpi < sr) min_rpi = sr;
-  const double c_item = 3.0;
-  const bool one_class = n_a == 0 || n_b == 0 || rows_a == rows_b;
-  long long best = min_rpi;
-  double best_cost = 1e300;
+  std::vector<long long> cand;
   for (int cls = 0; cls < 2; ++cls) {
     const int rows = cls == 0 ? rows_a : rows_b;
     if (rows <= 0) continue;
     for (int k = 1; k <= kItemSlotsPerUnit; ++k) {
-      long long rpi = ceil_div(ceil_div(rows, k), sr) * sr;
-      if (rpi < min_rpi) rpi = min_rpi;
-      const long long ia = n_a ? ceil_div(rows_a, rpi) : 0, ib = n_b ? ceil_div(rows_b, rpi) : 0;
-      const long long items = n_a * ia + n_b * ib;
-      double cost;
-      if (one_class) {
-        // equal items (the last of a unit may be shorter): whole rounds of the grid
-        cost = double(ceil_div(items, grid)) * (double(rpi) / sr + c_item);
-      } else {
-        const double stages =
-            double(n_a) * ceil_div(rows_a, sr) + double(n_b) * ceil_div(rows_b, sr);
-        const long long big = (ia > 1 || ib > 1) ? rpi : (rows_a > rows_b ? rows_a : rows_b);
-        cost = (stages + c_item * double(items)) / grid + 0.5 * (double(big) / sr + c_item);
-      }
-      if (cost < best_cost) {
-        best_cost = cost;
-        best = rpi;
-      }
+      const long long rpi = std::max(min_rpi, ceil_div(ceil_div(rows, k), sr) * sr);
+      if (std::find(cand.begin(), cand.end(), rpi) == cand.end()) cand.push_back(rpi);
     }
   }
+  // In long launches fewer streams than SMs lose more bandwidth than the
+  // simulation shows: keep at least one item per CTA whenever a split
+  // provides that.  (Short launches are dominated by per-item latency.)
+  auto items_of = [&](long long rpi) {
+    return n_a * ceil_div(rows_a, rpi) + n_b * ceil_div(rows_b, rpi);
+  };
+  const double stages = double(n_a) * ceil_div(rows_a, sr) + double(n_b) * ceil_div(rows_b, sr);
+  const bool can_fill = items_of(min_rpi) >= grid && stages >= 64.0 * grid;
+  long long best = min_rpi;
+  double best_cost = 1e300;
+  for (long long rpi : cand) {
+    if (can_fill && items_of(rpi) < grid) continue;
+    const double cost = simulate_launch(n_a, rows_a, n_b, rows_b, rpi, sr, grid);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = rpi;
+    }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() >= 256) cache.clear();
+  cache.emplace_back(key, int(best));
   return int(best);
 }
 

@@ -52,6 +52,8 @@ namespace sfi {
 // concurrently running kernel held -- simply take fewer items.  The last CTA
 // to finish fetching resets the counters for the next launch.
 constexpr int kItemRing = 4;
+// words of the sequence-rank table that follows the unit table in shared memory
+constexpr int kRankWords = kMaxBatch / 32 + 1;
 // misc[] words of the CTA's shared scratch
 constexpr int kMiscAbort = 14, kMiscLast = 15, kMiscRing = 16, kMiscCurItem = 24;
 
@@ -75,7 +77,7 @@ struct AttnCfg {
   static constexpr size_t FIXED_B = (2 * 6 + 2 * kItemRing) * 8 +                   // mbarriers
                                     (MMA ? 0 : size_t(NCW) * RB * (G + 1) * 4) +  // SIMT scratch
                                     size_t(NCW) * G * (D + 2) * 4 + 128 +          // reduce + misc
-                                    (size_t(kMaxUnits) + 1) * 4;                   // unit table
+                                    (size_t(kMaxUnits) + 1 + kRankWords) * 4;      // unit table
   static constexpr int NS_FIT = int((227 * 1024 - FIXED_B) / (2 * size_t(SR) * ROWB));
   static constexpr int NS = NS_FIT > 6 ? 6 : (NS_FIT < 2 ? 2 : NS_FIT);
   static constexpr int PW = 4;              // producer warps (each copies SR / PW rows)
@@ -96,9 +98,9 @@ struct AttnCfg {
   static constexpr size_t OFF_RED = OFF_SN + (MMA ? 0 : size_t(NCW) * RB * 4);
   static constexpr size_t OFF_MISC = OFF_RED + size_t(NCW) * G * (D + 2) * 4;
   static constexpr size_t OFF_UNITS = OFF_MISC + 128;
-  static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1) * 4; }
+  static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1 + kRankWords) * 4; }
   static constexpr bool OFF_UNITS_MAX_CHECK() {
-    return OFF_UNITS + (size_t(kMaxUnits) + 1) * 4 <= size_t(227) * 1024;
+    return OFF_UNITS + (size_t(kMaxUnits) + 1 + kRankWords) * 4 <= size_t(227) * 1024;
   }
   static_assert(OFF_UNITS_MAX_CHECK(), "shared memory plan exceeds 227 KB");
   // Byte offset of 16-byte chunk c of stage row r.  Tensor-core path: the
@@ -134,6 +136,9 @@ __device__ __forceinline__ int ring_fetch_publish(const AttnArgs& a, int total, 
     }
   }
   it = __shfl_sync(kFull, it, 0);
+  // no more items for this CTA: the next launch on the stream may start
+  // (programmatic dependent launch; it waits for this grid before it reads)
+  if (it < 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lane == 0 && fetched_end) {
     // every CTA fetches past the end exactly once; the last one resets
     if (atomicAdd(a.work_ctr + 1, 1u) == gridDim.x - 1) {
@@ -183,15 +188,57 @@ __device__ __forceinline__ int attn_unit_rows(const AttnArgs& a, int u, bool rep
   return ns + cnt + max(n - wlo, 0);
 }
 
+// Items are numbered largest first: the units of slow sequences (whole
+// histories) come before those of fast ones (managed state only), each group
+// in sequence order, so the small fast items are the last ones taken and fill
+// the end of the launch.  The unit table lives in shared memory as
+// [n_units + 1] first-item offsets (in that order) followed by kRankWords
+// counts: rank[w] = slow sequences in mask words below w.
+__device__ __forceinline__ int nth_set_bit(uint32_t m, int k) {
+  for (int i = 0; i < k; ++i) m &= m - 1;
+  return __ffs(m) - 1;
+}
+
+// Sequence of rank j: the j-th slow sequence if j < n_slow, else the
+// (j - n_slow)-th fast one (both in increasing order).
+__device__ __forceinline__ int seq_of_rank(const AttnArgs& a, const int* rank, int j) {
+  const int nw = (a.B + 31) >> 5;
+  const int n_slow = rank[nw];
+  int w = 0;
+  if (j < n_slow) {
+    while (rank[w + 1] <= j) ++w;
+    return 32 * w + nth_set_bit(a.slow.bits[w], j - rank[w]);
+  }
+  const int jf = j - n_slow;  // < B - n_slow, so the scan stops below nw
+  while (32 * (w + 1) - rank[w + 1] <= jf) ++w;
+  return 32 * w + nth_set_bit(~a.slow.bits[w], jf - (32 * w - rank[w]));
+}
+
+// Unit (b * H_kv + g) at position v of the item order.
+__device__ __forceinline__ int unit_at(const AttnArgs& a, const int* rank, int v) {
+  return seq_of_rank(a, rank, v / a.H_kv) * a.H_kv + v % a.H_kv;
+}
+
 template <int NT>
 __device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int* scratch) {
-  // units[u] = first item of unit u, units[n_units] = total items.
+  // units[v] = first item of the unit at position v, units[n_units] = total items.
   const int t = threadIdx.x;
+  int* rank = units + n_units + 1;
+  if (t == 0) {
+    const int nw = (a.B + 31) >> 5;
+    int c = 0;
+    for (int w = 0; w < nw; ++w) {
+      rank[w] = c;
+      c += __popc(a.slow.bits[w]);
+    }
+    rank[nw] = c;
+  }
+  __syncthreads();
   const int per = (n_units + NT - 1) / NT;
   const int u0 = min(t * per, n_units), u1 = min(u0 + per, n_units);
   int local = 0;
   for (int u = u0; u < u1; ++u) {
-    const int rows = attn_unit_rows(a, u, blockIdx.x == 0);
+    const int rows = attn_unit_rows(a, unit_at(a, rank, u), blockIdx.x == 0);
     const int it = (rows + a.rows_per_item - 1) / a.rows_per_item;
     units[u] = it;
     local += it;
@@ -236,12 +283,12 @@ __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* u
     else hi = mid - 1;
   }
   ItemInfo I;
-  I.u = lo;
-  I.b = lo / a.H_kv;
-  I.g = lo % a.H_kv;
+  I.u = unit_at(a, units + n_units + 1, lo);
+  I.b = I.u / a.H_kv;
+  I.g = I.u % a.H_kv;
   I.first = units[lo];
   I.n_items = units[lo + 1] - units[lo];
-  const int rows = attn_unit_rows(a, lo, false);
+  const int rows = attn_unit_rows(a, I.u, false);
   I.r0 = (it - I.first) * a.rows_per_item;
   I.r1 = min(rows, I.r0 + a.rows_per_item);
   I.n = a.len[I.b];
@@ -720,11 +767,84 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
   }
 }
 
+// Merge the n_items partial results of unit I.u (run by the CTA that
+// finished its last item; `scr` is free shared scratch of at least
+// G * (kItemSlotsPerUnit + 2) floats).  Warp hh < G takes head hh's maxima
+// and sums (one item per lane), forms the global max M and the item scale
+// factors 2^(m_i - M), and reduces Z; then every thread forms output
+// elements as sum_i scale_i a_i[dim] with many loads in flight.  The order
+// of every sum is fixed, so the result does not depend on the schedule.
+template <int D, int G>
+__device__ __forceinline__ void attn_merge_items(const AttnArgs& a, const ItemInfo& I, bool emit,
+                                                 float* scr, int tid, int nct) {
+  static_assert(G <= 8, "one warp per head");
+  static_assert(kItemSlotsPerUnit <= 64, "two items per lane");
+  constexpr int P = D + 2;
+  const int n = I.n_items;  // <= kItemSlotsPerUnit = 64
+  const float* part = a.partials + size_t(I.first) * G * P;
+  float* sc = scr;                                 // [n][G]
+  float* mz = scr + kItemSlotsPerUnit * G;         // [G][2]: M, Z
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < G) {
+    const int hh = warp;
+    float m[2], z[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      m[r] = i < n ? __ldcg(part + (size_t(i) * G + hh) * P) : -INFINITY;
+      z[r] = i < n ? __ldcg(part + (size_t(i) * G + hh) * P + 1) : 0.f;
+    }
+    float M = fmaxf(m[0], m[1]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float Z = 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = lane + 32 * r;
+      const float f = i < n ? exp2f(m[r] - M) : 0.f;
+      if (i < n) sc[i * G + hh] = f;
+      Z = fmaf(z[r], f, Z);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) Z += __shfl_xor_sync(kFull, Z, o);
+    if (lane == 0) {
+      mz[2 * hh] = M;
+      mz[2 * hh + 1] = Z;
+    }
+  }
+  named_bar_sync(1, nct);
+  for (int j = tid; j < G * D; j += nct) {
+    const int hh = j / D, dim = j % D;
+    const float* pa = part + size_t(hh) * P + 2 + dim;
+    const size_t stride = size_t(G) * P;
+    float A = 0.f;
+    int i = 0;
+    for (; i + 16 <= n; i += 16) {
+      float v[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) v[t] = __ldcg(pa + (i + t) * stride);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) A = fmaf(v[t], sc[(i + t) * G + hh], A);
+    }
+    for (; i < n; ++i) A = fmaf(__ldcg(pa + i * stride), sc[i * G + hh], A);
+    const float M = mz[2 * hh], Z = mz[2 * hh + 1];
+    const size_t qh = size_t(I.b) * a.H_q + size_t(I.g) * G + hh;
+    a.out[qh * D + dim] = A / Z;
+    if (emit && dim == 0) {
+      a.stats[qh * 2] = M;
+      a.stats[qh * 2 + 1] = Z;
+    }
+  }
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
     attn_kernel(const __grid_constant__ AttnArgs a) {
   using C = AttnCfg<T, D, G>;
   extern __shared__ __align__(1024) unsigned char smem[];
+  // launched as a programmatic dependent: wait until the previous grid on the
+  // stream has completed and its writes are visible before any global access
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_units = a.B * a.H_kv;
   int* units = reinterpret_cast<int*>(smem + C::OFF_UNITS);
@@ -834,35 +954,7 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
       named_bar_sync(1, nct);
       if (misc[kMiscLast]) {
         __threadfence();
-        for (int j = tid; j < G * D; j += nct) {
-          const int hh = j / D, dim = j % D;
-          const float* pbase = a.partials + (size_t(I.first) * G + hh) * (D + 2);
-          const size_t pstride = size_t(G) * (D + 2);
-          // pass 1: the global max (independent loads)
-          float M = -INFINITY;
-          int i = 0;
-          for (; i + 4 <= I.n_items; i += 4) {
-            const float m0 = __ldcg(pbase + (i + 0) * pstride), m1 = __ldcg(pbase + (i + 1) * pstride);
-            const float m2 = __ldcg(pbase + (i + 2) * pstride), m3 = __ldcg(pbase + (i + 3) * pstride);
-            M = fmaxf(M, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
-          }
-          for (; i < I.n_items; ++i) M = fmaxf(M, __ldcg(pbase + i * pstride));
-          // pass 2: rescaled sums
-          float A = 0.f, Z = 0.f;
-#pragma unroll 4
-          for (i = 0; i < I.n_items; ++i) {
-            const float* p = pbase + i * pstride;
-            const float sc = exp2f(__ldcg(p) - M);
-            Z = fmaf(__ldcg(p + 1), sc, Z);
-            A = fmaf(__ldcg(p + 2 + dim), sc, A);
-          }
-          const size_t qh = size_t(I.b) * a.H_q + size_t(I.g) * G + hh;
-          a.out[qh * D + dim] = A / Z;
-          if (emit && dim == 0) {
-            a.stats[qh * 2] = M;
-            a.stats[qh * 2 + 1] = Z;
-          }
-        }
+        attn_merge_items<D, G>(a, I, emit, red_all, tid, nct);
         if (tid == 0) a.counters[I.u] = 0;
       }
     }
@@ -878,9 +970,17 @@ cudaError_t launch_attn_t(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<T, D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  const int grid = device_sm_count();
-  attn_kernel<T, D, G><<<grid, C::NT, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count());
+  cfg.blockDim = dim3(C::NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_kernel<T, D, G>, a);
 }
 
 }  // namespace sfi

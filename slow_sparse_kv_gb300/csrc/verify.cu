@@ -50,7 +50,9 @@ struct VerifyCfg {
   static constexpr size_t OFF_RED = OFF_BAR + (2 * NS + 2 * kItemRing) * 8;
   static constexpr size_t OFF_MISC = OFF_RED + RED_B;
   static constexpr size_t OFF_UNITS = OFF_MISC + 128;
-  static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1) * 4; }
+  static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1 + kRankWords) * 4; }
+  static_assert(OFF_UNITS + (size_t(kMaxUnits) + 1 + kRankWords) * 4 <= size_t(227) * 1024,
+                "shared memory plan exceeds 227 KB");
   static __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
     return uint32_t((c >> 3) * (SR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
   }
