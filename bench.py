@@ -501,8 +501,9 @@ def run_kernel_cases(args):
     import slow_sparse_kv_gb300 as sfi
     wl = W.cfg2(n_layers=1, n_steps=1)
     wl.shape = W.Shape(args.case_batch, 32, 8, 128, "bf16")
-    wl.n0 = [wl.n0[i % len(wl.n0)] for i in range(args.case_batch)]
-    wl.cap = [wl.cap[i % len(wl.cap)] for i in range(args.case_batch)]
+    ctx_len = args.case_context or wl.n0[0]
+    wl.n0 = [ctx_len] * args.case_batch
+    wl.cap = [ctx_len + (wl.cap[0] - wl.n0[0])] * args.case_batch
     R = Cfg2Runner(wl, 0)
     sh = wl.shape
     B = sh.batch
@@ -647,6 +648,9 @@ def main():
     ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast: time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
     ap.add_argument("--case-batch", type=int, default=2)
+    ap.add_argument("--case-context", type=int, default=0,
+                    help="context of the --kernel-case layer (default: the 131072 of the decode "
+                         "benchmark); the fast step's work does not depend on it")
     ap.add_argument("--ragged-sweep", action="store_true", help="time one mixed slow/fast step of "
                     "the 32-sequence ragged batch for k in {1024, 4096, 16384} x window in {128, 256, 512}")
     args = ap.parse_args()

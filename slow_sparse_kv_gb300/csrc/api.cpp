@@ -142,7 +142,7 @@ namespace {
 
 // Length of a launch, in stage times of a CTA streaming at its fair share of
 // HBM, when `grid` CTAs take items in order (n_a units of rows_a rows, then
-// n_b units of rows_b rows, each split into items of rpi rows).  While items
+// n_b units of rows_b rows, each split into ceil(rows / rpi) items).  While items
 // remain every CTA is busy and all stream at the same rate (list scheduling
 // with a min-heap of the CTAs' free times).  Once the last item is taken the
 // CTAs that are still busy share HBM among fewer streams and speed up, each
@@ -166,13 +166,12 @@ double simulate_launch(long long n_a, int rows_a, long long n_b, int rows_b, lon
     const long long n = cls == 0 ? n_a : n_b;
     const int rows = cls == 0 ? rows_a : rows_b;
     if (n <= 0 || rows <= 0) continue;
-    const long long full = rows / rpi, rem = rows - full * rpi;
-    const double c_full = double(ceil_div(rpi, sr)) + kItemCost;
-    const double c_rem = double(ceil_div(rem, sr)) + kItemCost;
-    for (long long u = 0; u < n; ++u) {
-      for (long long i = 0; i < full; ++i) take(c_full);
-      if (rem > 0) take(c_rem);
-    }
+    // k items per unit share the unit's S stages cyclically: S % k items
+    // of S / k + 1 stages, then the rest of S / k
+    const long long k = ceil_div(rows, rpi), S = ceil_div(rows, sr);
+    const long long q = S / k, r = S % k;
+    for (long long u = 0; u < n; ++u)
+      for (long long i = 0; i < k; ++i) take(double(q + (i < r ? 1 : 0)) + kItemCost);
   }
   // the tail: remaining work of every CTA after the last item was taken
   double t = t_last, done = 0.0;

@@ -168,8 +168,14 @@ __device__ __forceinline__ int ring_read(const AttnArgs& a, const ItemRing& r, u
   return it;
 }
 
+// Work item: item i of the n_items items of unit u takes the unit's stages
+// i, i + n_items, i + 2 n_items, ... (n_st of them; stage s covers rows
+// [s * SR, min((s + 1) * SR, rows))).  The items of a unit thus have equal
+// shares (within one stage) and the CTAs that share a unit read
+// neighbouring addresses.
 struct ItemInfo {
-  int u, b, g, r0, r1, n, first, n_items;
+  int u, b, g, n, first, n_items;
+  int rows, c_first, c_step, n_st;
   bool slow;
 };
 
@@ -274,7 +280,7 @@ __device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int
 }
 
 __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* units, int n_units,
-                                                 int it) {
+                                                 int it, int sr) {
   // largest u with units[u] <= it
   int lo = 0, hi = n_units - 1;
   while (lo < hi) {
@@ -288,9 +294,12 @@ __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* u
   I.g = I.u % a.H_kv;
   I.first = units[lo];
   I.n_items = units[lo + 1] - units[lo];
-  const int rows = attn_unit_rows(a, I.u, false);
-  I.r0 = (it - I.first) * a.rows_per_item;
-  I.r1 = min(rows, I.r0 + a.rows_per_item);
+  I.rows = attn_unit_rows(a, I.u, false);
+  const int i = it - I.first, k = I.n_items;
+  const int n_stages = (I.rows + sr - 1) / sr;
+  I.c_first = i * sr;
+  I.c_step = k * sr;
+  I.n_st = (n_stages - i + k - 1) / k;
   I.n = a.len[I.b];
   I.slow = seq_is_slow(a.slow, I.b);
   return I;
@@ -320,7 +329,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
     const int it = pw == 0 ? ring_fetch_publish(a, total, ring, iseq, abort_flag, lane)
                            : ring_read(a, ring, iseq, abort_flag, lane);
     if (it < 0) break;
-    const ItemInfo I = attn_resolve(a, units, n_units, it);
+    const ItemInfo I = attn_resolve(a, units, n_units, it, C::SR);
     const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
     const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
     const char* vb = reinterpret_cast<const char*>(a.v) + head0 * C::ES;
@@ -336,13 +345,13 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
     if constexpr (C::MMA) {
       const long long off = a.kv_offset[I.b];
       row0 = off / D + (long long)I.g * a.kv_cap[I.b];
-      tma_unit = a.use_tma && tma_ok && I.slow && off % D == 0 && row0 + I.r1 < (1LL << 31);
+      tma_unit = a.use_tma && tma_ok && I.slow && off % D == 0 && row0 + I.rows < (1LL << 31);
     }
     // Row positions of stage c0 (lane l: rows l, l + 32, ...).  Gathered
     // positions come from the index list in global memory, so the loads
     // for the next stage are issued one stage ahead of their use.
     auto resolve_pos = [&](int c0s, int (&out)[PJ]) {
-      const int nrs = min(C::SR, I.r1 - c0s);
+      const int nrs = min(C::SR, I.rows - c0s);
 #pragma unroll
       for (int j = 0; j < PJ; ++j) {
         const int r = rbase + lane + 32 * j;
@@ -361,9 +370,10 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
       }
     };
     int pos_next[PJ];
-    resolve_pos(I.r0, pos_next);
-    for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
-      const int nr = min(C::SR, I.r1 - c0);
+    resolve_pos(I.c_first, pos_next);
+    for (int si = 0; si < I.n_st; ++si) {
+      const int c0 = I.c_first + si * I.c_step;
+      const int nr = min(C::SR, I.rows - c0);
       const int slot = stage % C::NS;
       const uint32_t ph = (stage / C::NS) & 1u;
       int pos[PJ];
@@ -376,7 +386,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
         }
         pos[j] = p;
       }
-      if (c0 + C::SR < I.r1) resolve_pos(c0 + C::SR, pos_next);
+      if (si + 1 < I.n_st) resolve_pos(c0 + I.c_step, pos_next);
       if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
         ok = false;
         break;
@@ -464,8 +474,9 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
       for (int e = 0; e < C::EPL; ++e) acc[hh][e] = 0.f;
     }
 
-    for (int c0 = I.r0; c0 < I.r1; c0 += C::SR) {
-      const int nr = min(C::SR, I.r1 - c0);
+    for (int si = 0; si < I.n_st; ++si) {
+      const int c0 = I.c_first + si * I.c_step;
+      const int nr = min(C::SR, I.rows - c0);
       const int slot = stage % C::NS;
       const uint32_t ph = (stage / C::NS) & 1u;
       // On a failed wait the warp skips the stage but keeps walking the
@@ -640,9 +651,10 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
   for (int c = 0; c < NTD; ++c) acc[c][0] = acc[c][1] = 0.f;
   float m = -INFINITY, zl = 0.f;
 
-  for (int c0 = I.r0; c0 < I.r1; c0 += C::SR, ++stage) {
+  for (int si = 0; si < I.n_st; ++si, ++stage) {
     if (int(stage & 1u) != wpar) continue;
-    const int nr = min(C::SR, I.r1 - c0);
+    const int c0 = I.c_first + si * I.c_step;
+    const int nr = min(C::SR, I.rows - c0);
     const int slot = stage % C::NS;
     const uint32_t ph = (stage / C::NS) & 1u;
     const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
@@ -901,7 +913,7 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
     const int it = *cur_item;
     named_bar_sync(1, nct);
     if (it < 0) break;
-    const ItemInfo I = attn_resolve(a, units, n_units, it);
+    const ItemInfo I = attn_resolve(a, units, n_units, it, C::SR);
     const bool emit = a.emit && I.slow;
     float* red = red_all + warp * G * (D + 2);
     // Tensor-core warps split stages by the parity of the CTA's running stage

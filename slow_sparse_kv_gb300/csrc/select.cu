@@ -202,6 +202,20 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, ui
   return r;
 }
 
+// The j-th sequence (in increasing order) whose bit is set in m, or -1.
+__device__ __forceinline__ int active_seq(const SeqMask& m, int j) {
+  for (int w = 0; w < kMaxBatch / 32; ++w) {
+    uint32_t bits = m.bits[w];
+    const int c = __popc(bits);
+    if (j < c) {
+      for (int i = 0; i < j; ++i) bits &= bits - 1;
+      return 32 * w + __ffs(bits) - 1;
+    }
+    j -= c;
+  }
+  return -1;
+}
+
 // One cluster of kSelCluster CTAs per unit; CTA `rank` owns the positions
 // [rank * ch, (rank + 1) * ch) of [0, n) and keeps their scores in shared
 // memory.  Cluster-wide quantities (the key-norm sum over E, the radix
@@ -227,10 +241,14 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
 
   const int tid = threadIdx.x;
   const int rank = int(cl.block_rank());
-  const int unit = blockIdx.x / kSelCluster;
+  // clusters are launched for the active units only: cluster c serves the
+  // (c / units-per-sequence)-th active sequence
   const bool per_seq = a.mode == SFI_SELECT_LOGIT_SUM_SEQ;
-  const int b = per_seq ? unit : unit / a.H_kv;
-  if (!seq_is_slow(a.active, b)) return;  // uniform over the cluster
+  const int ups = per_seq ? 1 : a.H_kv;  // units per sequence
+  const int c = blockIdx.x / kSelCluster;
+  const int b = active_seq(a.active, c / ups);
+  if (b < 0 || b >= a.B) return;  // uniform over the cluster (cannot happen for a valid grid)
+  const int unit = per_seq ? b : b * a.H_kv + c % ups;
   const int u = per_seq ? b * a.H_kv : unit;
   const int n = a.len[b];
   if (n < 1 || n > a.max_len) {
@@ -485,7 +503,10 @@ cudaError_t launch_select_t(const SelectArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel<EV_G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  const int units = a.mode == SFI_SELECT_LOGIT_SUM_SEQ ? a.B : a.B * a.H_kv;
+  int n_active = 0;
+  for (int b = 0; b < a.B; ++b) n_active += int((a.active.bits[b >> 5] >> (b & 31)) & 1u);
+  const int units = n_active * (a.mode == SFI_SELECT_LOGIT_SUM_SEQ ? 1 : a.H_kv);
+  if (units == 0) return cudaSuccess;
   select_cluster_kernel<EV_G><<<units * kSelCluster, kSelCT, smem, st>>>(a);
   return cudaGetLastError();
 }

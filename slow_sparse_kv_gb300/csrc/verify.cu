@@ -107,8 +107,9 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
   const float qs = a.qscale;
   const int n_pre = I.n - va.R;
 
-  for (int c0 = I.r0; c0 < I.r1; c0 += C::SR, ++stage) {
-    const int nr = min(C::SR, I.r1 - c0);
+  for (int si = 0; si < I.n_st; ++si, ++stage) {
+    const int c0 = I.c_first + si * I.c_step;
+    const int nr = min(C::SR, I.rows - c0);
     const int slot = stage % C::NS;
     const uint32_t ph = (stage / C::NS) & 1u;
     const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
     const int it = *cur_item;
     named_bar_sync(1, nct);
     if (it < 0) break;
-    const ItemInfo I = attn_resolve(a, units, n_units, it);
+    const ItemInfo I = attn_resolve(a, units, n_units, it, C::SR);
     verify_item<D, G>(va, I, smem, bar_full, bar_empty, abort_flag, stage, warp, lane,
                       red_all + warp * 16 * (D + 2));
     named_bar_sync(1, nct);
