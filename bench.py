@@ -78,6 +78,27 @@ def schedule_counts(slow_masks: np.ndarray):
     return s, int(slow_masks.size - s)
 
 
+# DRAM traffic of the attention kernel relative to its algorithmic bytes,
+# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# decode driver's mixed launch: batch 8 at context 131072, sequence 0
+# refreshing and seven fast -- 662.87 MB read + 6.90 MB written for
+# 661.77 MB algorithmic.  It holds for the kernel sources it was taken on
+# (their SHA-256 below); after any change the roofline reports null traffic
+# until the capture is repeated.
+ATTN_TRAFFIC = {"ratio": (662873856 + 6903552) / 661766144,
+                "sources": ["attn_kernel.cuh", "attn_bf16.cu", "common.cuh", "sfi_internal.h", "api.cpp"],
+                "sha256": "9eafb4f5d125c1b7575f0caaab421d86a345938b713313b6a665de8930c8b639"}
+
+
+def attn_traffic_ratio():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ATTN_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, "slow_sparse_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return ATTN_TRAFFIC["ratio"] if h.hexdigest() == ATTN_TRAFFIC["sha256"] else None
+
+
 def attention_bytes(wl: W.Workload, slow_masks: np.ndarray) -> float:
     """Algorithmic bytes the attention launches read: the whole K and V of a slow
     (sequence, layer) step, and the gathered sink + selected + window rows of a
@@ -295,9 +316,10 @@ class Cfg2Runner:
         self.vp = [t.data_ptr() for t in self.V]
         self.op = [t.data_ptr() for t in self.out]
 
-    def decode_pass(self, q_ptrs=None, token_events=None, h2d=None, d2h=None):
-        """One whole decode pass.  q_ptrs[t][l] overrides the query pointers;
-        h2d(t) / d2h(t) enqueue the per-token host copies (end-to-end mode)."""
+    def decode_pass(self, q_ptrs=None, token_events=None, h2d=None, d2h=None, o_ptrs=None):
+        """One whole decode pass.  q_ptrs(t, l) / o_ptrs(t, l) override the query
+        and output pointers; h2d(t) / d2h(t) enqueue the per-token host copies
+        (end-to-end mode)."""
         sfi, wl = self.sfi, self.wl
         lib, h = sfi.lib, self.ctx.h
         st = self.stream.cuda_stream
@@ -312,7 +334,8 @@ class Cfg2Runner:
             lay = ctypes.byref(self.layouts[t])
             for l in range(L):
                 qp = self.Q[l][t].data_ptr() if q_ptrs is None else q_ptrs(t, l)
-                r = lib.sfi_decode_step(h, l, self.bnd[t], lay, qp, self.kp[l], self.vp[l], self.op[l], st)
+                op = self.op[l] if o_ptrs is None else o_ptrs(t, l)
+                r = lib.sfi_decode_step(h, l, self.bnd[t], lay, qp, self.kp[l], self.vp[l], op, st)
                 if r != 0:
                     raise sfi.SfiError("sfi_decode_step", r)
             if token_events is not None:
@@ -365,19 +388,27 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    R.ctx.profile(True)
+    # Nothing is recorded between the launches of the timed passes: an event
+    # between two attention launches would break their programmatic
+    # dependence (the next launch could no longer start as the previous one
+    # drains), so the per-launch timings come from separate passes below.
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for s in range(args.steps):
-        R.decode_pass(token_events=ev)
-        if s == args.steps - 1:
-            pass
+        R.decode_pass()
     e1.record()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
     total_ms = e0.elapsed_time(e1)
+    # ---------------- profiled passes (the same work): CUDA events around every
+    # attention and selector launch on its own stream (roofline, breakdown) and
+    # around every token (fast vs refresh token times)
+    R.ctx.profile(True)
+    for s in range(args.steps):
+        R.decode_pass(token_events=ev)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
     attn_ms, attn_n, sel_ms, sel_n = R.ctx.profile_read()
     R.ctx.profile(False)
     for t in range(T):  # token times of the last pass
@@ -393,28 +424,57 @@ def run_ours(args, rank, world, local_rank):
     for l in range(L):
         q_host[:, l].copy_(R.Q[l].cpu())
     o_host = torch.empty(T, L, B, sh.n_q_heads, sh.head_dim, dtype=torch.float32, pin_memory=True)
-    q_stage = torch.empty(L, B, sh.n_q_heads, sh.head_dim, dtype=dt, device=R.dev)
-    out_all = torch.stack(R.out)  # [L, B, H_q, d] staging of the outputs
-    R.op = [out_all[l].data_ptr() for l in range(L)]
-    h2d_bytes = q_stage.numel() * q_stage.element_size()
-    d2h_bytes = out_all.numel() * 4
+    # A serving loop: the copies run on their own stream, double-buffered, so
+    # token t's outputs go back and token t+1's queries come in while the
+    # decode stream computes; events order each copy against the compute that
+    # produces or consumes its buffer.
+    q_stage = torch.empty(2, L, B, sh.n_q_heads, sh.head_dim, dtype=dt, device=R.dev)
+    o_stage = torch.empty(2, L, B, sh.n_q_heads, sh.head_dim, dtype=torch.float32, device=R.dev)
+    h2d_bytes = q_stage[0].numel() * q_stage.element_size()
+    d2h_bytes = o_stage[0].numel() * 4
+    # one stream per direction: an upload queued behind a download would wait
+    # for the compute that the download waits for
+    cs_in, cs_out = torch.cuda.Stream(device=R.dev), torch.cuda.Stream(device=R.dev)
+    main = R.stream
+    ev = lambda: torch.cuda.Event(blocking=False)
+    q_ready, q_free = [ev(), ev()], [ev(), ev()]
+    o_done, o_free = [ev(), ev()], [ev(), ev()]
+    for e in q_free + o_free:
+        e.record(main)
 
     def h2d(t):
-        q_stage.copy_(q_host[t], non_blocking=True)
+        p = t & 1
+        cs_in.wait_event(q_free[p])           # token t-2 has read this buffer
+        with torch.cuda.stream(cs_in):
+            q_stage[p].copy_(q_host[t], non_blocking=True)
+        q_ready[p].record(cs_in)
+        main.wait_event(q_ready[p])
+        main.wait_event(o_free[p])            # token t-2's outputs have left this buffer
 
     def d2h(t):
-        o_host[t].copy_(out_all, non_blocking=True)
+        p = t & 1
+        q_free[p].record(main)
+        o_done[p].record(main)
+        cs_out.wait_event(o_done[p])
+        with torch.cuda.stream(cs_out):
+            o_host[t].copy_(o_stage[p], non_blocking=True)
+        o_free[p].record(cs_out)
 
-    qp = [q_stage[l].data_ptr() for l in range(L)]
+    qp = [[q_stage[p][l].data_ptr() for l in range(L)] for p in range(2)]
+    opp = [[o_stage[p][l].data_ptr() for l in range(L)] for p in range(2)]
+    e_kw = dict(q_ptrs=lambda t, l: qp[t & 1][l], o_ptrs=lambda t, l: opp[t & 1][l], h2d=h2d, d2h=d2h)
     e_steps = max(1, min(args.steps, 3))
-    R.decode_pass(q_ptrs=lambda t, l: qp[l], h2d=h2d, d2h=d2h)  # warm
+    R.decode_pass(**e_kw)  # warm
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
+    e2e_pass_s = []
     for _ in range(e_steps):
-        R.decode_pass(q_ptrs=lambda t, l: qp[l], h2d=h2d, d2h=d2h)
-    torch.cuda.synchronize()
+        tp = time.perf_counter()
+        R.decode_pass(**e_kw)
+        torch.cuda.synchronize()
+        e2e_pass_s.append(round(time.perf_counter() - tp, 4))
     e2e_s = aggregate_max(time.perf_counter() - t0, world)
     e2e_rate = world * T * e_steps / e2e_s
     # ---------------- full-KV dense baseline (every step dense, no evidence)
@@ -435,6 +495,9 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- roofline of the attention kernel (all its launches in the timed region)
     peak, peak_kind = measured_peak_gbs()
     achieved = (alg_bytes * args.steps) / (attn_ms / 1e3) / 1e9
+    ratio = attn_traffic_ratio()
+    # per launch, like `achieved`: DRAM bytes of an average attention launch of the pass
+    traffic = None if ratio is None else round(ratio * alg_bytes * args.steps / attn_n)
     gpu_launches = int(attn_n + sel_n)
     line = {
         "metric": "SFI decode steps/s (slow & fast) and achieved HBM GB/s as % of GB300 peak",
@@ -473,13 +536,19 @@ def run_ours(args, rank, world, local_rank):
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "traffic_note": "bytes per attention launch: the ncu DRAM/algorithmic ratio of the "
+                            "mixed launch times this pass's algorithmic bytes per launch",
+            "algorithmic_bytes_per_launch": round(alg_bytes * args.steps / attn_n),
+            "timing": "CUDA events around every attention launch on its stream, over K profiled "
+                      "passes of the same work run right after the timed passes",
             "kernel": "sfi attention (mixed slow/fast launch)",
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
             "algorithmic_bytes_per_pass": alg_bytes,
         },
         "e2e": {"value": round(e2e_rate, 3), "unit": "decode steps/s",
-                "h2d_bytes_per_step": int(h2d_bytes * T), "d2h_bytes_per_step": int(d2h_bytes * T)},
+                "h2d_bytes_per_step": int(h2d_bytes * T), "d2h_bytes_per_step": int(d2h_bytes * T),
+                "pass_s": e2e_pass_s},
         "gpu_launches": gpu_launches,
         "device_status": status,
     }
@@ -528,6 +597,22 @@ def run_kernel_cases(args):
         "fast": (lambda: sfi.sfi_fast_attn(lay, prm, q, R.K[0], R.V[0], idx, cnt, out, ws),
                  B * (wl.n_sink + wl.k + wl.window) * row),
     }
+    # "mixed": one decode-step launch of the decode driver with sequence 0
+    # refreshing (dense + evidence) and the others fast, as in a refresh step
+    # of the decode benchmark; its selector runs in line after it.
+    dctx = None
+    if "mixed" in args.kernel_case.split(","):
+        dctx = sfi.DecodeContext(B, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16, R.max_len, 1,
+                                 prm, 0, async_select=False)
+        all_slow = (ctypes.c_uint8 * B)(*([1] * B))
+        one_slow = (ctypes.c_uint8 * B)(*([1] + [0] * (B - 1)))
+        st = R.stream.cuda_stream
+        assert sfi.lib.sfi_decode_step(dctx.h, 0, all_slow, R.layouts[0], q.data_ptr(), R.kp[0], R.vp[0],
+                                       R.op[0], st) == 0
+        dctx.profile(True)
+        cases["mixed"] = (lambda: sfi.lib.sfi_decode_step(dctx.h, 0, one_slow, R.layouts[0], q.data_ptr(),
+                                                           R.kp[0], R.vp[0], R.op[0], st),
+                          n * row + (B - 1) * (wl.n_sink + wl.k + wl.window) * row)
     res = {}
     cases["slow"][0]()
     cases["select"][0]()
@@ -536,6 +621,9 @@ def run_kernel_cases(args):
         fn, nbytes = cases[name]
         times = []
         for i in range(args.warmup + args.steps):
+            if name == "mixed" and i == args.warmup:
+                torch.cuda.synchronize()
+                dctx.profile(True)  # restart: count the timed repetitions only
             flush.fill_(i & 0xFF)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -546,6 +634,14 @@ def run_kernel_cases(args):
                 times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
         res[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / ms / 1e6, 1), "bytes": nbytes}
+        if name == "mixed":
+            a_ms, a_n, s_ms, s_n = dctx.profile_read()
+            res[name]["attention_ms"] = round(a_ms / a_n, 4)
+            res[name]["attention_GB/s"] = round(nbytes / (a_ms / a_n) / 1e6, 1)
+            res[name]["select_ms"] = round(s_ms / max(s_n, 1), 4)
+    if dctx is not None:
+        res["mixed_device_status"] = dctx.read_status()
+        dctx.close()
     res["device_status"] = sfi.sfi_read_status(ws)
     return {"kernel_cases": res, "batch": B, "context": n}
 
@@ -645,7 +741,7 @@ def main():
     ap.add_argument("--sync-select", action="store_true",
                     help="run each layer's selector on the decode stream instead of overlapping it "
                          "with the next layer's attention")
-    ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast: time "
+    ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast,mixed: time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
     ap.add_argument("--case-batch", type=int, default=2)
     ap.add_argument("--case-context", type=int, default=0,
