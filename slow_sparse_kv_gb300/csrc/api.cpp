@@ -20,8 +20,8 @@
 
 namespace sfi {
 
-cudaError_t launch_attn_f32(const AttnArgs& a, int D, int G, cudaStream_t st);
-cudaError_t launch_attn_bf16(const AttnArgs& a, int D, int G, cudaStream_t st);
+cudaError_t launch_attn_f32(const AttnArgs& a, int D, int G, cudaStream_t st, bool pdl);
+cudaError_t launch_attn_bf16(const AttnArgs& a, int D, int G, cudaStream_t st, bool pdl);
 int attn_stage_rows_f32(int D);
 int attn_stage_rows_bf16(int D);
 
@@ -318,12 +318,12 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
 }
 
 sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,
-                    long long n_fast_units, int fast_rows, cudaStream_t st) {
+                    long long n_fast_units, int fast_rows, cudaStream_t st, bool pdl) {
   const int G = L->n_q_heads / L->n_kv_heads;
   a.rows_per_item = choose_rows_per_item(n_slow_units, slow_rows, n_fast_units, fast_rows,
                                          stage_rows(L->dtype, L->head_dim), device_sm_count());
-  const cudaError_t e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st)
-                                            : launch_attn_bf16(a, L->head_dim, G, st);
+  const cudaError_t e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st, pdl)
+                                            : launch_attn_bf16(a, L->head_dim, G, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SFI_OK;
 }

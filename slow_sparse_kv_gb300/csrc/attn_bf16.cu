@@ -4,9 +4,9 @@
 
 namespace sfi {
 
-cudaError_t launch_attn_bf16(const AttnArgs& a, int D, int G, cudaStream_t st) {
+cudaError_t launch_attn_bf16(const AttnArgs& a, int D, int G, cudaStream_t st, bool pdl) {
 #define SFI_CASE(DD, GG) \
-  if (D == DD && G == GG) return launch_attn_t<bf16_t, DD, GG>(a, st);
+  if (D == DD && G == GG) return launch_attn_t<bf16_t, DD, GG>(a, st, pdl);
   SFI_CASE(64, 1) SFI_CASE(64, 2) SFI_CASE(64, 4) SFI_CASE(64, 8)
   SFI_CASE(128, 1) SFI_CASE(128, 2) SFI_CASE(128, 4) SFI_CASE(128, 8)
 #undef SFI_CASE

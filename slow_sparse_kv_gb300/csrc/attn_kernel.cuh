@@ -975,7 +975,7 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_attn_t(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_attn_t(const AttnArgs& a, cudaStream_t st, bool pdl) {
   using C = AttnCfg<T, D, G>;
   const int n_units = a.B * a.H_kv;
   const size_t smem = C::smem_bytes(n_units);
@@ -991,7 +991,7 @@ cudaError_t launch_attn_t(const AttnArgs& a, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, attn_kernel<T, D, G>, a);
 }
 

@@ -33,6 +33,7 @@ struct sfi_ctx {
   int32_t* idx = nullptr;      // [L][B*H_kv][k]
   int32_t* count = nullptr;    // [L][B*H_kv]
   int n_sets = 1;
+  bool sel_in_flight = false;  // the last layer step sent its selector to the side stream
   cudaStream_t side = nullptr;
   cudaEvent_t attn_done[2] = {nullptr, nullptr}, sel_done[2] = {nullptr, nullptr};
   // host schedule state
@@ -187,6 +188,7 @@ sfi_status sfi_ctx_reset(sfi_ctx* c) {
   std::fill(c->since.begin(), c->since.end(), 0);
   std::fill(c->slow.begin(), c->slow.end(), 0);
   c->decided = false;
+  c->sel_in_flight = false;
   cudaError_t e = c->side ? cudaStreamSynchronize(c->side) : cudaSuccess;
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   for (int p = 0; p < c->n_sets && e == cudaSuccess; ++p) e = cudaMemset(c->ws[p], 0, c->plan.total);
@@ -331,8 +333,15 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   const int fast_bound = fast_unit_rows_bound(&Lc, &d.params);
   if (c->profiling) e = record_pair(c->ev_attn, c->n_attn_pending, c->attn_ms, false, st);
   if (e != cudaSuccess) return cuda_fail(e, "profiling event");
+  // Right after a layer whose selector went to the side stream, launch
+  // without programmatic dependence: this launch then becomes ready only when
+  // the previous one has completed -- together with that selector, which
+  // (higher priority) is placed first and runs beside this launch; as a
+  // programmatic dependent this launch would take every SM first.
+  const bool pdl = !c->sel_in_flight;
+  c->sel_in_flight = false;
   if ((s = run_attn(a, &Lc, (long long)n_slow * d.n_kv_heads, d.max_len,
-                    (long long)(d.batch - n_slow) * d.n_kv_heads, fast_bound, st)) != SFI_OK)
+                    (long long)(d.batch - n_slow) * d.n_kv_heads, fast_bound, st, pdl)) != SFI_OK)
     return s;
   if (c->profiling) {
     e = record_pair(c->ev_attn, c->n_attn_pending, c->attn_ms, true, st);
@@ -381,6 +390,7 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
     c->sel_launches += 1;
   }
   if (c->side) {
+    c->sel_in_flight = true;
     e = cudaEventRecord(c->sel_done[p], ss);
     // join at the last layer: the token's work ends on the caller's stream
     if (e == cudaSuccess && layer == d.n_layers - 1) e = cudaStreamWaitEvent(st, c->sel_done[p], 0);

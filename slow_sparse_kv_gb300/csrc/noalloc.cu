@@ -19,8 +19,8 @@
 
 namespace sfi {
 
-cudaError_t launch_attn_f32(const AttnArgs& a, int D, int G, cudaStream_t st);
-cudaError_t launch_attn_bf16(const AttnArgs& a, int D, int G, cudaStream_t st);
+cudaError_t launch_attn_f32(const AttnArgs& a, int D, int G, cudaStream_t st, bool pdl);
+cudaError_t launch_attn_bf16(const AttnArgs& a, int D, int G, cudaStream_t st, bool pdl);
 int attn_stage_rows_f32(int D);
 int attn_stage_rows_bf16(int D);
 
@@ -125,8 +125,8 @@ extern "C" sfi_status sfi_fast_attn_noalloc(const sfi_layout* L, const sfi_param
   if (rpi < balanced) rpi = balanced;
   rpi = (rpi + sr - 1) / sr * sr;
   a.rows_per_item = int(rpi);
-  e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st)
-                          : launch_attn_bf16(a, L->head_dim, G, st);
+  e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st, true)
+                          : launch_attn_bf16(a, L->head_dim, G, st, true);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SFI_OK;
 }

@@ -38,6 +38,20 @@ constexpr int kRadixPasses = 3;  // digits of 11, 11 and 10 bits
 constexpr int kRadixBins = 2048;
 constexpr int kRadixShift0 = 21;
 constexpr int kRadixShift1 = 10;
+// Largest cluster-wide count of keys in the k-th key's top bin for which the
+// two lower digits are found on a gathered list (it must fit two rows of the
+// total histograms).
+constexpr int kCandCap = 4096;
+static_assert(kCandCap <= (kRadixPasses - 1) * kRadixBins, "gathered list fits hist_g rows 1..2");
+
+// Dynamic shared memory of a selector CTA: its scores (ceil(max_len / 8)
+// floats), the candidate list, and, when it fits, a copy of its key norms.
+__host__ __device__ constexpr size_t select_cand_offset(int max_len) {
+  return (size_t((max_len + kSelCluster - 1) / kSelCluster) * sizeof(float) + 15) / 16 * 16;
+}
+__host__ __device__ constexpr size_t select_kn_offset(int max_len) {
+  return select_cand_offset(max_len) + size_t(kCandCap) * sizeof(uint32_t);
+}
 
 // Eight consecutive scores sc[o .. o+7] (o a multiple of 8, scores past `lim`
 // read as 0); two 16-byte shared-memory loads when the block is in range.
@@ -141,36 +155,6 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool acti
   }
 }
 
-// Pick the digit d with above(d) < krem <= above(d) + hist[d], where
-// above(d) counts keys in higher bins (NB bins).  Warp 0 only.
-template <int NB>
-__device__ void pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_digit,
-                           uint32_t* out_above) {
-  constexpr int PER = NB / 32;
-  const int lane = threadIdx.x & 31;
-  uint32_t sum = 0;
-  for (int j = 0; j < PER; ++j) sum += hist[NB - 1 - PER * lane - j];
-  uint32_t incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const uint32_t excl = incl - sum;
-  if (excl < krem && krem <= incl) {
-    uint32_t accum = excl;
-    for (int j = 0; j < PER; ++j) {
-      const uint32_t c = hist[NB - 1 - PER * lane - j];
-      if (accum + c >= krem) {
-        *out_digit = uint32_t(NB - 1 - PER * lane - j);
-        *out_above = accum;
-        break;
-      }
-      accum += c;
-    }
-  }
-}
-
 // Exclusive block scan of one packed (gt << 16 | eq) count per thread; also
 // returns the block total.  Two barriers.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t& total) {
@@ -200,6 +184,41 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, ui
   const uint32_t r = sh[w] + incl - v;
   __syncthreads();
   return r;
+}
+
+// Pick the digit d with above(d) < krem <= above(d) + hist[d] (above(d)
+// counts the keys in higher bins), with the whole block: thread t sums
+// NB / kSelCT consecutive bins from the top, a block scan gives the count
+// above its range, and the one thread whose range holds the krem-th key
+// walks its bins.  0 < krem <= the histogram's total.  Ends with a barrier.
+template <int NB>
+__device__ void block_pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_digit,
+                                 uint32_t* out_above, uint32_t* scan_sh) {
+  constexpr int PER = NB / kSelCT;
+  static_assert(PER * kSelCT == NB, "bins split evenly over the block");
+  const int top = NB - 1 - PER * int(threadIdx.x);  // bins top, top - 1, ..., top - PER + 1
+  uint32_t c[PER];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    c[j] = hist[top - j];
+    sum += c[j];
+  }
+  uint32_t tot;
+  const uint32_t excl = block_excl_scan(sum, scan_sh, tot);
+  if (excl < krem && krem <= excl + sum) {
+    uint32_t acc = excl;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      if (acc + c[j] >= krem) {
+        *out_digit = uint32_t(top - j);
+        *out_above = acc;
+        break;
+      }
+      acc += c[j];
+    }
+  }
+  __syncthreads();
 }
 
 // The j-th sequence (in increasing order) whose bit is set in m, or -1.
@@ -232,7 +251,13 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   extern __shared__ __align__(16) unsigned char sel_smem[];
   float* sc = reinterpret_cast<float*>(sel_smem);
   __shared__ uint32_t hist[kRadixBins];
-  __shared__ uint32_t hist_g[kRadixPasses][kRadixBins];  // cluster totals, used in rank 0
+  __shared__ uint32_t hist_loc[kRadixBins];  // this CTA's pass-0 histogram
+  // cluster totals, used in rank 0; on the candidate path rows 1-2 hold the
+  // gathered candidate keys
+  __shared__ uint32_t hist_g[kRadixPasses][kRadixBins];
+  // this CTA's keys in the k-th key's top bin (dynamic memory, after the scores)
+  uint32_t* cand = reinterpret_cast<uint32_t*>(sel_smem + select_cand_offset(a.max_len));
+  __shared__ uint32_t cand_n, sh_tau, sh_take, sh_off;
   __shared__ float shf[33];
   __shared__ float part_nu;
   __shared__ uint32_t cnt_gt, cnt_eq;
@@ -278,6 +303,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   // Positions are processed kSelU at a time per thread with every load
   // issued before any is used, so the loop is bound by bandwidth, not by the
   // latency of one load after another.
+  float* kns = a.kn_smem ? reinterpret_cast<float*>(sel_smem + select_kn_offset(a.max_len)) : nullptr;
   float part = 0.f;
   for (int base = p0; base < p1; base += kSelCT * kSelU) {
     float lg[kSelU][EV_G > 0 ? EV_G : 1];
@@ -304,6 +330,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       if (i < p1) {
         if constexpr (EV_G > 0) ev[j] = evidence_from_logits<EV_G>(lg[j], M, iz);
         sc[i - p0] = ev[j];
+        if (kns) kns[i - p0] = kv[j];
         part += kv[j];
       }
     }
@@ -333,7 +360,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
 #pragma unroll
     for (int j = 0; j < kSelU; ++j) {
       const int i = base + j * kSelCT + tid;
-      kv[j] = (!per_seq && i < p1 && i >= lo && i < hi) ? kn[i] : 0.f;
+      kv[j] = (!per_seq && i < p1 && i >= lo && i < hi) ? (kns ? kns[i - p0] : kn[i]) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kSelU; ++j) {
@@ -354,19 +381,115 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   int32_t* out_idx = a.idx + size_t(per_seq ? b * a.H_kv : unit) * a.k;
   if (need_radix) {
     // ------------------------------------------------------------ radix select
-    // Three passes of 11, 11 and 10 bits over the order keys of E.  Shared-
-    // memory reads go 8 positions per thread (two 16-byte loads) in tiles
-    // aligned to the CTA's first position.
+    // Digits of 11, 11 and 10 bits of the order keys of E.  Pass 0's
+    // histogram was built with the scores; its cluster total gives the top
+    // digit d0 of the k-th key.  Few keys share that digit (at the decode
+    // workloads about 2% of E), so when at most kCandCap do, each CTA lists
+    // its keys of bin d0 and rank 0 finishes the two lower digits on the
+    // gathered list alone; otherwise every CTA runs the two passes over all
+    // its keys.  Shared-memory reads go 8 positions per thread (two 16-byte
+    // loads) in tiles aligned to the CTA's first position.
     uint32_t prefix = 0, krem = uint32_t(keff);
     const int e0 = max(p0, lo), e1 = min(p1, hi);
-    for (int pass = 0; pass < kRadixPasses; ++pass) {
-      const int shift = pass == 0 ? kRadixShift0 : (pass == 1 ? kRadixShift1 : 0);
-      const int width = pass == 0 ? 32 - kRadixShift0 : (pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1);
-      const uint32_t dmask = (1u << width) - 1u;
-      if (pass > 0) {
+    for (int i = tid; i < kRadixBins; i += kSelCT) {
+      hist_loc[i] = hist[i];
+      if (hist[i]) atomicAdd(cl.map_shared_rank(&hist_g[0][i], 0), hist[i]);
+    }
+    if (tid == 0) cand_n = 0;
+    cl.sync();
+    for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = *cl.map_shared_rank(&hist_g[0][i], 0);
+    __syncthreads();
+    block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
+    const uint32_t d0 = sh_digit;
+    prefix = d0;
+    krem -= sh_above;
+    const uint32_t n_cand = hist[d0];  // keys of E with top digit d0, cluster-wide
+    uint32_t tau, take_eq, my_gt, my_eq;
+    if (n_cand <= uint32_t(kCandCap)) {
+      // ---- this CTA's keys of bin d0: into its own list and, at offset
+      // (keys of bin d0 in lower ranks), into rank 0's gathered list (the
+      // rows 1-2 of its total histograms, unused on this path)
+      const int lane = tid & 31;
+      if (tid < 32) {
+        uint32_t v = tid < rank ? *cl.map_shared_rank(&hist_loc[d0], tid) : 0u;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+        if (tid == 0) sh_off = v;
+      }
+      __syncthreads();
+      const uint32_t my_off = sh_off;
+      uint32_t* all_r0 = cl.map_shared_rank(&hist_g[1][0], 0);
+      for (int tb = p0; tb < e1; tb += kSelCT * 8) {
+        const int i0 = tb + tid * 8;
+        float v8[8];
+        load8(sc, i0 - p0, p1 - p0, v8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j;
+          const uint32_t key = order_key(v8[j]);
+          const bool m = i >= e0 && i < e1 && (key >> kRadixShift0) == d0;
+          const unsigned bal = __ballot_sync(kFull, m);
+          if (bal) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(&cand_n, uint32_t(__popc(bal)));
+            base = __shfl_sync(kFull, base, 0);
+            if (m) {
+              const uint32_t at = base + __popc(bal & ((1u << lane) - 1u));
+              cand[at] = key;
+              all_r0[my_off + at] = key;
+            }
+          }
+        }
+      }
+      cl.sync();  // every CTA's list is complete
+      if (rank == 0) {
+        const uint32_t* all = &hist_g[1][0];  // the n_cand gathered keys
+        for (int pass = 1; pass < kRadixPasses; ++pass) {
+          const int shift = pass == 1 ? kRadixShift1 : 0;
+          const int width = pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1;
+          const uint32_t dmask = (1u << width) - 1u;
+          const int hs = shift + width;
+          for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = 0;
+          __syncthreads();
+          for (uint32_t j0 = 0; j0 < n_cand; j0 += kSelCT) {
+            const uint32_t j = j0 + tid;
+            const uint32_t key = j < n_cand ? all[j] : 0u;
+            hist_add(hist, (key >> shift) & dmask, j < n_cand && (key >> hs) == prefix);
+          }
+          __syncthreads();
+          if (width == 11) block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
+          else block_pick_digit<1024>(hist, krem, &sh_digit, &sh_above, scan_sh);
+          prefix = (prefix << width) | sh_digit;
+          krem -= sh_above;
+        }
+        if (tid == 0) {
+          sh_tau = prefix;
+          sh_take = krem;
+        }
+      }
+      cl.sync();  // tau is known in rank 0; no list is read any more
+      tau = *cl.map_shared_rank(&sh_tau, 0);
+      take_eq = *cl.map_shared_rank(&sh_take, 0);
+      // this CTA's keys above tau: all of its bins above d0, and its list's
+      uint32_t g = 0, q = 0;
+      for (int i = tid; i < kRadixBins; i += kSelCT)
+        if (uint32_t(i) > d0) g += hist_loc[i];
+      for (uint32_t j = tid; j < cand_n; j += kSelCT) {
+        g += cand[j] > tau;
+        q += cand[j] == tau;
+      }
+      uint32_t tot;
+      block_excl_scan((g << 16) | q, scan_sh, tot);  // counts < 2^16 per CTA
+      my_gt = tot >> 16;
+      my_eq = tot & 0xffffu;
+    } else {
+      for (int pass = 1; pass < kRadixPasses; ++pass) {
+        const int shift = pass == 1 ? kRadixShift1 : 0;
+        const int width = pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1;
+        const uint32_t dmask = (1u << width) - 1u;
+        const int hs = shift + width;
         for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = 0;
         __syncthreads();
-        const int hs = shift + width;
         for (int tb = p0; tb < e1; tb += kSelCT * 8) {
           const int i0 = tb + tid * 8;
           float v8[8];
@@ -380,41 +503,41 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
           }
         }
         __syncthreads();
+        for (int i = tid; i < kRadixBins; i += kSelCT)
+          if (hist[i]) atomicAdd(cl.map_shared_rank(&hist_g[pass][i], 0), hist[i]);
+        cl.sync();
+        for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = *cl.map_shared_rank(&hist_g[pass][i], 0);
+        __syncthreads();
+        if (width == 11) block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
+        else block_pick_digit<1024>(hist, krem, &sh_digit, &sh_above, scan_sh);
+        prefix = (prefix << width) | sh_digit;
+        krem -= sh_above;
       }
-      for (int i = tid; i < kRadixBins; i += kSelCT)
-        if (hist[i]) atomicAdd(cl.map_shared_rank(&hist_g[pass][i], 0), hist[i]);
-      cl.sync();
-      for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = *cl.map_shared_rank(&hist_g[pass][i], 0);
-      __syncthreads();
-      if (tid < 32) {
-        if (width == 11) pick_digit<2048>(hist, krem, &sh_digit, &sh_above);
-        else pick_digit<1024>(hist, krem, &sh_digit, &sh_above);
-      }
-      __syncthreads();
-      prefix = (prefix << width) | sh_digit;
-      krem -= sh_above;
-    }
-    const uint32_t tau = prefix, take_eq = krem;
-    // ------------------------------------------------------------ compaction
-    uint32_t g_loc = 0, q_loc = 0;
-    for (int tb = p0; tb < e1; tb += kSelCT * 8) {
-      const int i0 = tb + tid * 8;
-      float v8[8];
-      load8(sc, i0 - p0, p1 - p0, v8);
+      tau = prefix;
+      take_eq = krem;
+      uint32_t g_loc = 0, q_loc = 0;
+      for (int tb = p0; tb < e1; tb += kSelCT * 8) {
+        const int i0 = tb + tid * 8;
+        float v8[8];
+        load8(sc, i0 - p0, p1 - p0, v8);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j;
-        const uint32_t key = order_key(v8[j]);
-        const bool in = i >= e0 && i < e1;
-        g_loc += in && key > tau;
-        q_loc += in && key == tau;
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j;
+          const uint32_t key = order_key(v8[j]);
+          const bool in = i >= e0 && i < e1;
+          g_loc += in && key > tau;
+          q_loc += in && key == tau;
+        }
       }
+      uint32_t tot;
+      block_excl_scan((g_loc << 16) | q_loc, scan_sh, tot);  // counts < 2^16 per CTA
+      my_gt = tot >> 16;
+      my_eq = tot & 0xffffu;
     }
-    const float gs = sel_block_sum(float(g_loc), shf);  // exact: counts < 2^24
-    const float qs = sel_block_sum(float(q_loc), shf);
+    // ------------------------------------------------------------ compaction
     if (tid == 0) {
-      cnt_gt = uint32_t(gs);
-      cnt_eq = uint32_t(qs);
+      cnt_gt = my_gt;
+      cnt_eq = my_eq;
     }
     cl.sync();
     uint32_t gt_before = 0, eq_before = 0;
@@ -493,13 +616,20 @@ cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-size_t select_smem_bytes(int max_len) {
-  return size_t((max_len + kSelCluster - 1) / kSelCluster) * sizeof(float);
+// Dynamic shared memory of a launch; the key-norm copy is kept when the CTA's
+// total stays within 227 KB (the static part is about 41 KB).
+size_t select_smem_bytes(int max_len, bool kn_smem) {
+  const size_t base = select_kn_offset(max_len);
+  return kn_smem ? base + size_t((max_len + kSelCluster - 1) / kSelCluster) * sizeof(float) : base;
 }
 
+bool select_kn_fits(int max_len) { return select_smem_bytes(max_len, true) <= size_t(180) * 1024; }
+
 template <int EV_G>
-cudaError_t launch_select_t(const SelectArgs& a, cudaStream_t st) {
-  const size_t smem = select_smem_bytes(a.max_len);
+cudaError_t launch_select_t(const SelectArgs& args, cudaStream_t st) {
+  SelectArgs a = args;
+  a.kn_smem = a.mode != SFI_SELECT_LOGIT_SUM_SEQ && select_kn_fits(a.max_len) ? 1 : 0;
+  const size_t smem = select_smem_bytes(a.max_len, a.kn_smem != 0);
   cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel<EV_G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;

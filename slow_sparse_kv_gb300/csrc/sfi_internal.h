@@ -84,6 +84,7 @@ struct SelectArgs {
   int32_t mode;
   SeqMask active;
   uint32_t* status;
+  int32_t kn_smem;  // set by the launcher: the CTAs keep their key norms in shared memory
 };
 
 // Verification attention (Vegas): R chain rows per head, collected logit sums.
@@ -117,8 +118,11 @@ sfi_status check_layout(const sfi_layout* L);
 sfi_status check_params(const sfi_params* P, bool for_select);
 void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const void* k,
                       const void* v, float* out, char* ws, const WsPlan& p);
+// pdl: launch as a programmatic dependent of the previous launch on `st`
+// (it may start while that launch drains; it waits for it before any global
+// access).
 sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,
-                    long long n_fast_units, int fast_rows, cudaStream_t st);
+                    long long n_fast_units, int fast_rows, cudaStream_t st, bool pdl = true);
 int fast_unit_rows_bound(const sfi_layout* L, const sfi_params* P);
 int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid);
 // Fill a.tmk / a.tmv for bf16 caches (sets a.use_tma; leaves it 0 if the
