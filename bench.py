@@ -244,7 +244,7 @@ class ClockSampler:
 class Cfg2Runner:
     """Device-resident decode workload driven through sfi_decode_step."""
 
-    def __init__(self, wl: W.Workload, device: int, async_select: bool = True):
+    def __init__(self, wl: W.Workload, device: int, async_select: bool = True, make_ctx: bool = True):
         import torch
         import slow_sparse_kv_gb300 as sfi
         self.torch, self.sfi, self.wl = torch, sfi, wl
@@ -308,9 +308,9 @@ class Cfg2Runner:
                                        lens[t].data_ptr()) for t in range(T)]
         self.trace = wl.boundary_trace()
         self.bnd = [(ctypes.c_uint8 * B)(*[int(x) for x in self.trace[t]]) for t in range(T)]
-        self.ctx = sfi.DecodeContext(B, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dt, self.max_len, L,
-                                     sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget,
-                                     async_select=async_select)
+        self.ctx = None if not make_ctx else sfi.DecodeContext(
+            B, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dt, self.max_len, L,
+            sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget, async_select=async_select)
         self.slow_masks = None
         self.kp = [t.data_ptr() for t in self.K]
         self.vp = [t.data_ptr() for t in self.V]
@@ -646,6 +646,49 @@ def run_kernel_cases(args):
     return {"kernel_cases": res, "batch": B, "context": n}
 
 
+def run_verify_cases(args):
+    """Vegas verification attention on the batch-4, 65536-prefix, gamma-4
+    workload (5 chain rows, G = 4): without logit sums, with Collect-2 (rows 0
+    and gamma) and with every row collected -- the cost of writing and
+    aggregating the logit sums.  CUDA events, median, 512 MB L2 flush between
+    repetitions."""
+    import torch
+    import slow_sparse_kv_gb300 as sfi
+    wl = W.cfg3()
+    wl.n_steps = 1
+    R = Cfg2Runner(wl, 0, make_ctx=False)
+    sh = wl.shape
+    B, rows = sh.batch, wl.gamma + 1
+    lens = [n + rows for n in wl.n0]
+    lay = sfi.Layout(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16, R.offsets, wl.cap, lens,
+                     R.max_len, device=R.dev)
+    ws = sfi.verify_workspace(lay, rows)
+    gen = torch.Generator(device=R.dev).manual_seed(wl.seed)
+    q = torch.randn(B, rows, sh.n_q_heads, sh.head_dim, device=R.dev, generator=gen).to(torch.bfloat16)
+    out = torch.empty(B, rows, sh.n_q_heads, sh.head_dim, device=R.dev)
+    lsum = torch.empty(B, sh.n_kv_heads, R.max_len, device=R.dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=R.dev)
+    nbytes = sum(2 * n * sh.n_kv_heads * sh.head_dim * 2 for n in lens)
+    cases = {"verify_no_sums": ([], None), "verify_collect2": ([0, wl.gamma], lsum),
+             "verify_all_rows": (list(range(rows)), lsum)}
+    res = {}
+    for name, (collect, ls) in cases.items():
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            sfi.sfi_verify_attn(lay, rows, collect, q, R.K[0], R.V[0], out, ls, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        res[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / ms / 1e6, 1), "bytes": nbytes}
+    res["device_status"] = sfi.sfi_read_status(ws)
+    return {"verify_cases": res, "batch": B, "prefix": wl.n0[0], "rows": rows, "workload": wl.name}
+
+
 def run_ragged_sweep(args):
     """Ragged serving batch (32 sequences, contexts log-uniform in [4096, 262144],
     25% at a boundary): per (k, window) point, an untimed all-slow step at n - 1
@@ -741,7 +784,7 @@ def main():
     ap.add_argument("--sync-select", action="store_true",
                     help="run each layer's selector on the decode stream instead of overlapping it "
                          "with the next layer's attention")
-    ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast,mixed: time "
+    ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast,mixed (or 'verify' alone): time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
     ap.add_argument("--case-batch", type=int, default=2)
     ap.add_argument("--case-context", type=int, default=0,
@@ -755,6 +798,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.ragged_sweep:
         print(json.dumps(run_ragged_sweep(args)), flush=True)
+        return
+    if args.kernel_case == "verify":
+        print(json.dumps(run_verify_cases(args)), flush=True)
         return
     if args.kernel_case:
         print(json.dumps(run_kernel_cases(args)), flush=True)

@@ -92,8 +92,9 @@ typedef struct {
 /* Selection and managed-state parameters (SFI pages, "Slow-Fast paradigm":
  * sink tokens, a recent window of about 256 tokens, selected memory). */
 typedef enum {
-  SFI_SELECT_FUSED = 0,        /* SFI: s = (1-lambda) f + lambda r per (b, KV head) */
-  SFI_SELECT_LOGIT_SUM_SEQ = 1 /* Vegas: top-k of the logit sum over all heads, one set per b */
+  SFI_SELECT_FUSED = 0,         /* SFI: s = (1-lambda) f + lambda r per (b, KV head) */
+  SFI_SELECT_LOGIT_SUM_SEQ = 1, /* Vegas: top-k of the logit sum over all heads, one set per b */
+  SFI_SELECT_LOGIT_SUM_HEAD = 2 /* Vegas grouped per KV head: top-k of each KV head's logit sum */
 } sfi_select_mode;
 
 typedef struct {
@@ -153,6 +154,11 @@ sfi_status sfi_slow_attn(const sfi_layout* layout, const void* q, const void* k,
  *   the top min(k, |P|) positions of L (ties to the lower position, ascending)
  *   are written to every KV head's row idx_out[b][g]; knorm is unused and
  *   lambda must be 0; s_out (if not NULL) receives L in row g = 0.
+ * SFI_SELECT_LOGIT_SUM_HEAD (Vegas, section 2.A with the head set of one KV
+ *   head), per (b, g): the top min(k, |P|) positions of P by that KV head's
+ *   logit sum evidence[b][g][i] (same order and tie rule, its own set per KV
+ *   head); knorm is unused, lambda and n_sink must be 0; s_out receives the
+ *   ranked values.
  * idx_out: [B][H_kv][k] int32; count_out: [B][H_kv] int32 (device). */
 size_t sfi_select_workspace_size(const sfi_layout* layout, const sfi_params* params);
 sfi_status sfi_select(const sfi_layout* layout, const sfi_params* params,
@@ -194,11 +200,14 @@ sfi_status sfi_fast_attn(const sfi_layout* layout, const sfi_params* params,
  *   logitsum_out[b][g][i] = sum over t in collect_rows, h in group g of
  *                           q_{t,h} . k_{g,i} / sqrt(d)      (natural units);
  * summing those rows over g gives the aggregated logits the selector's
- * SFI_SELECT_LOGIT_SUM_SEQ mode ranks (with window = n_rows, n_sink = 0).
+ * SFI_SELECT_LOGIT_SUM_SEQ mode ranks (with window = n_rows, n_sink = 0);
+ * SFI_SELECT_LOGIT_SUM_HEAD ranks each KV head's row on its own.
+ * collect_rows = {0, n_rows - 1} is Collect-2; every row (0 .. n_rows - 1)
+ * is the un-reduced aggregation of section 2.A.
  * q: [B][n_rows][H_q][d] bf16; out: [B][n_rows][H_q][d] fp32;
  * collect_rows: host array of n_collect distinct rows.
  * Limits (SFI_ERR_UNSUPPORTED beyond them): bf16 only; n_rows <= 8;
- * n_rows * G <= 32; n_collect * G <= 16.  The workspace is sized by
+ * n_rows * G <= 32.  The workspace is sized by
  * sfi_verify_attn_workspace_size (it holds n_rows * G partial rows per
  * work item). */
 size_t sfi_verify_attn_workspace_size(const sfi_layout* layout, int32_t n_rows);

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libsfi.so")
 
 SFI_OK, SFI_ERR_INVALID_ARG, SFI_ERR_UNSUPPORTED, SFI_ERR_CAPACITY, SFI_ERR_WORKSPACE, SFI_ERR_CUDA = range(6)
 SFI_F32, SFI_BF16 = 0, 1
-SFI_SELECT_FUSED, SFI_SELECT_LOGIT_SUM_SEQ = 0, 1
+SFI_SELECT_FUSED, SFI_SELECT_LOGIT_SUM_SEQ, SFI_SELECT_LOGIT_SUM_HEAD = 0, 1, 2
 SFI_DEV_LEN_OVER_CAP, SFI_DEV_BAD_INDEX, SFI_DEV_WAIT_TIMEOUT, SFI_DEV_ITEMS_OVERFLOW = 1, 2, 4, 8
 
 

@@ -113,9 +113,10 @@ sfi_status check_params(const sfi_params* P, bool for_select) {
                 P->window);
   if (!(P->lambda >= 0.f && P->lambda <= 1.f))
     return fail(SFI_ERR_INVALID_ARG, "lambda must lie in [0, 1] (got %g)", double(P->lambda));
-  if (P->mode != SFI_SELECT_FUSED && P->mode != SFI_SELECT_LOGIT_SUM_SEQ)
+  if (P->mode != SFI_SELECT_FUSED && P->mode != SFI_SELECT_LOGIT_SUM_SEQ &&
+      P->mode != SFI_SELECT_LOGIT_SUM_HEAD)
     return fail(SFI_ERR_INVALID_ARG, "unknown selection mode %d", P->mode);
-  if (for_select && P->mode == SFI_SELECT_LOGIT_SUM_SEQ && (P->lambda != 0.f || P->n_sink != 0))
+  if (for_select && P->mode != SFI_SELECT_FUSED && (P->lambda != 0.f || P->n_sink != 0))
     return fail(SFI_ERR_INVALID_ARG, "logit-sum selection takes lambda = 0 and n_sink = 0");
   if (!for_select && P->n_sink + (long long)P->window < 1)
     return fail(SFI_ERR_INVALID_ARG,
@@ -488,8 +489,6 @@ sfi_status sfi_verify_attn(const sfi_layout* L, int32_t n_rows, const int32_t* c
   if (logitsum_out) {
     if (n_collect < 0 || n_collect > n_rows || (n_collect > 0 && !collect_rows))
       return fail(SFI_ERR_INVALID_ARG, "collect_rows must list 0..n_rows distinct rows");
-    if (n_collect * G > 16)
-      return fail(SFI_ERR_UNSUPPORTED, "n_collect * G must be <= 16 (got %d)", n_collect * G);
     for (int i = 0; i < n_collect; ++i) {
       const int t = collect_rows[i];
       if (t < 0 || t >= n_rows || used[t])

@@ -269,6 +269,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   // clusters are launched for the active units only: cluster c serves the
   // (c / units-per-sequence)-th active sequence
   const bool per_seq = a.mode == SFI_SELECT_LOGIT_SUM_SEQ;
+  const bool prior = a.mode == SFI_SELECT_FUSED;  // key-norm prior and (1 - lambda) weight
   const int ups = per_seq ? 1 : a.H_kv;  // units per sequence
   const int c = blockIdx.x / kSelCluster;
   const int b = active_seq(a.active, c / ups);
@@ -288,7 +289,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   const int ch = (n_sc + kSelCluster - 1) / kSelCluster;
   const int p0 = min(n_sc, rank * ch), p1 = min(n_sc, p0 + ch);
   const bool need_radix = keff > 0 && keff < ne;
-  const float* kn = per_seq ? nullptr : a.knorm + size_t(u) * a.max_len;
+  const float* kn = prior ? a.knorm + size_t(u) * a.max_len : nullptr;
 
   // ---------------------------------------------------------------- evidence
   float M[EV_G > 0 ? EV_G : 1], iz[EV_G > 0 ? EV_G : 1];
@@ -321,7 +322,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
         } else {
           ev[j] = a.evidence[size_t(u) * a.max_len + i];
         }
-        if (!per_seq && i >= lo && i < hi) kv[j] = kn[i];
+        if (prior && i >= lo && i < hi) kv[j] = kn[i];
       }
     }
 #pragma unroll
@@ -341,26 +342,26 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       for (int j = 0; j < kRadixPasses; ++j) hist_g[j][i] = 0;
     }
   }
-  if (!per_seq) {
+  if (prior) {
     const float t = sel_block_sum(part, shf);
     if (tid == 0) part_nu = t;
   }
   cl.sync();  // partial norm sums and the zeroed cluster histograms are visible
   float coef = 0.f;
-  if (!per_seq) {
+  if (prior) {
     float tot = 0.f;
     for (int r = 0; r < kSelCluster; ++r) tot += *cl.map_shared_rank(&part_nu, r);
     coef = tot > 0.f ? a.lambda / tot : 0.f;
   }
   // ---------------------------------------------------------------- scores
   float* srow = a.s ? a.s + size_t(u) * a.max_len : nullptr;
-  const float w_f = per_seq ? 1.0f : 1.0f - a.lambda;
+  const float w_f = prior ? 1.0f - a.lambda : 1.0f;
   for (int base = p0; base < p1; base += kSelCT * kSelU) {
     float kv[kSelU];
 #pragma unroll
     for (int j = 0; j < kSelU; ++j) {
       const int i = base + j * kSelCT + tid;
-      kv[j] = (!per_seq && i < p1 && i >= lo && i < hi) ? (kns ? kns[i - p0] : kn[i]) : 0.f;
+      kv[j] = (prior && i < p1 && i >= lo && i < hi) ? (kns ? kns[i - p0] : kn[i]) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kSelU; ++j) {
@@ -369,7 +370,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       float v = 0.f;
       if (in) {
         v = w_f * sc[i - p0];
-        if (!per_seq && i >= lo && i < hi) v = fmaf(coef, kv[j], v);
+        if (prior && i >= lo && i < hi) v = fmaf(coef, kv[j], v);
         sc[i - p0] = v;
         if (srow) srow[i] = v;
       }
@@ -404,7 +405,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
     prefix = d0;
     krem -= sh_above;
     const uint32_t n_cand = hist[d0];  // keys of E with top digit d0, cluster-wide
-    uint32_t tau, take_eq, my_gt, my_eq;
+    uint32_t tau, take_eq;
     if (n_cand <= uint32_t(kCandCap)) {
       // ---- this CTA's keys of bin d0: into its own list and, at offset
       // (keys of bin d0 in lower ranks), into rank 0's gathered list (the
@@ -470,18 +471,6 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       cl.sync();  // tau is known in rank 0; no list is read any more
       tau = *cl.map_shared_rank(&sh_tau, 0);
       take_eq = *cl.map_shared_rank(&sh_take, 0);
-      // this CTA's keys above tau: all of its bins above d0, and its list's
-      uint32_t g = 0, q = 0;
-      for (int i = tid; i < kRadixBins; i += kSelCT)
-        if (uint32_t(i) > d0) g += hist_loc[i];
-      for (uint32_t j = tid; j < cand_n; j += kSelCT) {
-        g += cand[j] > tau;
-        q += cand[j] == tau;
-      }
-      uint32_t tot;
-      block_excl_scan((g << 16) | q, scan_sh, tot);  // counts < 2^16 per CTA
-      my_gt = tot >> 16;
-      my_eq = tot & 0xffffu;
     } else {
       for (int pass = 1; pass < kRadixPasses; ++pass) {
         const int shift = pass == 1 ? kRadixShift1 : 0;
@@ -515,66 +504,52 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       }
       tau = prefix;
       take_eq = krem;
-      uint32_t g_loc = 0, q_loc = 0;
-      for (int tb = p0; tb < e1; tb += kSelCT * 8) {
-        const int i0 = tb + tid * 8;
-        float v8[8];
-        load8(sc, i0 - p0, p1 - p0, v8);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + j;
-          const uint32_t key = order_key(v8[j]);
-          const bool in = i >= e0 && i < e1;
-          g_loc += in && key > tau;
-          q_loc += in && key == tau;
-        }
-      }
-      uint32_t tot;
-      block_excl_scan((g_loc << 16) | q_loc, scan_sh, tot);  // counts < 2^16 per CTA
-      my_gt = tot >> 16;
-      my_eq = tot & 0xffffu;
     }
     // ------------------------------------------------------------ compaction
+    // Ascending positions: warp w walks the contiguous segment
+    // [e0 + w * seg, ...) 32 positions per step (lane l takes base + l), so
+    // the order is (rank, warp, step, lane).  A counting walk, one block scan
+    // of the warps' counts and an exchange of the CTAs' totals give every
+    // warp its first output slot.
+    constexpr int NW = kSelCT / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int ne_cta = max(e1 - e0, 0);
+    const int seg = ((ne_cta + NW - 1) / NW + 31) / 32 * 32;
+    const int s0 = min(e1, e0 + warp * seg), s1 = min(e1, s0 + seg);
+    uint32_t wg = 0, wq = 0;
+    for (int base = s0; base < s1; base += 32) {
+      const int i = base + lane;
+      const uint32_t key = i < s1 ? order_key(sc[i - p0]) : 0u;
+      wg += __popc(__ballot_sync(kFull, i < s1 && key > tau));
+      wq += __popc(__ballot_sync(kFull, i < s1 && key == tau));
+    }
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(lane == 0 ? (wg << 16) | wq : 0u, scan_sh, tot);  // < 2^16 per CTA
+    const uint32_t w_ex = __shfl_sync(kFull, ex, 0);
     if (tid == 0) {
-      cnt_gt = my_gt;
-      cnt_eq = my_eq;
+      cnt_gt = tot >> 16;
+      cnt_eq = tot & 0xffffu;
     }
     cl.sync();
-    uint32_t gt_before = 0, eq_before = 0;
+    uint32_t gb = w_ex >> 16, qb = w_ex & 0xffffu;
     for (int r = 0; r < rank; ++r) {
-      gt_before += *cl.map_shared_rank(&cnt_gt, r);
-      eq_before += *cl.map_shared_rank(&cnt_eq, r);
+      gb += *cl.map_shared_rank(&cnt_gt, r);
+      qb += *cl.map_shared_rank(&cnt_eq, r);
     }
-    for (int tb = p0; tb < e1; tb += kSelCT * 8) {
-      const int i0 = tb + tid * 8;
-      float v8[8];
-      load8(sc, i0 - p0, p1 - p0, v8);
-      uint32_t fg = 0, fq = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j;
-        const uint32_t key = order_key(v8[j]);
-        const bool in = i >= e0 && i < e1;
-        fg |= uint32_t(in && key > tau) << j;
-        fq |= uint32_t(in && key == tau) << j;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = s0; base < s1; base += 32) {
+      const int i = base + lane;
+      const uint32_t key = i < s1 ? order_key(sc[i - p0]) : 0u;
+      const unsigned bg = __ballot_sync(kFull, i < s1 && key > tau);
+      const unsigned bq = __ballot_sync(kFull, i < s1 && key == tau);
+      const uint32_t g_at = gb + __popc(bg & lt), q_at = qb + __popc(bq & lt);
+      if ((bg >> lane) & 1u) {
+        out_idx[g_at + min(q_at, take_eq)] = i;
+      } else if (((bq >> lane) & 1u) && q_at < take_eq) {
+        out_idx[g_at + q_at] = i;
       }
-      uint32_t tile_tot;
-      const uint32_t ex = block_excl_scan((uint32_t(__popc(fg)) << 16) | uint32_t(__popc(fq)),
-                                          scan_sh, tile_tot);
-      uint32_t gb = gt_before + (ex >> 16), qb = eq_before + (ex & 0xffffu);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j;
-        if ((fg >> j) & 1u) {
-          out_idx[gb + min(qb, take_eq)] = i;
-          ++gb;
-        } else if ((fq >> j) & 1u) {
-          if (qb < take_eq) out_idx[gb + qb] = i;
-          ++qb;
-        }
-      }
-      gt_before += tile_tot >> 16;
-      eq_before += tile_tot & 0xffffu;
+      gb += __popc(bg);
+      qb += __popc(bq);
     }
   } else {
     // keep all of E (or nothing): position lo + j goes to slot j
@@ -628,7 +603,7 @@ bool select_kn_fits(int max_len) { return select_smem_bytes(max_len, true) <= si
 template <int EV_G>
 cudaError_t launch_select_t(const SelectArgs& args, cudaStream_t st) {
   SelectArgs a = args;
-  a.kn_smem = a.mode != SFI_SELECT_LOGIT_SUM_SEQ && select_kn_fits(a.max_len) ? 1 : 0;
+  a.kn_smem = a.mode == SFI_SELECT_FUSED && select_kn_fits(a.max_len) ? 1 : 0;
   const size_t smem = select_smem_bytes(a.max_len, a.kn_smem != 0);
   cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel<EV_G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

@@ -49,7 +49,9 @@ struct VerifyCfg {
   static constexpr size_t OFF_BAR = OFF_V + size_t(NS) * STAGE_B;
   static constexpr size_t OFF_RED = OFF_BAR + (2 * NS + 2 * kItemRing) * 8;
   static constexpr size_t OFF_MISC = OFF_RED + RED_B;
-  static constexpr size_t OFF_UNITS = OFF_MISC + 128;
+  // collected-row sums passed from tile 1 to tile 0: [stage parity][warp slot][16 rows]
+  static constexpr size_t OFF_XCH = OFF_MISC + 128;
+  static constexpr size_t OFF_UNITS = OFF_XCH + 2 * 4 * 16 * 4;
   static size_t smem_bytes(int n_units) { return OFF_UNITS + size_t(n_units + 1 + kRankWords) * 4; }
   static_assert(OFF_UNITS + (size_t(kMaxUnits) + 1 + kRankWords) * 4 <= size_t(227) * 1024,
                 "shared memory plan exceeds 227 KB");
@@ -72,6 +74,12 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
                                             unsigned char* smem, uint32_t bar_full,
                                             uint32_t bar_empty, volatile int* abort_flag,
                                             uint32_t& stage, int warp, int lane, float* red) {
+  // Collected rows are tile rows [0, ncg): when they reach into tile 1, each
+  // tile-1 warp hands its collected sums to the tile-0 warp of the same stage
+  // rows through shared memory (a two-warp named barrier per stage, reached
+  // by both warps on every stage).
+  float* xch = reinterpret_cast<float*>(smem + VerifyCfg<D>::OFF_XCH);
+  const bool xtile = va.lsum != nullptr && va.ncg > 16;
   using C = VerifyCfg<D>;
   const AttnArgs& a = va.base;
   constexpr int KS = D / 16;
@@ -115,6 +123,8 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
     const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
     const int r0 = wslot * C::MW;
     const int nw = min(C::MW, nr - r0);
+    float lsv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    bool lvalid = false;
     if (have && nw > 0 && tile_rows > 0) {
       const uint32_t kst = kbase + slot * C::STAGE_B;
       const uint32_t vst = vbase + slot * C::STAGE_B;
@@ -132,21 +142,20 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
           mma_bf16_full(sacc[nt], qa[k1][0], qa[k1][1], qa[k1][2], qa[k1][3], b2, b3);
         }
       }
-      // Collect-2 logit sums (tile 0 holds the collected rows)
-      if (va.lsum && tile == 0) {
+      // collected logit sums of this tile's rows (lanes with g4 == 0 hold them)
+      if (va.lsum) {
+        const bool c_lo = 16 * tile + g4 < va.ncg, c_hi = 16 * tile + g4 + 8 < va.ncg;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            float v = (g4 < va.ncg ? sacc[nt][j] : 0.f) + (g4 + 8 < va.ncg ? sacc[nt][2 + j] : 0.f);
+            float v = (c_lo ? sacc[nt][j] : 0.f) + (c_hi ? sacc[nt][2 + j] : 0.f);
             v += __shfl_xor_sync(kFull, v, 4);
             v += __shfl_xor_sync(kFull, v, 8);
             v += __shfl_xor_sync(kFull, v, 16);
-            const int rr = nt * 8 + 2 * t4 + j;
-            const int pos = c0 + r0 + rr;
-            if (g4 == 0 && rr < nw && pos < n_pre)
-              va.lsum[size_t(I.u) * a.max_len + pos] = v * va.lscale;
+            lsv[nt][j] = v;
           }
+        lvalid = true;
       }
       // logits (log2 domain) of rows g4 (hr 0) and g4 + 8 (hr 1), masked
       float l[2][4];
@@ -203,6 +212,32 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
         mma_bf16_full(acc[2 * dp], pa[0][0], pa[1][0], pa[0][1], pa[1][1], b0, b1);
         mma_bf16_full(acc[2 * dp + 1], pa[0][0], pa[1][0], pa[0][1], pa[1][1], b2, b3);
       }
+    }
+    if (xtile) {
+      float* xb = xch + ((stage & 1u) * 4 + wslot) * 16;
+      if (tile == 1 && g4 == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) xb[nt * 8 + 2 * t4 + j] = lsv[nt][j];
+      }
+      named_bar_sync(2 + wslot, 64);
+      if (tile == 0 && g4 == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) lsv[nt][j] += xb[nt * 8 + 2 * t4 + j];
+      }
+    }
+    if (lvalid && tile == 0 && g4 == 0) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int rr = nt * 8 + 2 * t4 + j;
+          const int pos = c0 + r0 + rr;
+          if (rr < nw && pos < n_pre) va.lsum[size_t(I.u) * a.max_len + pos] = lsv[nt][j] * va.lscale;
+        }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);

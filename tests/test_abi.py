@@ -91,6 +91,9 @@ def test_select_and_fast_param_validation(sfi):
     assert sel(sfi.params(4, 16, 8, 1.5)) == sfi.SFI_ERR_INVALID_ARG        # lambda outside [0, 1]
     assert sel(sfi.params(4, 16, 8, float("nan"))) == sfi.SFI_ERR_INVALID_ARG
     assert sel(sfi.params(4, 16, 8, 0.3, mode=9)) == sfi.SFI_ERR_INVALID_ARG
+    for m in (sfi.SFI_SELECT_LOGIT_SUM_SEQ, sfi.SFI_SELECT_LOGIT_SUM_HEAD):
+        assert sel(sfi.params(0, 5, 8, 0.3, mode=m)) == sfi.SFI_ERR_INVALID_ARG  # lambda must be 0
+        assert sel(sfi.params(4, 5, 8, 0.0, mode=m)) == sfi.SFI_ERR_INVALID_ARG  # n_sink must be 0
     assert sel(sfi.params(4, 16, 8, 0.3, mode=sfi.SFI_SELECT_LOGIT_SUM_SEQ)) == sfi.SFI_ERR_INVALID_ARG
     assert sel(sfi.params(4, 16, 8, 0.3), kn=None) == sfi.SFI_ERR_INVALID_ARG
     assert sel(sfi.params(4, 16, 8, 0.3), ev=None) == sfi.SFI_ERR_INVALID_ARG
@@ -120,3 +123,26 @@ def test_schedule_matches_oracle(sfi):
             assert list(got) == list(ref[t].astype(np.uint8)), (budget, t)
     with pytest.raises(sfi.SfiError):
         sfi.sfi_schedule(np.zeros(2, np.uint8), np.zeros(2, np.uint8), np.zeros(2, np.int32), -1)
+
+
+def test_verify_validation_codes(sfi):
+    """Verification attention rejects unsupported shapes and bad collected-row
+    lists on the host (G = 4 here: n_rows * G may reach 32, every row may be
+    collected)."""
+    def verify(L, n_rows, collect, lsum=FAKE, ws=FAKE, q=FAKE):
+        arr = (ctypes.c_int32 * max(1, len(collect)))(*collect) if collect is not None else None
+        n = len(collect) if collect is not None else 0
+        return sfi.lib.sfi_verify_attn(ctypes.byref(L), n_rows, arr, n, q, FAKE, FAKE, FAKE, lsum, ws,
+                                       1 << 40, None)
+    Lb = layout(sfi, dtype=sfi.SFI_BF16)
+    assert verify(layout(sfi), 5, [0, 4]) == sfi.SFI_ERR_UNSUPPORTED           # fp32 cache
+    assert verify(Lb, 0, [0]) == sfi.SFI_ERR_UNSUPPORTED
+    assert verify(Lb, 9, [0]) == sfi.SFI_ERR_UNSUPPORTED                       # > 8 rows
+    assert verify(layout(sfi, dtype=sfi.SFI_BF16, n_q_heads=16), 5, [0]) == sfi.SFI_ERR_UNSUPPORTED  # 5 * 8 > 32
+    assert verify(Lb, 5, [0, 0]) == sfi.SFI_ERR_INVALID_ARG                    # repeated row
+    assert verify(Lb, 5, [5]) == sfi.SFI_ERR_INVALID_ARG                       # row outside the chain
+    assert verify(Lb, 5, [0, 1, 2, 3, 4, 0]) == sfi.SFI_ERR_INVALID_ARG        # more rows than the chain
+    assert verify(Lb, 5, [0, 1, 2, 3, 4], q=None) == sfi.SFI_ERR_INVALID_ARG
+    # every row collected passes the row checks and stops at the missing workspace
+    assert verify(Lb, 5, [0, 1, 2, 3, 4], ws=None) == sfi.SFI_ERR_WORKSPACE
+    assert verify(Lb, 8, list(range(8)), ws=None) == sfi.SFI_ERR_WORKSPACE

@@ -24,7 +24,9 @@ def sfi():
     return load_sfi()
 
 
-def run_vegas(sfi, wl, n_pre, gamma, k, collect):
+def run_vegas(sfi, wl, n_pre, gamma, k, collect, per_head=False):
+    """per_head: rank each KV head's logit sums on its own (one set per KV
+    head) instead of their sum over heads (one set per sequence)."""
     sh = wl.shape
     B, R = sh.batch, gamma + 1
     dl = DeviceLayer.build(wl)
@@ -42,7 +44,8 @@ def run_vegas(sfi, wl, n_pre, gamma, k, collect):
     assert sfi.sfi_read_status(ws) == 0
     out, lsum_np = out.cpu().numpy(), lsum.cpu().numpy()
     # selection: per-sequence top-k of the head-summed logit sums
-    prm = sfi.params(0, R, k, 0.0, mode=sfi.SFI_SELECT_LOGIT_SUM_SEQ)
+    mode = sfi.SFI_SELECT_LOGIT_SUM_HEAD if per_head else sfi.SFI_SELECT_LOGIT_SUM_SEQ
+    prm = sfi.params(0, R, k, 0.0, mode=mode)
     idx = torch.full((B, sh.n_kv_heads, k), -1, dtype=torch.int32, device="cuda")
     cnt = torch.full((B, sh.n_kv_heads), -1, dtype=torch.int32, device="cuda")
     s_out = torch.full((B, sh.n_kv_heads, lay.max_len), -7.0, device="cuda")
@@ -59,9 +62,18 @@ def run_vegas(sfi, wl, n_pre, gamma, k, collect):
         got = lsum_np[b, :, :n_pre[b]]
         assert np.all(np.abs(got - Lg) <= L_TOL * (1 + np.abs(Lg))), float(np.max(np.abs(got - Lg)))
         assert np.all(lsum_np[b, :, n_pre[b]:] == -7.0), "wrote past the prefix"
-        L = Lg.sum(0)
         ke = min(k, n_pre[b])
         assert np.all(cnt[b] == ke)
+        if per_head:
+            sets = []
+            for g in range(sh.n_kv_heads):
+                sel = idx[b, g, :ke]
+                check_selection(sel, Lg[g], 0, n_pre[b], k, rtol=1e-6, atol=L_TOL * (1 + np.abs(Lg[g]).max()))
+                assert np.array_equal(sel, O.top_k(s_np[b, g].astype(np.float64), 0, n_pre[b], k))
+                sets.append(sel.astype(np.int64))
+            T.append(sets)
+            continue
+        L = Lg.sum(0)
         sel = idx[b, 0, :ke]
         for g in range(1, sh.n_kv_heads):
             assert np.array_equal(idx[b, g, :ke], sel)
@@ -83,7 +95,10 @@ def run_vegas(sfi, wl, n_pre, gamma, k, collect):
         assert sfi.sfi_read_status(ws2) == 0
         o = o.cpu().numpy()
         for b in range(B):
-            ref = O.draft_step(qf[b], dl.K64[b], dl.V64[b], n_pre[b], lens_j[b], T[b])
+            if per_head:  # each KV head attends to its own set and the tail since the prefix
+                ref = O.fast_step(qf[b], dl.K64[b], dl.V64[b], lens_j[b], T[b], 0, lens_j[b] - n_pre[b])
+            else:
+                ref = O.draft_step(qf[b], dl.K64[b], dl.V64[b], n_pre[b], lens_j[b], T[b])
             assert max_abs(o[b], ref) <= O_TOL[sh.dtype], (j, b, max_abs(o[b], ref))
 
 
@@ -102,6 +117,27 @@ def test_vegas_other_shapes(sfi):
     n_pre = [1500]
     wl = W.small(1, 8, 2, 128, "bf16", [n + 5 for n in n_pre], seed=33, k=1500)
     run_vegas(sfi, wl, n_pre, gamma=4, k=1500, collect=[1, 3, 4])
+
+
+def test_vegas_all_rows_two_tiles(sfi):
+    """Every chain row collected (the aggregation before Collect-2's reduction):
+    at G = 4 the five rows span both 16-row tiles (20 collected rows), at
+    G = 8 four rows fill both tiles (32)."""
+    n_pre = [2500, 777]
+    wl = W.small(2, 32, 8, 128, "bf16", [n + 5 for n in n_pre], seed=34, k=300)
+    run_vegas(sfi, wl, n_pre, gamma=4, k=300, collect=[0, 1, 2, 3, 4])
+    n_pre = [1900]
+    wl = W.small(1, 16, 2, 64, "bf16", [n + 4 for n in n_pre], seed=35, k=128)
+    run_vegas(sfi, wl, n_pre, gamma=3, k=128, collect=[3, 0, 2, 1])
+
+
+def test_vegas_per_kv_head(sfi):
+    """Selection grouped per KV head (each KV head ranks its own collected sums),
+    with Collect-2 and with every row collected."""
+    n_pre = [3000, 1234]
+    wl = W.small(2, 32, 8, 128, "bf16", [n + 5 for n in n_pre], seed=36, k=200)
+    run_vegas(sfi, wl, n_pre, gamma=4, k=200, collect=[0, 4], per_head=True)
+    run_vegas(sfi, wl, n_pre, gamma=4, k=200, collect=[0, 1, 2, 3, 4], per_head=True)
 
 
 def test_vegas_cfg3_full_size(sfi):
