@@ -589,6 +589,9 @@ def run_kernel_cases(args):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=R.dev)
     row = 2 * sh.n_kv_heads * sh.head_dim * 2
     n = wl.n0[0]
+    gen = torch.Generator(device="cpu").manual_seed(wl.seed)
+    run0 = torch.randint(wl.n_sink, max(wl.n_sink + 1, n - wl.window - wl.k), (B, sh.n_kv_heads), generator=gen)
+    contig = (run0[:, :, None] + torch.arange(wl.k)[None, None, :]).to(torch.int32).to(R.dev)
     cases = {
         "dense": (lambda: sfi.sfi_slow_attn(lay, q, R.K[0], R.V[0], out, None, None, ws), B * n * row),
         "slow": (lambda: sfi.sfi_slow_attn(lay, q, R.K[0], R.V[0], out, f, kn, ws), B * n * row),
@@ -596,6 +599,10 @@ def run_kernel_cases(args):
                    B * sh.n_kv_heads * n * 8),
         "fast": (lambda: sfi.sfi_fast_attn(lay, prm, q, R.K[0], R.V[0], idx, cnt, out, ws),
                  B * (wl.n_sink + wl.k + wl.window) * row),
+        # the same fast step over one contiguous run of k positions per unit
+        # (what a step reading a compacted copy of the selected rows streams)
+        "fast_contig": (lambda: sfi.sfi_fast_attn(lay, prm, q, R.K[0], R.V[0], contig, cnt, out, ws),
+                        B * (wl.n_sink + wl.k + wl.window) * row),
     }
     # "mixed": one decode-step launch of the decode driver with sequence 0
     # refreshing (dense + evidence) and the others fast, as in a refresh step
@@ -784,7 +791,7 @@ def main():
     ap.add_argument("--sync-select", action="store_true",
                     help="run each layer's selector on the decode stream instead of overlapping it "
                          "with the next layer's attention")
-    ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast,mixed (or 'verify' alone): time "
+    ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast,fast_contig,mixed (or 'verify' alone): time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
     ap.add_argument("--case-batch", type=int, default=2)
     ap.add_argument("--case-context", type=int, default=0,
