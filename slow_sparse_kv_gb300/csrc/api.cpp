@@ -11,7 +11,6 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
-#include <queue>
 #include <string>
 #include <utility>
 #include <vector>
@@ -142,117 +141,137 @@ int stage_rows(int dtype, int D) {
 namespace {
 
 // Length of a launch, in stage times of a CTA streaming at its fair share of
-// HBM, when `grid` CTAs take items in order (n_a units of rows_a rows, then
-// n_b units of rows_b rows, each split into ceil(rows / rpi) items).  While items
-// remain every CTA is busy and all stream at the same rate (list scheduling
-// with a min-heap of the CTAs' free times).  Once the last item is taken the
-// CTAs that are still busy share HBM among fewer streams and speed up, each
-// to at most kCtaCap times its fair share (the stages a CTA keeps in
-// flight bound its own rate).  Each item also costs kItemCost stage times
-// (its epilogue, and its share of the merge of split units).
-double simulate_launch(long long n_a, int rows_a, long long n_b, int rows_b, long long rpi, int sr,
-                       int grid) {
-  constexpr double kItemCost = 3.0;
-  constexpr double kCtaCap = 1.3;
-  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-  for (int i = 0; i < grid; ++i) free_at.push(0.0);
-  double t_last = 0.0;
-  auto take = [&](double cost) {
-    const double t = free_at.top();
-    free_at.pop();
-    t_last = t;
-    free_at.push(t + cost);
-  };
+// HBM, when `grid` CTAs take items in order: n_a units of rows_a rows split
+// into ceil(rows_a / rpi_a) items each, then n_b units of rows_b rows split
+// by rpi_b.  List scheduling with a min-heap of the CTAs' free times; each
+// item costs its stages plus kItemCost (its start, epilogue and share of the
+// merge of split units).  Once the last item is taken, the CTAs still busy
+// share HBM among fewer streams and speed up to at most `cap` times their
+// fair share: their own pipeline bounds them (measured: ~1.5 for plain
+// attention, ~1.0 when slow units also write their logits and key norms,
+// which holds each stage longer).
+double simulate_launch(long long n_a, int rows_a, long long rpi_a, long long n_b, int rows_b,
+                       long long rpi_b, int sr, int grid, double cap) {
+  constexpr long long kItemCost = 3;
+  // Item costs are whole stage counts, so the CTAs' free times are integers:
+  // free[t] counts the CTAs free at time t, and the earliest free time only
+  // grows as items are handed out.
+  long long horizon = 1;
   for (int cls = 0; cls < 2; ++cls) {
     const long long n = cls == 0 ? n_a : n_b;
     const int rows = cls == 0 ? rows_a : rows_b;
+    const long long rpi = cls == 0 ? rpi_a : rpi_b;
+    if (n > 0 && rows > 0) horizon += n * (ceil_div(rows, sr) + ceil_div(rows, rpi) * kItemCost);
+  }
+  horizon = horizon / grid + 2 * (ceil_div(std::max(rows_a, rows_b), sr) + kItemCost) + 2;
+  std::vector<int> free_at(size_t(horizon), 0);
+  free_at[0] = grid;
+  long long t_min = 0;
+  for (int cls = 0; cls < 2; ++cls) {
+    const long long n = cls == 0 ? n_a : n_b;
+    const int rows = cls == 0 ? rows_a : rows_b;
+    const long long rpi = cls == 0 ? rpi_a : rpi_b;
     if (n <= 0 || rows <= 0) continue;
     // k items per unit share the unit's S stages cyclically: S % k items
     // of S / k + 1 stages, then the rest of S / k
     const long long k = ceil_div(rows, rpi), S = ceil_div(rows, sr);
     const long long q = S / k, r = S % k;
     for (long long u = 0; u < n; ++u)
-      for (long long i = 0; i < k; ++i) take(double(q + (i < r ? 1 : 0)) + kItemCost);
+      for (long long i = 0; i < k; ++i) {
+        while (free_at[size_t(t_min)] == 0) ++t_min;
+        --free_at[size_t(t_min)];
+        ++free_at[size_t(t_min + q + (i < r ? 1 : 0) + kItemCost)];
+      }
   }
-  // the tail: remaining work of every CTA after the last item was taken
-  double t = t_last, done = 0.0;
+  // the tail: remaining work of every CTA after the last item was taken at
+  // t_min, shortest first
+  double t = double(t_min), done = 0.0;
   int active = grid;
-  while (!free_at.empty()) {
-    const double r = free_at.top() - t_last;  // ascending
-    free_at.pop();
-    if (r > done) {
-      const double rate = std::min(double(grid) / active, kCtaCap);
-      t += (r - done) / rate;
-      done = r;
+  for (long long x = t_min; x < horizon && active > 0; ++x)
+    for (int c = free_at[size_t(x)]; c > 0; --c) {
+      const double rem = double(x - t_min);
+      if (rem > done) {
+        t += (rem - done) / std::min(double(grid) / active, cap);
+        done = rem;
+      }
+      --active;
     }
-    --active;
-  }
   return t;
 }
 
-struct RpiKey {
+struct SplitKey {
   long long n_a, n_b;
   int rows_a, rows_b, sr, grid;
-  bool operator==(const RpiKey& o) const {
+  bool emit;
+  bool operator==(const SplitKey& o) const {
     return n_a == o.n_a && n_b == o.n_b && rows_a == o.rows_a && rows_b == o.rows_b &&
-           sr == o.sr && grid == o.grid;
+           sr == o.sr && grid == o.grid && emit == o.emit;
   }
 };
 
+// Candidate rows per item splitting `rows` into 1..kmax even items (at least
+// min_rpi rows each), distinct.
+std::vector<long long> split_candidates(int rows, int kmax, long long min_rpi, int sr) {
+  std::vector<long long> c;
+  for (int k = 1; k <= kmax; ++k) {
+    const long long rpi = std::max(min_rpi, ceil_div(ceil_div(rows, k), sr) * sr);
+    if (std::find(c.begin(), c.end(), rpi) == c.end()) c.push_back(rpi);
+  }
+  return c;
+}
+
 }  // namespace
 
-// Rows per work item for a launch whose units come in two classes (n_a units
-// of at most rows_a rows, taken first, then n_b of at most rows_b): the
-// candidate that splits either class into 1..kItemSlotsPerUnit even items
+// Item sizes for a launch whose units come in two classes (n_a units of at
+// most rows_a rows, taken first, then n_b of at most rows_b): the pair of
+// splits -- each class into 1..kItemSlotsPerUnit even items (the workspace
+// holds that many partials per unit), the second class into at most 16 --
 // with the shortest simulated launch, among those that give every CTA an
-// item when any does and the launch is long (at most kItemSlotsPerUnit items per unit: the
-// workspace holds that many partials).  Results are cached per
-// launch shape; a decode loop meets only a handful of shapes.
-int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid) {
+// item when any does and the launch is long.  Results are cached per launch shape;
+// a decode loop meets only a handful of shapes.
+ItemSplit choose_item_split(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid,
+                            bool emit) {
   if (n_a <= 0 || rows_a <= 0) n_a = 0, rows_a = 0;
   if (n_b <= 0 || rows_b <= 0) n_b = 0, rows_b = 0;
-  const RpiKey key{n_a, n_b, rows_a, rows_b, sr, grid};
+  const SplitKey key{n_a, n_b, rows_a, rows_b, sr, grid, emit};
+  const double cap = emit ? 1.0 : 1.5;
   static std::mutex mu;
-  static std::vector<std::pair<RpiKey, int>> cache;
+  static std::vector<std::pair<SplitKey, ItemSplit>> cache;
   {
     std::lock_guard<std::mutex> lk(mu);
     for (const auto& e : cache)
       if (e.first == key) return e.second;
   }
-  const int rows_max = rows_a > rows_b ? rows_a : rows_b;
-  long long min_rpi = ceil_div(ceil_div(rows_max, kItemSlotsPerUnit), sr) * sr;
-  if (min_rpi < sr) min_rpi = sr;
-  std::vector<long long> cand;
-  for (int cls = 0; cls < 2; ++cls) {
-    const int rows = cls == 0 ? rows_a : rows_b;
-    if (rows <= 0) continue;
-    for (int k = 1; k <= kItemSlotsPerUnit; ++k) {
-      const long long rpi = std::max(min_rpi, ceil_div(ceil_div(rows, k), sr) * sr);
-      if (std::find(cand.begin(), cand.end(), rpi) == cand.end()) cand.push_back(rpi);
-    }
-  }
-  // In long launches fewer streams than SMs lose more bandwidth than the
-  // simulation shows: keep at least one item per CTA whenever a split
-  // provides that.  (Short launches are dominated by per-item latency.)
-  auto items_of = [&](long long rpi) {
-    return n_a * ceil_div(rows_a, rpi) + n_b * ceil_div(rows_b, rpi);
+  auto min_rpi = [&](int rows) {
+    return std::max<long long>(sr, ceil_div(ceil_div(rows, kItemSlotsPerUnit), sr) * sr);
+  };
+  const std::vector<long long> ca =
+      n_a ? split_candidates(rows_a, kItemSlotsPerUnit, min_rpi(rows_a), sr) : std::vector<long long>{sr};
+  const std::vector<long long> cb =
+      n_b ? split_candidates(rows_b, 16, min_rpi(rows_b), sr) : std::vector<long long>{sr};
+  // In long launches fewer streams than SMs cost more than the tail model
+  // shows (measured on dense launches): every CTA gets an item when a split
+  // allows it.
+  auto items_of = [&](long long ra, long long rb) {
+    return (n_a ? n_a * ceil_div(rows_a, ra) : 0) + (n_b ? n_b * ceil_div(rows_b, rb) : 0);
   };
   const double stages = double(n_a) * ceil_div(rows_a, sr) + double(n_b) * ceil_div(rows_b, sr);
-  const bool can_fill = items_of(min_rpi) >= grid && stages >= 64.0 * grid;
-  long long best = min_rpi;
+  const bool can_fill = stages >= 64.0 * grid && items_of(ca.back(), cb.back()) >= grid;
+  ItemSplit best{int(ca.back()), int(cb.back())};
   double best_cost = 1e300;
-  for (long long rpi : cand) {
-    if (can_fill && items_of(rpi) < grid) continue;
-    const double cost = simulate_launch(n_a, rows_a, n_b, rows_b, rpi, sr, grid);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = rpi;
+  for (long long ra : ca)
+    for (long long rb : cb) {
+      if (can_fill && items_of(ra, rb) < grid) continue;
+      const double cost = simulate_launch(n_a, rows_a, ra, n_b, rows_b, rb, sr, grid, cap);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = ItemSplit{int(ra), int(rb)};
+      }
     }
-  }
   std::lock_guard<std::mutex> lk(mu);
   if (cache.size() >= 256) cache.clear();
-  cache.emplace_back(key, int(best));
-  return int(best);
+  cache.emplace_back(key, best);
+  return best;
 }
 
 namespace {
@@ -321,8 +340,11 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
 sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,
                     long long n_fast_units, int fast_rows, cudaStream_t st, bool pdl) {
   const int G = L->n_q_heads / L->n_kv_heads;
-  a.rows_per_item = choose_rows_per_item(n_slow_units, slow_rows, n_fast_units, fast_rows,
-                                         stage_rows(L->dtype, L->head_dim), device_sm_count());
+  const ItemSplit sp = choose_item_split(n_slow_units, slow_rows, n_fast_units, fast_rows,
+                                        stage_rows(L->dtype, L->head_dim), device_sm_count(),
+                                        a.emit != 0 && n_slow_units > 0);
+  a.rpi_slow = sp.rpi_a;
+  a.rpi_fast = sp.rpi_b;
   const cudaError_t e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st, pdl)
                                             : launch_attn_bf16(a, L->head_dim, G, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -513,8 +535,9 @@ sfi_status sfi_verify_attn(const sfi_layout* L, int32_t n_rows, const int32_t* c
   std::memset(&va, 0, sizeof(va));
   fill_attn_common(va.base, L, q, k, v, out, static_cast<char*>(ws), p);
   for (int b = 0; b < L->batch; ++b) va.base.slow.bits[b >> 5] |= 1u << (b & 31);
-  va.base.rows_per_item = choose_rows_per_item((long long)L->batch * L->n_kv_heads, L->max_len, 0,
-                                               0, verify_stage_rows(), device_sm_count());
+  va.base.rpi_slow = va.base.rpi_fast =
+      choose_item_split((long long)L->batch * L->n_kv_heads, L->max_len, 0, 0, verify_stage_rows(),
+                        device_sm_count(), logitsum_out != nullptr).rpi_a;
   va.R = n_rows;
   va.ncg = n_collect * G;
   for (int i = 0; i < n_ord; ++i) va.t_of_slot[i] = order[i];

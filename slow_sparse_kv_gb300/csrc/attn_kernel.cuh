@@ -244,8 +244,10 @@ __device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int
   const int u0 = min(t * per, n_units), u1 = min(u0 + per, n_units);
   int local = 0;
   for (int u = u0; u < u1; ++u) {
-    const int rows = attn_unit_rows(a, unit_at(a, rank, u), blockIdx.x == 0);
-    const int it = (rows + a.rows_per_item - 1) / a.rows_per_item;
+    const int uu = unit_at(a, rank, u);
+    const int rows = attn_unit_rows(a, uu, blockIdx.x == 0);
+    const int rpi = seq_is_slow(a.slow, uu / a.H_kv) ? a.rpi_slow : a.rpi_fast;
+    const int it = (rows + rpi - 1) / rpi;
     units[u] = it;
     local += it;
   }

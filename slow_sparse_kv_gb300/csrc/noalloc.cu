@@ -124,7 +124,7 @@ extern "C" sfi_status sfi_fast_attn_noalloc(const sfi_layout* L, const sfi_param
   const long long balanced = (units * bound + grid - 1) / grid;
   if (rpi < balanced) rpi = balanced;
   rpi = (rpi + sr - 1) / sr * sr;
-  a.rows_per_item = int(rpi);
+  a.rpi_slow = a.rpi_fast = int(rpi);
   e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st, true)
                           : launch_attn_bf16(a, L->head_dim, G, st, true);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");

@@ -12,16 +12,22 @@
 // Evidence pass: f[b][g][i] = (1/G) sum_h 2^(l_{h,i} - M_h) / Z_h from the
 // log2-scaled logits and per-head (M, Z) the attention kernel stored.
 //
-// Selector: one CTA of 1024 threads per (sequence, KV head) -- or per
-// sequence in logit-sum mode.  Pass 1 sums the key norms over the eligible
-// set E; pass 2 writes s for every position and builds the histogram of the
-// top 8 bits of the order key of s over E; three more 8-bit radix passes
-// find the exact k-th largest key tau and how many keys equal to tau to
-// keep; a final pass compacts the chosen positions in ascending order (keys
-// above tau, then the lowest-positioned keys equal to tau), so ties go to
-// the lower position exactly as the definition says.  Histograms use
-// warp-aggregated shared-memory atomics (the score distribution is very
-// skewed, so many lanes hit the same bin).
+// Selector: one thread-block cluster of 8 CTAs (512 threads each) per
+// (sequence, KV head) -- or per sequence in the per-sequence logit-sum mode
+// -- launched for the refreshing sequences only.  Each CTA holds the scores
+// of one eighth of the positions in shared memory.  The evidence pass forms
+// f (from the logits on the decode path) and the CTA's part of the key-norm
+// sum over E; after a cluster barrier every CTA writes s and the histogram of
+// the top 11 bits of the order key of s over E.  The cluster total of that
+// histogram fixes the top digit of the k-th largest key; the keys in that
+// bin (few, at the decode workloads) are gathered in rank 0, which finds the
+// two lower digits (11 and 10 bits) alone -- or, when the bin holds more than
+// kCandCap keys, every CTA runs the two passes over all its keys.  A final
+// ordered compaction writes the keys above tau, then the lowest-positioned
+// keys equal to tau, in ascending position order, so ties go to the lower
+// position exactly as the definition says.  Histograms use warp-aggregated
+// shared-memory atomics (the score distribution is very skewed, so many
+// lanes hit the same bin).
 #include <cooperative_groups.h>
 #include <math.h>
 

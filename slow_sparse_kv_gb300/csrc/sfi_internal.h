@@ -44,7 +44,7 @@ struct AttnArgs {
   int32_t n_sink;
   int32_t window;
   int32_t B, H_q, H_kv, max_len;
-  int32_t rows_per_item;
+  int32_t rpi_slow, rpi_fast;  // rows per work item of slow and of fast units
   int32_t max_items;
   int32_t emit;    // slow units write logits, stats (and knorm if non-null)
   float qscale;    // log2(e) / sqrt(D)
@@ -124,7 +124,14 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
 sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, int slow_rows,
                     long long n_fast_units, int fast_rows, cudaStream_t st, bool pdl = true);
 int fast_unit_rows_bound(const sfi_layout* L, const sfi_params* P);
-int choose_rows_per_item(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid);
+// Rows per work item of each unit class: class a (n_a units of at most
+// rows_a rows, taken first) and class b (n_b units of at most rows_b).
+struct ItemSplit {
+  int rpi_a, rpi_b;
+};
+// emit: class-a units write evidence (their CTAs cannot speed up in a tail).
+ItemSplit choose_item_split(long long n_a, int rows_a, long long n_b, int rows_b, int sr, int grid,
+                            bool emit);
 // Fill a.tmk / a.tmv for bf16 caches (sets a.use_tma; leaves it 0 if the
 // driver entry point is unavailable).
 void attach_tensor_maps(AttnArgs& a, const sfi_layout* L);
