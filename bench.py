@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import gc
 import json
 import math
 import multiprocessing as mp
@@ -388,6 +389,10 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    # The host enqueues every launch of a pass; a garbage-collection pause there
+    # would stall the device, so collection is off while passes are timed.
+    gc.collect()
+    gc.disable()
     # Nothing is recorded between the launches of the timed passes: an event
     # between two attention launches would break their programmatic
     # dependence (the next launch could no longer start as the previous one
@@ -476,6 +481,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         e2e_pass_s.append(round(time.perf_counter() - tp, 4))
     e2e_s = aggregate_max(time.perf_counter() - t0, world)
+    gc.enable()
     e2e_rate = world * T * e_steps / e2e_s
     # ---------------- full-KV dense baseline (every step dense, no evidence)
     lay0 = sfi.Layout(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dt, R.offsets, wl.cap, wl.n0, R.max_len,

@@ -122,13 +122,15 @@ struct ItemRing {
 };
 
 // Fetch the next item id for this CTA and publish it (first producer warp).
+// The CTA's first id was fetched at kernel start (first_id, lane 0), while
+// the unit table was being built.
 __device__ __forceinline__ int ring_fetch_publish(const AttnArgs& a, int total, const ItemRing& r,
                                                   uint32_t seq, volatile int* abort_flag,
-                                                  int lane) {
+                                                  int lane, unsigned first_id) {
   int it = -1;
   bool fetched_end = false;
   if (lane == 0) {
-    const unsigned x = atomicAdd(a.work_ctr, 1u);
+    const unsigned x = seq == 0 ? first_id : atomicAdd(a.work_ctr, 1u);
     if (x < unsigned(total)) {
       it = int(x);
     } else {
@@ -182,14 +184,17 @@ struct ItemInfo {
 // Rows of unit u in this launch (0 for an invalid length).
 __device__ __forceinline__ int attn_unit_rows(const AttnArgs& a, int u, bool report) {
   const int b = u / a.H_kv;
+  // all three loads go out before any of them is used
   const int n = a.len[b];
-  if (n < 1 || n > a.kv_cap[b] || n > a.max_len) {
+  const int cap = a.kv_cap[b];
+  const int craw = a.count != nullptr ? a.count[u] : 0;
+  if (n < 1 || n > cap || n > a.max_len) {
     if (report) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
     return 0;
   }
   if (seq_is_slow(a.slow, b)) return n;
   const int ns = min(a.n_sink, n);
-  const int cnt = min(max(a.count[u], 0), a.idx_stride);
+  const int cnt = min(max(craw, 0), a.idx_stride);
   const int wlo = max(a.n_sink, n - a.window);
   return ns + cnt + max(n - wlo, 0);
 }
@@ -316,7 +321,8 @@ template <class C>
 __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units, int n_units,
                                              int total, unsigned char* smem, uint32_t bar_full,
                                              uint32_t bar_empty, const ItemRing& ring,
-                                             volatile int* abort_flag, int pw, int lane) {
+                                             volatile int* abort_flag, int pw, int lane,
+                                             unsigned first_id) {
   constexpr int D = C::DIM;
   constexpr int RPW = C::SR / C::PW;        // rows of a stage per producer warp
   constexpr int PJ = (RPW + 31) / 32;       // positions per lane
@@ -328,7 +334,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
   uint32_t stage = 0;
   bool ok = true;
   for (uint32_t iseq = 0; ok; ++iseq) {
-    const int it = pw == 0 ? ring_fetch_publish(a, total, ring, iseq, abort_flag, lane)
+    const int it = pw == 0 ? ring_fetch_publish(a, total, ring, iseq, abort_flag, lane, first_id)
                            : ring_read(a, ring, iseq, abort_flag, lane);
     if (it < 0) break;
     const ItemInfo I = attn_resolve(a, units, n_units, it, C::SR);
@@ -866,12 +872,22 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
   const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
   const uint32_t bar_empty = bar_full + C::NS * 8;
 
+  // the first producer warp's lane 0 takes the CTA's first item id now; the
+  // atomic's round trip overlaps the unit table's loads
+  unsigned first_id = 0;
+  const bool fetcher = warp == C::NCW && lane == 0;
+  if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
   if (a.len_copy && blockIdx.x == 0)
     for (int b = tid; b < a.B; b += C::NT) a.len_copy[b] = a.len[b];
   attn_build_units<C::NT>(a, units, n_units, misc);
   const int total = units[n_units];
   if (total > a.max_items) {
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
+    // leave the work counters at zero for the next launch
+    if (fetcher && atomicAdd(a.work_ctr + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.work_ctr, 0u);
+      atomicExch(a.work_ctr + 1, 0u);
+    }
     return;
   }
   volatile int* abort_flag = misc + kMiscAbort;  // misc[0..12]: unit-table scan scratch
@@ -895,7 +911,7 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
 
   if (warp >= C::NCW) {
     attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, ring, abort_flag,
-                    warp - C::NCW, lane);
+                    warp - C::NCW, lane, first_id);
     return;
   }
 

@@ -272,10 +272,18 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
   int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
   const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
   const uint32_t bar_empty = bar_full + C::NS * 8;
+  // the CTA's first item id, fetched while the unit table is built
+  unsigned first_id = 0;
+  const bool fetcher = warp == C::NCW && lane == 0;
+  if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
   attn_build_units<C::NT>(a, units, n_units, misc);
   const int total = units[n_units];
   if (total > a.max_items) {
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
+    if (fetcher && atomicAdd(a.work_ctr + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.work_ctr, 0u);
+      atomicExch(a.work_ctr + 1, 0u);
+    }
     return;
   }
   volatile int* abort_flag = misc + kMiscAbort;  // misc[0..12]: unit-table scan scratch
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
   __syncthreads();
   if (warp >= C::NCW) {
     attn_produce<C>(a, units, n_units, total, smem, bar_full, bar_empty, ring, abort_flag,
-                    warp - C::NCW, lane);
+                    warp - C::NCW, lane, first_id);
     return;
   }
   float* red_all = reinterpret_cast<float*>(smem + C::OFF_RED);
