@@ -82,13 +82,13 @@ def schedule_counts(slow_masks: np.ndarray):
 # DRAM traffic of the attention kernel relative to its algorithmic bytes,
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # decode driver's mixed launch: batch 8 at context 131072, sequence 0
-# refreshing and seven fast -- 662.86 MB read + 7.35 MB written for
+# refreshing and seven fast -- 662.85 MB read + 7.30 MB written for
 # 661.77 MB algorithmic.  It holds for the kernel sources it was taken on
 # (their SHA-256 below); after any change the roofline reports null traffic
 # until the capture is repeated.
-ATTN_TRAFFIC = {"ratio": (662855424 + 7349248) / 661766144,
+ATTN_TRAFFIC = {"ratio": (662854400 + 7298816) / 661766144,
                 "sources": ["attn_kernel.cuh", "attn_bf16.cu", "common.cuh", "sfi_internal.h", "api.cpp"],
-                "sha256": "33b5e754247f537079926c3d34c8e1539a3acbac4381dae09bbcb0b836f34999"}
+                "sha256": "e8792f0f8739c8e460eab18d0bb9b49b58a6f3a211b71decdcce12b87aaf0d78"}
 
 
 def attn_traffic_ratio():

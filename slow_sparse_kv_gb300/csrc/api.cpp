@@ -537,7 +537,7 @@ sfi_status sfi_verify_attn(const sfi_layout* L, int32_t n_rows, const int32_t* c
   for (int b = 0; b < L->batch; ++b) va.base.slow.bits[b >> 5] |= 1u << (b & 31);
   va.base.rpi_slow = va.base.rpi_fast =
       choose_item_split((long long)L->batch * L->n_kv_heads, L->max_len, 0, 0, verify_stage_rows(),
-                        device_sm_count(), logitsum_out != nullptr).rpi_a;
+                        device_sm_count(), false).rpi_a;  // 4-byte logit sums barely lengthen a stage
   va.R = n_rows;
   va.ncg = n_collect * G;
   for (int i = 0; i < n_ord; ++i) va.t_of_slot[i] = order[i];
