@@ -83,21 +83,31 @@ def schedule_counts(slow_masks: np.ndarray):
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # decode driver's mixed launch: batch 8 at context 131072, sequence 0
 # refreshing and seven fast -- 662.85 MB read + 7.30 MB written for
-# 661.77 MB algorithmic.  It holds for the kernel sources it was taken on
-# (their SHA-256 below); after any change the roofline reports null traffic
-# until the capture is repeated.
+# 661.77 MB algorithmic.  It holds for the kernel code it was taken on (the
+# SHA-256 of the sources below with comments and whitespace removed); after
+# any change to that code the roofline reports null traffic until the
+# capture is repeated.
 ATTN_TRAFFIC = {"ratio": (662854400 + 7298816) / 661766144,
                 "sources": ["attn_kernel.cuh", "attn_bf16.cu", "common.cuh", "sfi_internal.h", "api.cpp"],
-                "sha256": "e8792f0f8739c8e460eab18d0bb9b49b58a6f3a211b71decdcce12b87aaf0d78"}
+                "sha256": "f56a9db0b11883ac6ac8cdb3499f93d2cd4937b462eb29cccbfec0c4891be0da"}
+
+
+def attn_code_hash() -> str:
+    """SHA-256 of the attention kernel's sources with comments and whitespace removed."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in ATTN_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, "slow_sparse_kv_gb300", "csrc", f)) as fh:
+            txt = fh.read()
+        txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
+        txt = re.sub(r"//[^\n]*", " ", txt)
+        h.update(" ".join(txt.split()).encode())
+    return h.hexdigest()
 
 
 def attn_traffic_ratio():
-    import hashlib
-    h = hashlib.sha256()
-    for f in ATTN_TRAFFIC["sources"]:
-        with open(os.path.join(ROOT, "slow_sparse_kv_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return ATTN_TRAFFIC["ratio"] if h.hexdigest() == ATTN_TRAFFIC["sha256"] else None
+    return ATTN_TRAFFIC["ratio"] if attn_code_hash() == ATTN_TRAFFIC["sha256"] else None
 
 
 def attention_bytes(wl: W.Workload, slow_masks: np.ndarray) -> float:

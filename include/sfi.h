@@ -174,9 +174,10 @@ sfi_status sfi_select(const sfi_layout* layout, const sfi_params* params,
  * For every (b, g) the row set is [0, min(n_sink, n_b)) + idx[b][g][0..count[b][g])
  * + [max(n_sink, n_b - window), n_b); each query head of group g attends to
  * those rows with softmax attention (scale 1/sqrt(d)).  The selected positions
- * must lie in [n_sink, n_b - window) (disjoint from sinks and window);
- * positions outside [0, n_b) are skipped and flagged SFI_DEV_BAD_INDEX.
- * Rows are gathered from the cache with bulk asynchronous copies. */
+ * must lie in [n_sink, n_b - window) (disjoint from sinks and window); a
+ * position outside [0, n_b) is replaced by position 0 and flagged
+ * SFI_DEV_BAD_INDEX (the call's output is then not meaningful).  Rows are
+ * gathered from the cache with 16-byte asynchronous copies. */
 size_t sfi_fast_attn_workspace_size(const sfi_layout* layout, const sfi_params* params);
 sfi_status sfi_fast_attn(const sfi_layout* layout, const sfi_params* params,
                          const void* q, const void* k, const void* v,

@@ -10,12 +10,14 @@
 //
 // Design (GB300; the step is HBM-bound: G = H_q / H_kv query heads per KV
 // head read every K and V row once):
-//  * the rows of each unit are cut into equal work items; CTAs (one per SM)
-//    walk the items round-robin;
-//  * one producer warp streams K and V rows into a 4-deep ring of shared-
-//    memory stages with completion on mbarriers: every lane copies 16-byte
-//    pieces with cp.async (dense runs and gathered rows alike); fp32 dense
-//    runs use one bulk copy (cp.async.bulk) per stage instead;
+//  * each unit's 64-row stages are dealt cyclically to a few work items
+//    (separate item sizes for slow and fast units); the persistent CTAs (one
+//    per SM) take items from a global counter, slow units' items first;
+//  * four producer warps stream K and V rows into a ring of up to 6 shared-
+//    memory stages with completion on mbarriers: full dense bf16 stages as
+//    64 x 64 2-D TMA boxes (128-byte swizzle), gathered rows and partial
+//    stages as 16-byte cp.async pieces into the same swizzled layout, fp32
+//    dense stages as one bulk copy (cp.async.bulk) per operand;
 //  * bf16 caches: eight consumer warps, four per stage, 16 rows each.  The
 //    G query vectors sit in registers as the A operand of mma.sync m16n8k16
 //    (rows G..15 zero); S = Q K^T comes from ldmatrix'ed K rows (the stages
@@ -312,11 +314,12 @@ __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* u
   return I;
 }
 
-// Producer warp: walks this CTA's items in order and fills the stage ring.
-// Dense rows and gathered rows are copied the same way: each lane moves
-// 16-byte chunks with cp.async (XOR-swizzled destination on the tensor-core
-// path) and arrives on the stage's mbarrier when its copies land; fp32 dense
-// stages use one bulk copy per operand instead.
+// Producer warp: takes this CTA's items as they are fetched (warp 0 fetches
+// and publishes the ids) and fills the stage ring with its share of every
+// stage's rows.  Full dense bf16 stages arrive as 2-D TMA boxes; gathered
+// rows and partial stages as 16-byte cp.async chunks (XOR-swizzled on the
+// tensor-core path), each lane arriving on the stage's mbarrier when its
+// copies land; fp32 dense stages use one bulk copy per operand.
 template <class C>
 __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units, int n_units,
                                              int total, unsigned char* smem, uint32_t bar_full,
