@@ -631,36 +631,46 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
 
 // Consumer warp, tensor-core path (bf16): warp `warp` takes rows
 // [16 * (warp % 4), +16) of every stage whose index has parity warp / 4.
+// S^T = K Q^T with the warp's 16 K rows as the A operand and the query heads
+// as the N dimension (heads G..7 are zero), then O^T += V^T P^T with 16
+// dimensions of V^T per A tile and P^T as the B operand, moved from the
+// accumulator layout by movmatrix.trans.  fp32 accumulation throughout; P is
+// rounded to bf16 for the product.  Lane (g, t) = (lane / 4, lane % 4) holds
+// S^T and O^T at rows (or dimensions) g and g + 8 and heads 2t and 2t + 1.
 template <int D, int G>
 __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo& I,
                                               unsigned char* smem, uint32_t bar_full,
                                               uint32_t bar_empty, volatile int* abort_flag,
                                               uint32_t& stage, int warp, int lane, float* red) {
   using C = AttnCfg<bf16_t, D, G>;
-  constexpr int KS = D / 16;  // k-steps of QK
-  constexpr int NTD = D / 8;  // 8-column output tiles of PV
-  const int g4 = lane >> 2, t4 = lane & 3;
+  constexpr int KS = D / 16;  // 16-dimension k-steps of S^T
+  constexpr int DT = D / 16;  // 16-dimension tiles of O^T
+  const int g = lane >> 2, t = lane & 3;
   const int wslot = warp & 3, wpar = warp >> 2;
   const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
   const bool emit = a.emit && I.slow;
   const bool emit_norm = emit && a.knorm != nullptr;
   const float qs = a.qscale;
 
-  // A operand: q of head g4 (zero for padding heads), bf16 pairs.
-  uint32_t qa[KS][2];
+  // B operand of S^T: q of head g (zero for heads >= G), bf16 pairs at
+  // dimensions 16 ks + 2t and 16 ks + 8 + 2t.
+  uint32_t qb[KS][2];
   {
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(a.q) +
-                           ((size_t(I.b) * a.H_q + size_t(I.g) * G + (g4 < G ? g4 : 0)) * D) / 2;
+                           ((size_t(I.b) * a.H_q + size_t(I.g) * G + (g < G ? g : 0)) * D) / 2;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = g4 < G ? __ldg(qrow + ks * 8 + t4) : 0u;
-      qa[ks][1] = g4 < G ? __ldg(qrow + ks * 8 + 4 + t4) : 0u;
+      qb[ks][0] = g < G ? __ldg(qrow + ks * 8 + t) : 0u;
+      qb[ks][1] = g < G ? __ldg(qrow + ks * 8 + 4 + t) : 0u;
     }
   }
-  float acc[NTD][2];
+  float acc[DT][4];
 #pragma unroll
-  for (int c = 0; c < NTD; ++c) acc[c][0] = acc[c][1] = 0.f;
-  float m = -INFINITY, zl = 0.f;
+  for (int c = 0; c < DT; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, zl[2] = {0.f, 0.f};  // heads 2t, 2t + 1
+  // ldmatrix row addresses: K rows for the A tiles of S^T, V rows for V^T
+  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8, kch = lane >> 4;
+  const int vrow = (lane & 7) + ((lane >> 4) & 1) * 8, vch = (lane >> 3) & 1;
 
   for (int si = 0; si < I.n_st; ++si, ++stage) {
     if (int(stage & 1u) != wpar) continue;
@@ -674,118 +684,126 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
     if (have && nw > 0) {
       const uint32_t kst = kbase + slot * C::STAGE_B;
       const uint32_t vst = vbase + slot * C::STAGE_B;
-      // ---- S = Q K^T over the warp's 16 rows (two 8-row column tiles)
-      float sacc[2][2];
-      float nsq[2] = {0.f, 0.f};
+      // ---- S^T = K Q^T over the warp's 16 rows (two accumulator chains);
+      // with key norms, the squares of the same K fragments.  The two
+      // variants are separate loops, so neither carries a branch that would
+      // keep the compiler from issuing the next k-step's loads early.
+      float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float nsq[2] = {0.f, 0.f};  // rows g, g + 8
+      auto qk = [&](auto with_norm) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sacc[nt][0] = sacc[nt][1] = 0.f;
-        const int row = r0 + nt * 8 + (lane & 7);
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kst + C::chunk_off(r0 + krow, 2 * ks + kch), a0, a1, a2, a3);
+          mma_bf16_16816(sa[ks & 1], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          if constexpr (decltype(with_norm)::value) {
+            const uint32_t lo[2] = {a0, a2}, hi[2] = {a1, a3};
 #pragma unroll
-        for (int kp = 0; kp < KS / 2; ++kp) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kst + C::chunk_off(row, kp * 4 + (lane >> 3)), b0, b1, b2, b3);
-          mma_bf16_top8(sacc[nt][0], sacc[nt][1], qa[2 * kp][0], qa[2 * kp][1], b0, b1);
-          mma_bf16_top8(sacc[nt][0], sacc[nt][1], qa[2 * kp + 1][0], qa[2 * kp + 1][1], b2, b3);
-          if (emit_norm) {
-            const uint32_t bb[4] = {b0, b1, b2, b3};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float lo = __uint_as_float(bb[j] << 16), hi = __uint_as_float(bb[j] & 0xffff0000u);
-              nsq[nt] = fmaf(lo, lo, fmaf(hi, hi, nsq[nt]));
+            for (int j = 0; j < 2; ++j) {
+              const float x0 = __uint_as_float(lo[j] << 16), x1 = __uint_as_float(lo[j] & 0xffff0000u);
+              const float y0 = __uint_as_float(hi[j] << 16), y1 = __uint_as_float(hi[j] & 0xffff0000u);
+              nsq[0] = fmaf(x0, x0, fmaf(x1, x1, nsq[0]));
+              nsq[1] = fmaf(y0, y0, fmaf(y1, y1, nsq[1]));
             }
           }
         }
+      };
+      if (emit_norm) {
+        qk(std::true_type{});
+      } else {
+        qk(std::false_type{});
       }
-      // this lane's logits: head g4, rows r0 + 8 nt + 2 t4 + j (log2 domain)
-      float l[4];
+      // this lane's logits (log2 domain): [row g / g + 8][head 2t / 2t + 1]
+      float l[2][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int rr = nt * 8 + 2 * t4 + j;
-          l[nt * 2 + j] = rr < nw ? sacc[nt][j] * qs : -INFINITY;
-        }
+        for (int h = 0; h < 2; ++h)
+          l[r][h] = g + 8 * r < nw ? (sa[0][2 * r + h] + sa[1][2 * r + h]) * qs : -INFINITY;
       if (emit) {
-        if (g4 < G) {
-          float* lo = a.logits + (size_t(I.u) * a.max_len + c0 + r0) * G + g4;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+        for (int r = 0; r < 2; ++r) {
+          const int rr = g + 8 * r;
+          if (rr < nw) {
+            float* lo = a.logits + (size_t(I.u) * a.max_len + c0 + r0 + rr) * G;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const int rr = nt * 8 + 2 * t4 + j;
-              if (rr < nw) lo[rr * G] = l[nt * 2 + j];
-            }
+            for (int h = 0; h < 2; ++h)
+              if (2 * t + h < G) lo[2 * t + h] = l[r][h];
+          }
         }
         if (emit_norm) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            float v = nsq[nt];
+          for (int r = 0; r < 2; ++r) {
+            float v = nsq[r];
             v += __shfl_xor_sync(kFull, v, 1);
             v += __shfl_xor_sync(kFull, v, 2);
-            const int rr = nt * 8 + g4;
-            if (t4 == 0 && rr < nw) a.knorm[size_t(I.u) * a.max_len + c0 + r0 + rr] = sqrtf(v);
+            const int rr = g + 8 * r;
+            if (t == 0 && rr < nw) a.knorm[size_t(I.u) * a.max_len + c0 + r0 + rr] = sqrtf(v);
           }
         }
       }
-      // ---- online softmax for head g4 (the quad shares the head)
-      float tmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
-      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
-      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
-      if (tmax > m) {
-        const float al = exp2f(m - tmax);
+      // ---- online softmax per head over the warp's 16 rows (lanes with the
+      // same t share a head; the max runs over g)
+      float p[2][2];
 #pragma unroll
-        for (int c = 0; c < NTD; ++c) {
-          acc[c][0] *= al;
-          acc[c][1] *= al;
+      for (int h = 0; h < 2; ++h) {
+        float tmax = fmaxf(l[0][h], l[1][h]);
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+        if (tmax > m[h]) {
+          const float al = exp2f(m[h] - tmax);
+#pragma unroll
+          for (int c = 0; c < DT; ++c) {
+            acc[c][h] *= al;
+            acc[c][2 + h] *= al;
+          }
+          zl[h] *= al;
+          m[h] = tmax;
         }
-        zl *= al;
-        m = tmax;
+        p[0][h] = exp2f(l[0][h] - m[h]);
+        p[1][h] = exp2f(l[1][h] - m[h]);
+        zl[h] += p[0][h] + p[1][h];
       }
-      float p[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        p[j] = exp2f(l[j] - m);
-        zl += p[j];
-      }
-      const uint32_t pa_lo = pack_bf16x2(p[0], p[1]);  // rows 2t4, 2t4+1
-      const uint32_t pa_hi = pack_bf16x2(p[2], p[3]);  // rows 8+2t4, 9+2t4
+      // P^T as the B operand: rows 0-7 and 8-15, transposed from the
+      // accumulator layout (row g, heads 2t..) to (rows 2t.., head g)
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p[0][0], p[0][1]));
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p[1][0], p[1][1]));
       // rows past the valid ones hold stale or unset data: zero their V
       uint32_t m_lo = 0xffffffffu, m_hi = 0xffffffffu;
       if (nw < C::MW) {
-        m_lo = (2 * t4 < nw ? 0x0000ffffu : 0u) | (2 * t4 + 1 < nw ? 0xffff0000u : 0u);
-        m_hi = (8 + 2 * t4 < nw ? 0x0000ffffu : 0u) | (9 + 2 * t4 < nw ? 0xffff0000u : 0u);
+        m_lo = (2 * t < nw ? 0x0000ffffu : 0u) | (2 * t + 1 < nw ? 0xffff0000u : 0u);
+        m_hi = (8 + 2 * t < nw ? 0x0000ffffu : 0u) | (9 + 2 * t < nw ? 0xffff0000u : 0u);
       }
-      // ---- O += P V
-      const int vrow = r0 + ((lane >> 3) & 1) * 8 + (lane & 7);
+      // ---- O^T += V^T P^T, 16 dimensions per tile
 #pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_trans(vst + C::chunk_off(vrow, 2 * dp + (lane >> 4)), b0, b1, b2, b3);
-        b0 &= m_lo;
-        b1 &= m_hi;
-        b2 &= m_lo;
-        b3 &= m_hi;
-        mma_bf16_top8(acc[2 * dp][0], acc[2 * dp][1], pa_lo, pa_hi, b0, b1);
-        mma_bf16_top8(acc[2 * dp + 1][0], acc[2 * dp + 1][1], pa_lo, pa_hi, b2, b3);
+      for (int dt = 0; dt < DT; ++dt) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vst + C::chunk_off(r0 + vrow, 2 * dt + vch), v0, v1, v2, v3);
+        mma_bf16_16816(acc[dt], v0 & m_lo, v1 & m_lo, v2 & m_hi, v3 & m_hi, pb0, pb1);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
   }
-  // ---- warp state: one head per quad
-  zl += __shfl_xor_sync(kFull, zl, 1);
-  zl += __shfl_xor_sync(kFull, zl, 2);
-  if (g4 < G) {
-    float* rw = red + g4 * (D + 2);
-    if (t4 == 0) {
-      rw[0] = m;
-      rw[1] = zl;
-    }
+  // ---- warp state of heads 2t, 2t + 1 (sums over the rows g)
 #pragma unroll
-    for (int c = 0; c < NTD; ++c) {
-      rw[2 + 8 * c + 2 * t4] = acc[c][0];
-      rw[2 + 8 * c + 2 * t4 + 1] = acc[c][1];
+  for (int h = 0; h < 2; ++h) {
+    zl[h] += __shfl_xor_sync(kFull, zl[h], 4);
+    zl[h] += __shfl_xor_sync(kFull, zl[h], 8);
+    zl[h] += __shfl_xor_sync(kFull, zl[h], 16);
+    const int hh = 2 * t + h;
+    if (hh < G) {
+      float* rw = red + hh * (D + 2);
+      if (g == 0) {
+        rw[0] = m[h];
+        rw[1] = zl[h];
+      }
+#pragma unroll
+      for (int c = 0; c < DT; ++c) {
+        rw[2 + 16 * c + g] = acc[c][h];
+        rw[2 + 16 * c + g + 8] = acc[c][2 + h];
+      }
     }
   }
 }

@@ -157,20 +157,24 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "r"(addr));
 }
 
-// D = A * B + D for one m16n8k16 bf16 tile with fp32 accumulation, where rows
-// 8..15 of A are zero: a0 holds A[g][2t..2t+1], a2 holds A[g][2t+8..2t+9]
-// (g = lane / 4, t = lane % 4); d0, d1 are D[g][2t..2t+1].  Rows 8..15 of D
-// are not kept.
-__device__ __forceinline__ void mma_bf16_top8(float& d0, float& d1, uint32_t a0, uint32_t a2,
-                                              uint32_t b0, uint32_t b1) {
-  float x2, x3;
+// D = A * B + D for one full m16n8k16 bf16 tile (fp32 accumulation):
+// a0 = A[g][2t..], a1 = A[g + 8][2t..], a2 = A[g][2t + 8..], a3 = A[g + 8][2t + 8..];
+// b0 = B[2t..][g], b1 = B[2t + 8..][g]; d = {D[g][2t], D[g][2t + 1], D[g + 8][2t], D[g + 8][2t + 1]}.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
-      : "=f"(d0), "=f"(d1), "=f"(x2), "=f"(x3)
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(0.f),
-        "f"(0.f));
-  (void)x2;
-  (void)x3;
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8 x 8 b16 matrix held one pair per lane (lane 4r + c holds
+// row r, columns 2c and 2c + 1): afterwards the lane holds the transposed
+// matrix's row r, i.e. the original's column r at rows 2c and 2c + 1.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.

@@ -60,15 +60,6 @@ struct VerifyCfg {
   }
 };
 
-// D = A * B + D for one full m16n8k16 bf16 tile (fp32 accumulation).
-__device__ __forceinline__ void mma_bf16_full(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                              uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 template <int D, int G>
 __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo& I,
                                             unsigned char* smem, uint32_t bar_full,
@@ -138,8 +129,8 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kst + C::chunk_off(row, kp * 4 + (lane >> 3)), b0, b1, b2, b3);
           const int k0 = 2 * kp, k1 = 2 * kp + 1;
-          mma_bf16_full(sacc[nt], qa[k0][0], qa[k0][1], qa[k0][2], qa[k0][3], b0, b1);
-          mma_bf16_full(sacc[nt], qa[k1][0], qa[k1][1], qa[k1][2], qa[k1][3], b2, b3);
+          mma_bf16_16816(sacc[nt], qa[k0][0], qa[k0][1], qa[k0][2], qa[k0][3], b0, b1);
+          mma_bf16_16816(sacc[nt], qa[k1][0], qa[k1][1], qa[k1][2], qa[k1][3], b2, b3);
         }
       }
       // collected logit sums of this tile's rows (lanes with g4 == 0 hold them)
@@ -209,8 +200,8 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
         b1 &= m_hi;
         b2 &= m_lo;
         b3 &= m_hi;
-        mma_bf16_full(acc[2 * dp], pa[0][0], pa[1][0], pa[0][1], pa[1][1], b0, b1);
-        mma_bf16_full(acc[2 * dp + 1], pa[0][0], pa[1][0], pa[0][1], pa[1][1], b2, b3);
+        mma_bf16_16816(acc[2 * dp], pa[0][0], pa[1][0], pa[0][1], pa[1][1], b0, b1);
+        mma_bf16_16816(acc[2 * dp + 1], pa[0][0], pa[1][0], pa[0][1], pa[1][1], b2, b3);
       }
     }
     if (xtile) {
