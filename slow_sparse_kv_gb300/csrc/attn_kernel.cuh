@@ -689,7 +689,10 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
       // variants are separate loops, so neither carries a branch that would
       // keep the compiler from issuing the next k-step's loads early.
       float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float nsq[2] = {0.f, 0.f};  // rows g, g + 8
+      // Key norms on the tensor cores: the A fragments of the K tile are also
+      // the B fragments of K^T, so K K^T (16 x 16, in two 8-column halves)
+      // accumulates next to S^T; its diagonal holds the squared row norms.
+      float gram[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       auto qk = [&](auto with_norm) {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -697,14 +700,8 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
           ldsm_x4(kst + C::chunk_off(r0 + krow, 2 * ks + kch), a0, a1, a2, a3);
           mma_bf16_16816(sa[ks & 1], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
           if constexpr (decltype(with_norm)::value) {
-            const uint32_t lo[2] = {a0, a2}, hi[2] = {a1, a3};
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const float x0 = __uint_as_float(lo[j] << 16), x1 = __uint_as_float(lo[j] & 0xffff0000u);
-              const float y0 = __uint_as_float(hi[j] << 16), y1 = __uint_as_float(hi[j] & 0xffff0000u);
-              nsq[0] = fmaf(x0, x0, fmaf(x1, x1, nsq[0]));
-              nsq[1] = fmaf(y0, y0, fmaf(y1, y1, nsq[1]));
-            }
+            mma_bf16_16816(gram[0], a0, a1, a2, a3, a0, a2);  // columns: rows 0-7
+            mma_bf16_16816(gram[1], a0, a1, a2, a3, a1, a3);  // columns: rows 8-15
           }
         }
       };
@@ -731,15 +728,13 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
               if (2 * t + h < G) lo[2 * t + h] = l[r][h];
           }
         }
-        if (emit_norm) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            float v = nsq[r];
-            v += __shfl_xor_sync(kFull, v, 1);
-            v += __shfl_xor_sync(kFull, v, 2);
-            const int rr = g + 8 * r;
-            if (t == 0 && rr < nw) a.knorm[size_t(I.u) * a.max_len + c0 + r0 + rr] = sqrtf(v);
-          }
+        if (emit_norm && t == (g >> 1)) {
+          // lane (g, g / 2) holds the diagonal entries (g, g) and (g + 8, g + 8)
+          const float n0 = (g & 1) ? gram[0][1] : gram[0][0];
+          const float n1 = (g & 1) ? gram[1][3] : gram[1][2];
+          float* kn = a.knorm + size_t(I.u) * a.max_len + c0 + r0;
+          if (g < nw) kn[g] = sqrtf(n0);
+          if (g + 8 < nw) kn[g + 8] = sqrtf(n1);
         }
       }
       // ---- online softmax per head over the warp's 16 rows (lanes with the
