@@ -82,14 +82,14 @@ def schedule_counts(slow_masks: np.ndarray):
 # DRAM traffic of the attention kernel relative to its algorithmic bytes,
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # decode driver's mixed launch: batch 8 at context 131072, sequence 0
-# refreshing and seven fast -- 662.85 MB read + 7.30 MB written for
+# refreshing and seven fast -- 662.85 MB read + 7.26 MB written for
 # 661.77 MB algorithmic.  It holds for the kernel code it was taken on (the
 # SHA-256 of the sources below with comments and whitespace removed); after
 # any change to that code the roofline reports null traffic until the
 # capture is repeated.
-ATTN_TRAFFIC = {"ratio": (662854400 + 7298816) / 661766144,
+ATTN_TRAFFIC = {"ratio": (662851584 + 7255808) / 661766144,
                 "sources": ["attn_kernel.cuh", "attn_bf16.cu", "common.cuh", "sfi_internal.h", "api.cpp"],
-                "sha256": "f56a9db0b11883ac6ac8cdb3499f93d2cd4937b462eb29cccbfec0c4891be0da"}
+                "sha256": "cf6a9e28e3112c443a52ef5bd068354941aa45b23ddce22f97bd696ddb5e2bac"}
 
 
 def attn_code_hash() -> str:
