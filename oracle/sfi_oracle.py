@@ -28,8 +28,9 @@ notes): f is the softmax probability of the decode row averaged over the query
 heads of a KV head; the prior is the key L2 norm normalised over the eligible
 set E = [n_sink, n - window); the window includes the current token; ties in
 Top-K go to the lower position and the result is returned in ascending
-position order; Soft-NMS and cross-head exclusivity are not applied (the pages
-give no formula for them).
+position order; Soft-NMS and cross-head exclusivity (named on the pages without
+a formula) are optional refinements in the builder's reading stated at the
+end of this module, off unless asked for.
 
 Parity: every function here is pinned by ``tests/test_oracle.py`` against
 library routines, closed forms, brute force or hand-computed fixtures; the
@@ -280,3 +281,77 @@ def draft_step(q, K, V, n_pre: int, n: int, T: np.ndarray):
     rows = [draft_rows(n_pre, n, T)] * hkv
     o, _, _ = attention_over_rows(q, K, V, rows)
     return o
+
+
+# ------------------------------------------------------------------ selector refinements
+#
+# The SFI pages list two refinements of the selector beside the fusion: a
+# Soft-NMS that keeps one head from spending its budget on neighbouring,
+# correlated tokens, and a cross-head exclusivity that penalises a token
+# chosen again by another head (it/pt/ko pages, section "Selector").  They
+# give no formula for either, so these functions are the builder's reading:
+#
+# * Soft-NMS is the greedy Gaussian-decay Soft-NMS of Bodla et al. (ICCV
+#   2017) with position i of E treated as the 1-D box [i - rho, i + rho]:
+#   repeatedly take the largest current score (ties to the lower position);
+#   every remaining position j whose box overlaps the taken one (|i - j| <=
+#   2 rho) has its score multiplied by exp(-IoU(i, j)^2 / sigma).  The first
+#   min(k, |E|) positions taken are the selection.  rho = 0 is plain Top-K.
+# * Exclusivity: the KV heads of a sequence select in index order; head g's
+#   fused scores are multiplied by exp(-beta * c_i), where c_i counts the
+#   heads before g whose selection holds i.  beta = 0 is no exclusivity.
+
+def nms_overlap(d: int, rho: int) -> float:
+    """Intersection over union of the position boxes [i - rho, i + rho] and
+    [j - rho, j + rho] at distance d = |i - j| (0 once they no longer meet)."""
+    w = 2 * rho + 1
+    return max(0, w - d) / (w + d)
+
+
+def soft_nms(score: np.ndarray, lo: int, hi: int, k: int, rho: int, sigma: float):
+    """Greedy Soft-NMS over E = [lo, hi): the first min(k, |E|) positions taken,
+    in the order taken, and each one's score at the moment it was taken."""
+    if hi <= lo or k <= 0:
+        return np.zeros(0, np.int64), np.zeros(0)
+    v = np.array(score[lo:hi], np.float64)
+    alive = np.ones(hi - lo, bool)
+    taken, at = [], []
+    for _ in range(min(k, hi - lo)):
+        i = int(np.argmax(np.where(alive, v, -np.inf)))  # first maximum: lower position
+        taken.append(lo + i)
+        at.append(v[i])
+        alive[i] = False
+        for j in range(max(0, i - 2 * rho), min(hi - lo, i + 2 * rho + 1)):
+            if alive[j]:
+                o = nms_overlap(abs(i - j), rho)
+                v[j] *= math.exp(-o * o / sigma)
+    return np.array(taken, np.int64), np.array(at)
+
+
+def refine_head(s_g: np.ndarray, counts: np.ndarray, lo: int, hi: int, k: int, rho: int,
+                sigma: float, beta: float):
+    """Selection of one KV head given the counts of earlier heads' picks.
+
+    Returns (ascending positions, each position's score when it was taken,
+    in the same order)."""
+    sh = np.asarray(s_g, np.float64) * np.exp(-beta * np.asarray(counts, np.float64))
+    if rho > 0:
+        taken, at = soft_nms(sh, lo, hi, k, rho, sigma)
+    else:
+        taken = top_k(sh, lo, hi, k)
+        at = sh[taken]
+    order = np.argsort(taken)
+    return taken[order], at[order]
+
+
+def refined_select(s: np.ndarray, lo: int, hi: int, k: int, rho: int, sigma: float,
+                   beta: float) -> List[np.ndarray]:
+    """Selections of every KV head of one sequence (s [H_kv, n]), heads in
+    index order, with exclusivity (beta) and Soft-NMS (rho, sigma)."""
+    counts = np.zeros(s.shape[1])
+    out = []
+    for g in range(s.shape[0]):
+        idx, _ = refine_head(s[g], counts, lo, hi, k, rho, sigma, beta)
+        counts[idx] += 1
+        out.append(idx)
+    return out

@@ -420,3 +420,130 @@ def test_workload_recipe():
     assert q.shape == (8, 64)
     tr = W.cfg2().boundary_trace()
     assert tr.shape == (256, 8) and 0.02 < tr.mean() < 0.09
+
+
+# ------------------------------------------------- selector refinements (builder's reading)
+
+def pin_refine_hand_fixture(O):
+    g = gold("refine_hand.json")
+    for c in g["soft_nms"]:
+        sc = np.array(c["score"])
+        for kk in (2, 3, 4):
+            if f"k{kk}_taken" not in c:
+                continue
+            taken, at = O.soft_nms(sc, c["lo"], c["hi"], kk, c["rho"], c["sigma"])
+            assert taken.tolist() == c[f"k{kk}_taken"]
+            np.testing.assert_allclose(at, c[f"k{kk}_at"], atol=5e-8, rtol=0)
+        if "plain_top3" in c:
+            assert O.top_k(sc, c["lo"], c["hi"], 3).tolist() == c["plain_top3"]
+    for c in g["exclusivity"]:
+        s = np.array(c["s"])
+        got = O.refined_select(s, c["lo"], c["hi"], c["k"], 0, 1.0, c["beta"])
+        assert [x.tolist() for x in got] == c["idx"]
+        got0 = O.refined_select(s, c["lo"], c["hi"], c["k"], 0, 1.0, 0.0)
+        assert [x.tolist() for x in got0] == c["idx_beta0"]
+
+
+def test_refine_hand_fixture():
+    pin_refine_hand_fixture(O)
+
+
+def pin_refine_without_refinement_is_topk(O):
+    """rho = 0 (or an infinitely wide decay) and beta = 0 leave plain Top-K."""
+    rng = np.random.default_rng(7)
+    for n, k in [(40, 7), (25, 25), (30, 40)]:
+        s = rng.random((3, n))
+        for rho, sigma in [(0, 1.0), (2, math.inf)]:
+            got = O.refined_select(s, 3, n - 4, k, rho, sigma, 0.0)
+            for g in range(3):
+                assert got[g].tolist() == O.top_k(s[g], 3, n - 4, k).tolist()
+
+
+def test_refine_without_refinement_is_topk():
+    pin_refine_without_refinement_is_topk(O)
+
+
+def _hard_nms_by_enumeration(sc, lo, hi, k, rho):
+    """Among k-subsets of [lo, hi) whose positions are pairwise more than
+    2 rho apart (boxes that do not overlap), the one whose scores, sorted
+    from the largest, are lexicographically largest -- what greedy hard
+    suppression keeps (the greedy choice on an independence system)."""
+    best, best_key = None, None
+    for sub in itertools.combinations(range(lo, hi), k):
+        if any(b - a <= 2 * rho for a, b in zip(sub, sub[1:])):
+            continue
+        key = sorted((sc[i] for i in sub), reverse=True)
+        if best_key is None or key > best_key:
+            best, best_key = list(sub), key
+    return best
+
+
+def pin_soft_nms_hard_limit_by_enumeration(O):
+    """As sigma -> 0 every overlapping neighbour of a taken position drops to
+    zero, i.e. hard NMS; with enough room for k separated picks the result is
+    the enumerated best separated subset."""
+    rng = np.random.default_rng(11)
+    for rho, k, n in [(1, 3, 12), (2, 2, 12), (1, 2, 9)]:
+        for _ in range(6):
+            sc = rng.random(n) + 0.01
+            taken, _ = O.soft_nms(sc, 0, n, k, rho, 1e-300)
+            assert sorted(taken.tolist()) == _hard_nms_by_enumeration(sc, 0, n, k, rho)
+
+
+def test_soft_nms_hard_limit_by_enumeration():
+    pin_soft_nms_hard_limit_by_enumeration(O)
+
+
+def pin_soft_nms_greedy_trace(O):
+    """Each pick is the best remaining position at that moment: its score at
+    the pick equals its fused score times the decays of the earlier picks
+    within 2 rho, and no remaining position then scores higher (ties: the
+    lower position first)."""
+    rng = np.random.default_rng(5)
+    for rho, sigma in [(1, 0.3), (2, 1.5), (3, 0.05)]:
+        n = 60
+        sc = rng.random(n)
+        taken, at = O.soft_nms(sc, 4, n, 25, rho, sigma)
+        assert len(set(taken.tolist())) == 25 and taken.min() >= 4 and taken.max() < n
+
+        def current(j, before):
+            x = sc[j]
+            for p in before:
+                d = abs(p - j)
+                if d <= 2 * rho:
+                    iou = (2 * rho + 1 - d) / (2 * rho + 1 + d)
+                    x *= math.exp(-iou * iou / sigma)
+            return x
+
+        for t, p in enumerate(taken):
+            before = taken[:t].tolist()
+            assert math.isclose(at[t], current(p, before), rel_tol=1e-12)
+            for j in range(4, n):
+                if j == p or j in before:
+                    continue
+                cj = current(j, before)
+                assert cj < at[t] or (cj == at[t] and j > p)
+        assert np.all(np.diff(at) <= 1e-15)  # scores at the pick never increase
+
+
+def test_soft_nms_greedy_trace():
+    pin_soft_nms_greedy_trace(O)
+
+
+def pin_exclusivity_limit_disjoint(O):
+    """With an overwhelming beta a position taken by an earlier head is never
+    taken again while enough untaken positions remain: head g's set is the
+    Top-K of its scores with the earlier heads' picks removed."""
+    rng = np.random.default_rng(13)
+    s = rng.random((4, 80)) + 0.01
+    got = O.refined_select(s, 2, 70, 10, 0, 1.0, 1e6)
+    seen = np.zeros(80, bool)
+    for g in range(4):
+        masked = np.where(seen, 0.0, s[g])
+        assert got[g].tolist() == O.top_k(masked, 2, 70, 10).tolist()
+        assert not seen[got[g]].any()
+        seen[got[g]] = True
+
+
+def test_exclusivity_limit_disjoint():
+    pin_exclusivity_limit_disjoint(O)

@@ -70,6 +70,12 @@ MUTANTS = {
     "schedule budget strict": ("schedule", None),
     "collect uses rows 0 and 1": ("collected_logit_sum", None),
     "verify without causal tail": ("verify_attention", None),
+    "soft-nms IoU without the distance in the union": ("nms_overlap", lambda d, rho: max(0, 2 * rho + 1 - d) / (2 * rho + 1)),
+    "soft-nms reaches only rho": ("soft_nms", None),
+    "soft-nms decay with IoU not squared": ("soft_nms", None),
+    "soft-nms ties to higher position": ("soft_nms", None),
+    "exclusivity rewards repeated picks": ("refine_head", None),
+    "exclusivity ignores earlier heads": ("refined_select", None),
 }
 
 
@@ -98,9 +104,43 @@ def _verify_no_tail(q_rows, K, V, n_pre):
     return o, logits
 
 
+def _soft_nms_variant(reach, power, last_max):
+    def run(score, lo, hi, k, rho, sigma):
+        if hi <= lo or k <= 0:
+            return np.zeros(0, np.int64), np.zeros(0)
+        v = np.array(score[lo:hi], np.float64)
+        alive = np.ones(hi - lo, bool)
+        taken, at = [], []
+        for _ in range(min(k, hi - lo)):
+            cur = np.where(alive, v, -np.inf)
+            i = int(len(cur) - 1 - np.argmax(cur[::-1])) if last_max else int(np.argmax(cur))
+            taken.append(lo + i); at.append(v[i]); alive[i] = False
+            r = reach(rho)
+            for j in range(max(0, i - r), min(hi - lo, i + r + 1)):
+                if alive[j]:
+                    o = O.nms_overlap(abs(i - j), rho)
+                    v[j] *= math.exp(-o ** power / sigma)
+        return np.array(taken, np.int64), np.array(at)
+    return run
+
+
+def _refine_head_reward(s_g, counts, lo, hi, k, rho, sigma, beta):
+    return O.__dict__["_orig_refine_head"](s_g, counts, lo, hi, k, rho, sigma, -beta)
+
+
+def _refined_select_no_counts(s, lo, hi, k, rho, sigma, beta):
+    return [O.refine_head(s[g], np.zeros(s.shape[1]), lo, hi, k, rho, sigma, beta)[0]
+            for g in range(s.shape[0])]
+
+
 SPECIAL = {"schedule budget strict": _schedule_strict,
            "collect uses rows 0 and 1": _collect_rows01,
-           "verify without causal tail": _verify_no_tail}
+           "verify without causal tail": _verify_no_tail,
+           "soft-nms reaches only rho": _soft_nms_variant(lambda r: r, 2, False),
+           "soft-nms decay with IoU not squared": _soft_nms_variant(lambda r: 2 * r, 1, False),
+           "soft-nms ties to higher position": _soft_nms_variant(lambda r: 2 * r, 2, True),
+           "exclusivity rewards repeated picks": _refine_head_reward,
+           "exclusivity ignores earlier heads": _refined_select_no_counts}
 
 
 def _caught(monkeypatch) -> bool:
