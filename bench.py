@@ -82,14 +82,14 @@ def schedule_counts(slow_masks: np.ndarray):
 # DRAM traffic of the attention kernel relative to its algorithmic bytes,
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # decode driver's mixed launch: batch 8 at context 131072, sequence 0
-# refreshing and seven fast -- 662.85 MB read + 7.26 MB written for
+# refreshing and seven fast -- 662.85 MB read + 7.24 MB written for
 # 661.77 MB algorithmic.  It holds for the kernel code it was taken on (the
 # SHA-256 of the sources below with comments and whitespace removed); after
 # any change to that code the roofline reports null traffic until the
 # capture is repeated.
-ATTN_TRAFFIC = {"ratio": (662851584 + 7255808) / 661766144,
+ATTN_TRAFFIC = {"ratio": (662852608 + 7235840) / 661766144,
                 "sources": ["attn_kernel.cuh", "attn_bf16.cu", "common.cuh", "sfi_internal.h", "api.cpp"],
-                "sha256": "cf6a9e28e3112c443a52ef5bd068354941aa45b23ddce22f97bd696ddb5e2bac"}
+                "sha256": "8566c9896059848c098d615916625f82e709e8ebc6b8d9e0f69842f053afc7e7"}
 
 
 def attn_code_hash() -> str:
@@ -620,6 +620,22 @@ def run_kernel_cases(args):
         "fast_contig": (lambda: sfi.sfi_fast_attn(lay, prm, q, R.K[0], R.V[0], contig, cnt, out, ws),
                         B * (wl.n_sink + wl.k + wl.window) * row),
     }
+    # selector refinements (Soft-NMS with rho = 1, sigma = 0.5; then with
+    # exclusivity beta = 0.5, KV heads one after another) on the same evidence
+    ref_ws = {}
+    idx_r = torch.empty_like(idx)
+    cnt_r = torch.empty_like(cnt)
+
+    def refined(rho, sigma, beta):
+        ref = sfi.sfi_refine(rho, sigma, beta)
+        key = (rho, sigma, beta)
+        if key not in ref_ws:
+            ref_ws[key] = torch.zeros(sfi.select_refined_workspace_size(lay, prm, ref), dtype=torch.uint8,
+                                      device=R.dev)
+        return lambda: sfi.sfi_select_refined(lay, prm, ref, f, kn, idx_r, cnt_r, None, ref_ws[key])
+
+    cases["select_nms"] = (refined(1, 0.5, 0.0), B * sh.n_kv_heads * n * 8)
+    cases["select_nms_excl"] = (refined(1, 0.5, 0.5), B * sh.n_kv_heads * n * 8)
     # "mixed": one decode-step launch of the decode driver with sequence 0
     # refreshing (dense + evidence) and the others fast, as in a refresh step
     # of the decode benchmark; its selector runs in line after it.
@@ -662,6 +678,8 @@ def run_kernel_cases(args):
             res[name]["attention_ms"] = round(a_ms / a_n, 4)
             res[name]["attention_GB/s"] = round(nbytes / (a_ms / a_n) / 1e6, 1)
             res[name]["select_ms"] = round(s_ms / max(s_n, 1), 4)
+    for key, w in ref_ws.items():
+        res[f"refine_device_status_{key[2]}"] = sfi.sfi_read_status(w)
     if dctx is not None:
         res["mixed_device_status"] = dctx.read_status()
         dctx.close()

@@ -71,6 +71,7 @@ typedef enum { SFI_F32 = 0, SFI_BF16 = 1 } sfi_dtype;
 #define SFI_DEV_BAD_INDEX      0x2u  /* a selected position outside [0, n_b) */
 #define SFI_DEV_WAIT_TIMEOUT   0x4u  /* a pipeline wait gave up */
 #define SFI_DEV_ITEMS_OVERFLOW 0x8u  /* more work items than the workspace holds */
+#define SFI_DEV_REFINE         0x10u /* a refinement met an inconsistent candidate list */
 
 typedef void* sfi_stream; /* a cudaStream_t */
 
@@ -165,6 +166,41 @@ sfi_status sfi_select(const sfi_layout* layout, const sfi_params* params,
                       const float* evidence, const float* knorm,
                       int32_t* idx_out, int32_t* count_out, float* s_out,
                       void* ws, size_t ws_bytes, sfi_stream stream);
+
+/* Selector refinements (SFI it/pt/ko pages, section "Selector": Soft-NMS
+ * against neighbouring, correlated tokens within one head; cross-head
+ * exclusivity against a token chosen again by another head).  The pages give
+ * no formula; this is the builder's reading:
+ *  - exclusivity: the KV heads of a sequence select in index order; head g
+ *    ranks s_i * exp(-excl_beta * c_i), where c_i counts the heads g' < g
+ *    whose selection holds i (excl_beta = 0: off);
+ *  - Soft-NMS: greedy Gaussian Soft-NMS (Bodla et al., ICCV 2017) with
+ *    position i as the box [i - rho, i + rho], rho = nms_radius: repeatedly
+ *    take the position of E with the largest current score (ties to the
+ *    lower position) and multiply the score of every remaining position j
+ *    with |i - j| <= 2 rho by exp(-IoU(i, j)^2 / nms_sigma), IoU(d) =
+ *    (2 rho + 1 - d) / (2 rho + 1 + d); the first min(k, |E|) positions
+ *    taken are the selection (nms_radius = 0: plain Top-K).
+ * sfi_select_refined computes s exactly as sfi_select in SFI_SELECT_FUSED mode
+ * (the only mode it takes) and writes each (b, g)'s selection to idx_out in
+ * ascending order, count_out = min(k, |E|).  Limits: nms_radius <= 8; with
+ * nms_radius > 0, (k - 1)(4 nms_radius + 1) + 1 <= 24576 (else
+ * SFI_ERR_CAPACITY).  With excl_beta > 0 the KV heads run one after another
+ * (two launches each).  The workspace (sfi_select_refined_workspace_size,
+ * 0 for invalid arguments) follows the shared rules; the call clears the part
+ * it needs cleared itself. */
+typedef struct {
+  int32_t nms_radius; /* rho >= 0 */
+  float nms_sigma;    /* sigma > 0 of the Gaussian decay (read when nms_radius > 0) */
+  float excl_beta;    /* beta >= 0 */
+} sfi_refine;
+
+size_t sfi_select_refined_workspace_size(const sfi_layout* layout, const sfi_params* params,
+                                         const sfi_refine* refine);
+sfi_status sfi_select_refined(const sfi_layout* layout, const sfi_params* params,
+                              const sfi_refine* refine, const float* f, const float* knorm,
+                              int32_t* idx_out, int32_t* count_out, float* s_out,
+                              void* ws, size_t ws_bytes, sfi_stream stream);
 
 /* ---------------------------------------------------------------- fast step */
 

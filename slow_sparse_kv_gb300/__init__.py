@@ -25,6 +25,7 @@ SFI_OK, SFI_ERR_INVALID_ARG, SFI_ERR_UNSUPPORTED, SFI_ERR_CAPACITY, SFI_ERR_WORK
 SFI_F32, SFI_BF16 = 0, 1
 SFI_SELECT_FUSED, SFI_SELECT_LOGIT_SUM_SEQ, SFI_SELECT_LOGIT_SUM_HEAD = 0, 1, 2
 SFI_DEV_LEN_OVER_CAP, SFI_DEV_BAD_INDEX, SFI_DEV_WAIT_TIMEOUT, SFI_DEV_ITEMS_OVERFLOW = 1, 2, 4, 8
+SFI_DEV_REFINE = 16
 
 
 class sfi_layout(ctypes.Structure):
@@ -36,6 +37,10 @@ class sfi_layout(ctypes.Structure):
 class sfi_params(ctypes.Structure):
     _fields_ = [("n_sink", c_int32), ("window", c_int32), ("k", c_int32),
                 ("lam", c_float), ("mode", c_int32)]
+
+
+class sfi_refine(ctypes.Structure):
+    _fields_ = [("nms_radius", c_int32), ("nms_sigma", c_float), ("excl_beta", c_float)]
 
 
 class sfi_ctx_desc(ctypes.Structure):
@@ -58,6 +63,9 @@ EXPORTS = {
     "sfi_select_workspace_size": (c_size_t, [_L, _P]),
     "sfi_select": (c_int32, [_L, _P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_size_t, c_void_p]),
+    "sfi_select_refined_workspace_size": (c_size_t, [_L, _P, POINTER(sfi_refine)]),
+    "sfi_select_refined": (c_int32, [_L, _P, POINTER(sfi_refine), c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "sfi_fast_attn_workspace_size": (c_size_t, [_L, _P]),
     "sfi_fast_attn": (c_int32, [_L, _P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -191,6 +199,19 @@ def sfi_select(layout: Layout, prm: sfi_params, evidence, knorm, idx_out, count_
     _check("sfi_select", lib.sfi_select(
         ctypes.byref(c), ctypes.byref(prm), _ptr(evidence), _ptr(knorm), _ptr(idx_out),
         _ptr(count_out), _ptr(s_out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def sfi_select_refined(layout: Layout, prm: sfi_params, ref: sfi_refine, f, knorm, idx_out,
+                       count_out, s_out=None, ws=None, stream=None):
+    c = layout.c
+    _check("sfi_select_refined", lib.sfi_select_refined(
+        ctypes.byref(c), ctypes.byref(prm), ctypes.byref(ref), _ptr(f), _ptr(knorm), _ptr(idx_out),
+        _ptr(count_out), _ptr(s_out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def select_refined_workspace_size(layout: Layout, prm: sfi_params, ref: sfi_refine) -> int:
+    return int(lib.sfi_select_refined_workspace_size(ctypes.byref(layout.c), ctypes.byref(prm),
+                                                     ctypes.byref(ref)))
 
 
 def sfi_fast_attn(layout: Layout, prm: sfi_params, q, k, v, idx, count, out, ws=None, stream=None):

@@ -457,6 +457,7 @@ sfi_status sfi_select(const sfi_layout* L, const sfi_params* P, const float* evi
   a.k = P->k;
   a.lambda = P->lambda;
   a.mode = P->mode;
+  a.g_only = -1;
   for (int b = 0; b < L->batch; ++b) a.active.bits[b >> 5] |= 1u << (b & 31);
   a.status = reinterpret_cast<uint32_t*>(w + p.status_off);
   const cudaError_t e = launch_select(a, static_cast<cudaStream_t>(stream));

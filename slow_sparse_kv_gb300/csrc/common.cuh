@@ -221,6 +221,32 @@ __device__ __forceinline__ bool seq_is_slow(const SeqMask& m, int b) {
   return (m.bits[b >> 5] >> (b & 31)) & 1u;
 }
 
+// Unsigned key with the order of the float x (larger x, larger key).
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The j-th sequence (in increasing order) whose bit is set in m, or -1.
+__device__ __forceinline__ int active_seq(const SeqMask& m, int j) {
+  for (int w = 0; w < kMaxBatch / 32; ++w) {
+    uint32_t bits = m.bits[w];
+    const int c = __popc(bits);
+    if (j < c) {
+      for (int i = 0; i < j; ++i) bits &= bits - 1;
+      return 32 * w + __ffs(bits) - 1;
+    }
+    j -= c;
+  }
+  return -1;
+}
+
+// Cross-head exclusivity factor exp(-beta * c) of a position that c earlier
+// KV heads of the sequence selected (1 when c = 0).
+__device__ __forceinline__ float excl_factor(uint32_t c, float beta) {
+  return c ? expf(-beta * float(c)) : 1.0f;
+}
+
 // Transpose-reduce across LPR lanes (LPR a power of two, lanes grouped by
 // lane / LPR): on entry each lane holds V partial values; on exit v[0..NV)
 // hold complete sums over the LPR lanes of the entries base .. base+NV-1,

@@ -380,6 +380,7 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   sa.k = d.params.k;
   sa.lambda = d.params.lambda;
   sa.mode = SFI_SELECT_FUSED;
+  sa.g_only = -1;
   sa.active = a.slow;
   sa.status = a.status;
   e = launch_select(sa, ss);

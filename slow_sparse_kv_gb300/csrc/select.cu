@@ -128,11 +128,6 @@ __global__ void __launch_bounds__(kFpassThreads) fpass_kernel(const FpassArgs a)
   }
 }
 
-__device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t u = __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Deterministic block sum (fixed reduction tree for a fixed block size).
 __device__ float sel_block_sum(float v, float* sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -227,20 +222,6 @@ __device__ void block_pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* 
   __syncthreads();
 }
 
-// The j-th sequence (in increasing order) whose bit is set in m, or -1.
-__device__ __forceinline__ int active_seq(const SeqMask& m, int j) {
-  for (int w = 0; w < kMaxBatch / 32; ++w) {
-    uint32_t bits = m.bits[w];
-    const int c = __popc(bits);
-    if (j < c) {
-      for (int i = 0; i < j; ++i) bits &= bits - 1;
-      return 32 * w + __ffs(bits) - 1;
-    }
-    j -= c;
-  }
-  return -1;
-}
-
 // One cluster of kSelCluster CTAs per unit; CTA `rank` owns the positions
 // [rank * ch, (rank + 1) * ch) of [0, n) and keeps their scores in shared
 // memory.  Cluster-wide quantities (the key-norm sum over E, the radix
@@ -276,11 +257,12 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   // (c / units-per-sequence)-th active sequence
   const bool per_seq = a.mode == SFI_SELECT_LOGIT_SUM_SEQ;
   const bool prior = a.mode == SFI_SELECT_FUSED;  // key-norm prior and (1 - lambda) weight
-  const int ups = per_seq ? 1 : a.H_kv;  // units per sequence
+  const bool one_head = prior && a.g_only >= 0;  // only KV head g_only of each sequence
+  const int ups = per_seq || one_head ? 1 : a.H_kv;  // units per sequence
   const int c = blockIdx.x / kSelCluster;
   const int b = active_seq(a.active, c / ups);
   if (b < 0 || b >= a.B) return;  // uniform over the cluster (cannot happen for a valid grid)
-  const int unit = per_seq ? b : b * a.H_kv + c % ups;
+  const int unit = per_seq ? b : b * a.H_kv + (one_head ? a.g_only : c % ups);
   const int u = per_seq ? b * a.H_kv : unit;
   const int n = a.len[b];
   if (n < 1 || n > a.max_len) {
@@ -362,12 +344,18 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
   // ---------------------------------------------------------------- scores
   float* srow = a.s ? a.s + size_t(u) * a.max_len : nullptr;
   const float w_f = prior ? 1.0f - a.lambda : 1.0f;
+  // exclusivity: the fused score is written to s as it is; the selection
+  // ranks it times exp(-beta * picks of the earlier KV heads)
+  const uint8_t* exrow = prior && a.excl ? a.excl + size_t(b) * a.max_len : nullptr;
   for (int base = p0; base < p1; base += kSelCT * kSelU) {
     float kv[kSelU];
+    uint32_t cx[kSelU];
 #pragma unroll
     for (int j = 0; j < kSelU; ++j) {
       const int i = base + j * kSelCT + tid;
-      kv[j] = (prior && i < p1 && i >= lo && i < hi) ? (kns ? kns[i - p0] : kn[i]) : 0.f;
+      const bool e = i < p1 && i >= lo && i < hi;
+      kv[j] = (prior && e) ? (kns ? kns[i - p0] : kn[i]) : 0.f;
+      cx[j] = exrow && e ? exrow[i] : 0u;
     }
 #pragma unroll
     for (int j = 0; j < kSelU; ++j) {
@@ -377,8 +365,9 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
       if (in) {
         v = w_f * sc[i - p0];
         if (prior && i >= lo && i < hi) v = fmaf(coef, kv[j], v);
-        sc[i - p0] = v;
         if (srow) srow[i] = v;
+        v *= excl_factor(cx[j], a.excl_beta);
+        sc[i - p0] = v;
       }
       if (need_radix) hist_add(hist, order_key(v) >> kRadixShift0, in && i >= lo && i < hi);
     }
@@ -616,7 +605,8 @@ cudaError_t launch_select_t(const SelectArgs& args, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   int n_active = 0;
   for (int b = 0; b < a.B; ++b) n_active += int((a.active.bits[b >> 5] >> (b & 31)) & 1u);
-  const int units = n_active * (a.mode == SFI_SELECT_LOGIT_SUM_SEQ ? 1 : a.H_kv);
+  const bool one_unit = a.mode == SFI_SELECT_LOGIT_SUM_SEQ || (a.mode == SFI_SELECT_FUSED && a.g_only >= 0);
+  const int units = n_active * (one_unit ? 1 : a.H_kv);
   if (units == 0) return cudaSuccess;
   select_cluster_kernel<EV_G><<<units * kSelCluster, kSelCT, smem, st>>>(a);
   return cudaGetLastError();

@@ -146,3 +146,38 @@ def test_verify_validation_codes(sfi):
     # every row collected passes the row checks and stops at the missing workspace
     assert verify(Lb, 5, [0, 1, 2, 3, 4], ws=None) == sfi.SFI_ERR_WORKSPACE
     assert verify(Lb, 8, list(range(8)), ws=None) == sfi.SFI_ERR_WORKSPACE
+
+
+def test_refine_validation_codes(sfi):
+    """Soft-NMS / exclusivity refinement: parameter limits and the candidate
+    capacity are checked on the host."""
+    L = layout(sfi)
+    Lbig = layout(sfi, max_len=131072)
+
+    def ref(p, r, lay=L, f=FAKE, ws=FAKE, ws_bytes=1 << 40):
+        rp = ctypes.byref(r) if r is not None else None
+        return sfi.lib.sfi_select_refined(ctypes.byref(lay), ctypes.byref(p), rp, f, FAKE, FAKE, FAKE,
+                                          None, ws, ws_bytes, None)
+
+    P = sfi.params(4, 16, 8, 0.3)
+    R = sfi.sfi_refine
+    assert ref(P, None) == sfi.SFI_ERR_INVALID_ARG
+    assert ref(sfi.params(0, 5, 8, 0.0, mode=sfi.SFI_SELECT_LOGIT_SUM_HEAD), R(1, 0.5, 0.0)) == sfi.SFI_ERR_INVALID_ARG
+    assert ref(P, R(-1, 0.5, 0.0)) == sfi.SFI_ERR_INVALID_ARG
+    assert ref(P, R(9, 0.5, 0.0)) == sfi.SFI_ERR_CAPACITY
+    for sig in (0.0, -1.0, float("nan"), float("inf")):
+        assert ref(P, R(1, sig, 0.0)) == sfi.SFI_ERR_INVALID_ARG
+    for beta in (-0.5, float("nan"), float("inf")):
+        assert ref(P, R(0, 1.0, beta)) == sfi.SFI_ERR_INVALID_ARG
+    # (k - 1)(4 rho + 1) + 1 candidates must fit one CTA's shared memory
+    assert ref(sfi.params(4, 256, 4096, 0.3), R(2, 0.5, 0.0), lay=Lbig) == sfi.SFI_ERR_CAPACITY
+    assert ref(sfi.params(4, 256, 4096, 0.3), R(1, 0.5, 0.0), lay=Lbig, ws=None) == sfi.SFI_ERR_WORKSPACE
+    assert ref(P, R(1, 0.5, 0.2), f=None) == sfi.SFI_ERR_INVALID_ARG
+    assert ref(P, R(1, 0.5, 0.2), ws_bytes=16) == sfi.SFI_ERR_WORKSPACE
+
+    def size(p, r, lay=L):
+        return sfi.lib.sfi_select_refined_workspace_size(ctypes.byref(lay), ctypes.byref(p), ctypes.byref(r))
+    assert size(P, R(9, 0.5, 0.0)) == 0
+    base = sfi.lib.sfi_select_workspace_size(ctypes.byref(L), ctypes.byref(P))
+    # rho = 1: (8 - 1) * 5 + 1 = 36 candidates per unit, beside the counts and the plain plan
+    assert size(P, R(1, 0.5, 0.0)) > size(P, R(0, 0.5, 0.0)) > base

@@ -1,0 +1,156 @@
+"""GPU parity of the selector refinements -- Soft-NMS within a KV head and
+cross-head exclusivity, in the builder's reading of the SFI pages' Selector
+section -- against the fp64 oracle, through the C ABI (binding).
+
+Decisions inside the greedy are taken in fp32 on the GPU and in fp64 in the
+oracle; the oracle is run on the GPU's own fused scores s, and each KV head's
+exclusivity counts come from the GPU's selections of the earlier heads, so a
+difference at a near-tie of one head cannot spread to the next.  The sets
+must agree except at positions whose score at the pick lies within 1e-6
+(relative) of the k-th pick's."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.sfi_oracle as O
+import sfi_workloads as W
+from tests.sfi_testlib import DeviceLayer, S_TOL, TIE_RTOL, load_sfi, max_abs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sfi():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return load_sfi()
+
+
+def run_refined(sfi, lay, prm, ref, f_d, kn_d, B, hkv, k):
+    ws = torch.zeros(sfi.select_refined_workspace_size(lay, prm, ref), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    idx = torch.full((B, hkv, k), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, hkv), -1, dtype=torch.int32, device="cuda")
+    s = torch.full((B, hkv, lay.max_len), -7.0, device="cuda")
+    sfi.sfi_select_refined(lay, prm, ref, f_d, kn_d, idx, cnt, s, ws)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws) == 0
+    return idx.cpu().numpy(), cnt.cpu().numpy(), s.cpu().numpy()
+
+
+def check_refined(idx, cnt, s_gpu, n, lo, hi, k, rho, sigma, beta):
+    """One sequence: every KV head's set against the oracle's greedy."""
+    hkv = s_gpu.shape[0]
+    counts = np.zeros(s_gpu.shape[1])
+    ke = max(0, min(k, hi - lo))
+    for g in range(hkv):
+        got = idx[g, :cnt[g]]
+        assert cnt[g] == ke, (g, cnt[g], ke)
+        if ke == 0:
+            continue
+        assert np.all(np.diff(got) > 0), "selection not strictly ascending"
+        assert got.min() >= lo and got.max() < hi, "selection outside E"
+        extra = min(hi - lo, k + 32)
+        sg = s_gpu[g].astype(np.float64)
+        sg[n:] = 0.0
+        ox, at = O.refine_head(sg, counts, lo, hi, extra, rho, sigma, beta)
+        order = np.lexsort((ox, -at))  # pick order: scores at the pick never increase
+        first = ox[order[:ke]]
+        tau = at[order[ke - 1]]
+        amb = {int(i) for i, a in zip(ox, at) if abs(a - tau) <= TIE_RTOL * abs(tau)}
+        bad = [i for i in set(got.tolist()) ^ set(first.tolist()) if i not in amb]
+        assert not bad, f"head {g}: {len(bad)} non-ambiguous positions differ, e.g. {sorted(bad)[:6]}"
+        counts[got] += 1
+
+
+# (B, H_q, H_kv, d, dtype, lens, n_sink, window, k, seed)
+SMALL = [
+    (2, 8, 2, 64, "f32", [2048, 1500], 4, 256, 128, 11),
+    (3, 16, 4, 128, "bf16", [3000, 700, 300], 4, 64, 200, 12),  # third: M > |E| > k
+    (2, 8, 4, 64, "f32", [40, 300], 4, 16, 50, 13),             # first: |E| <= k, all of E
+    (2, 8, 2, 64, "f32", [10, 600], 4, 16, 8, 14),              # first: E empty
+]
+REFINES = [(1, 0.5, 0.0), (2, 0.3, 0.7), (0, 1.0, 1.5), (4, 2.0, 0.2), (8, 0.1, 0.0)]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"B{c[0]}-hkv{c[2]}-{c[4]}-k{c[8]}")
+def test_refined_selection_parity(sfi, case):
+    B, hq, hkv, d, dt, lens, ns, win, k, seed = case
+    wl = W.small(B, hq, hkv, d, dt, lens, seed, n_sink=ns, window=win, k=k)
+    dl = DeviceLayer.build(wl)
+    lay = dl.layout(sfi, lens)
+    ws = sfi.alloc_workspace(lay)
+    qd, q64 = dl.queries(0)
+    out = torch.empty(B, hq, d, device="cuda")
+    f_d = torch.zeros(B, hkv, lay.max_len, device="cuda")
+    kn_d = torch.zeros_like(f_d)
+    sfi.sfi_slow_attn(lay, qd, dl.k, dl.v, out, f_d, kn_d, ws)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws) == 0
+    prm = sfi.params(ns, win, k, wl.lam)
+    # plain selection, for the no-refinement identity
+    idx0 = torch.full((B, hkv, k), -1, dtype=torch.int32, device="cuda")
+    cnt0 = torch.full((B, hkv), -1, dtype=torch.int32, device="cuda")
+    sfi.sfi_select(lay, prm, f_d, kn_d, idx0, cnt0, None, ws)
+    torch.cuda.synchronize()
+    idx0, cnt0 = idx0.cpu().numpy(), cnt0.cpu().numpy()
+    for rho, sigma, beta in REFINES + [(0, 1.0, 0.0)]:
+        ref = sfi.sfi_refine(rho, sigma, beta)
+        idx, cnt, s = run_refined(sfi, lay, prm, ref, f_d, kn_d, B, hkv, k)
+        if rho == 0 and beta == 0.0:
+            np.testing.assert_array_equal(cnt, cnt0)
+            for b in range(B):
+                for g in range(hkv):
+                    np.testing.assert_array_equal(idx[b, g, :cnt[b, g]], idx0[b, g, :cnt0[b, g]])
+            continue
+        for b in range(B):
+            n = lens[b]
+            st = O.slow_step(q64[b], dl.K64[b], dl.V64[b], n, ns, win, k, wl.lam)
+            assert max_abs(s[b, :, :n], st["s"]) <= S_TOL
+            assert np.all(s[b, :, n:] == -7.0), "wrote past n"
+            check_refined(idx[b], cnt[b], s[b], n, st["lo"], st["hi"], k, rho, sigma, beta)
+        # the same call again gives the same bytes
+        idx2, cnt2, _ = run_refined(sfi, lay, prm, ref, f_d, kn_d, B, hkv, k)
+        np.testing.assert_array_equal(cnt2, cnt)
+        np.testing.assert_array_equal(idx2, idx)
+
+
+def synthetic_evidence(B, hkv, n_max, lens, seed):
+    """Seeded stand-ins for f and the key norms at full context: per (b, g), 1%
+    of the positions carry a heavy logit; f is the softmax; norms ~ |N(0, I_128)|."""
+    rng = np.random.default_rng(seed)
+    f = np.zeros((B, hkv, n_max), np.float32)
+    kn = np.zeros((B, hkv, n_max), np.float32)
+    for b in range(B):
+        n = lens[b]
+        for g in range(hkv):
+            lg = 0.8 * rng.standard_normal(n)
+            lg[rng.choice(n, n // 100, replace=False)] += 4.0
+            e = np.exp(lg - lg.max())
+            f[b, g, :n] = e / e.sum()
+            kn[b, g, :n] = np.sqrt(rng.chisquare(128, n))
+    return f, kn
+
+
+def test_refined_selection_full_context(sfi):
+    """Two sequences at 131072 and 100000 positions, 8 KV heads, k = 4096,
+    window 256: rho = 1 (20476 candidates per unit) with exclusivity."""
+    B, hkv, k, ns, win, lam = 2, 8, 4096, 4, 256, 0.3
+    lens = [131072, 100000]
+    n_max = 131072
+    f, kn = synthetic_evidence(B, hkv, n_max, lens, 21)
+    lay = sfi.Layout(32, hkv, 128, torch.bfloat16, [0, 0], [n_max, n_max], lens, n_max)
+    prm = sfi.params(ns, win, k, lam)
+    rho, sigma, beta = 1, 0.5, 0.5
+    ref = sfi.sfi_refine(rho, sigma, beta)
+    idx, cnt, s = run_refined(sfi, lay, prm, ref, torch.from_numpy(f).cuda(), torch.from_numpy(kn).cuda(),
+                              B, hkv, k)
+    for b in range(B):
+        n = lens[b]
+        lo, hi = O.eligible_range(n, ns, win)
+        f64 = f[b, :, :n].astype(np.float64)
+        r = O.prior_r(kn[b, :, :n].astype(np.float64), lo, hi)
+        assert max_abs(s[b, :, :n], O.fuse(f64, r, lam)) <= S_TOL
+        check_refined(idx[b], cnt[b], s[b], n, lo, hi, k, rho, sigma, beta)
+    # Soft-NMS spreads the picks: fewer adjacent pairs than the plain Top-K
+    plain = O.top_k(s[0, 0].astype(np.float64), *O.eligible_range(lens[0], ns, win), k)
+    assert np.sum(np.diff(idx[0, 0, :k]) <= 2) < np.sum(np.diff(plain) <= 2)
