@@ -252,10 +252,19 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU leg
 
+def parse_refine(text: str):
+    """'rho,sigma,beta' -> (int, float, float), or None for an empty string."""
+    if not text:
+        return None
+    rho, sigma, beta = text.split(",")
+    return int(rho), float(sigma), float(beta)
+
+
 class Cfg2Runner:
     """Device-resident decode workload driven through sfi_decode_step."""
 
-    def __init__(self, wl: W.Workload, device: int, async_select: bool = True, make_ctx: bool = True):
+    def __init__(self, wl: W.Workload, device: int, async_select: bool = True, make_ctx: bool = True,
+                 refine=None):
         import torch
         import slow_sparse_kv_gb300 as sfi
         self.torch, self.sfi, self.wl = torch, sfi, wl
@@ -321,7 +330,8 @@ class Cfg2Runner:
         self.bnd = [(ctypes.c_uint8 * B)(*[int(x) for x in self.trace[t]]) for t in range(T)]
         self.ctx = None if not make_ctx else sfi.DecodeContext(
             B, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, dt, self.max_len, L,
-            sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget, async_select=async_select)
+            sfi.params(wl.n_sink, wl.window, wl.k, wl.lam), wl.budget, async_select=async_select,
+            refine=sfi.sfi_refine(*refine) if refine else None)
         self.slow_masks = None
         self.kp = [t.data_ptr() for t in self.K]
         self.vp = [t.data_ptr() for t in self.V]
@@ -378,7 +388,8 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         wl.seed = rank_seed(wl.seed, rank)
     t_setup = time.perf_counter()
-    R = Cfg2Runner(wl, local_rank, async_select=not args.sync_select)
+    refine = parse_refine(args.refine)
+    R = Cfg2Runner(wl, local_rank, async_select=not args.sync_select, refine=refine)
     setup_s = time.perf_counter() - t_setup
     sfi = R.sfi
     sh = wl.shape
@@ -538,6 +549,8 @@ def run_ours(args, rank, world, local_rank):
                 sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9),
             "parallelism": f"dp{world} (independent sequences per GPU)",
             "selector": "in line" if args.sync_select else "overlapped with the next layer",
+            **({"refine": {"nms_radius": refine[0], "nms_sigma": refine[1], "excl_beta": refine[2]}}
+               if refine else {}),
         },
         "tokens_per_s": round(steps_per_s * sh.batch, 1),
         "breakdown": {
@@ -827,6 +840,8 @@ def main():
                          "with the next layer's attention")
     ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast,fast_contig,mixed (or 'verify' alone): time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
+    ap.add_argument("--refine", default="", help="rho,sigma,beta: decode with the Soft-NMS / "
+                    "exclusivity selector refinement (default: plain Top-K)")
     ap.add_argument("--case-batch", type=int, default=2)
     ap.add_argument("--case-context", type=int, default=0,
                     help="context of the --kernel-case layer (default: the 131072 of the decode "

@@ -296,11 +296,16 @@ typedef struct {
    * second set of evidence buffers; the caller's stream joins it at the last
    * layer of each step.  0: the selector runs on the caller's stream. */
   int32_t async_select;
+  /* Selector refinements applied at every refresh (reading and limits as for
+   * sfi_select_refined); all zero: plain Top-K.  With excl_beta > 0 a
+   * refreshing layer runs its KV heads' selections one after another. */
+  sfi_refine refine;
 } sfi_ctx_desc;
 
 /* Create a decode context: allocates (with cudaMalloc, once) each layer's
  * selection buffers and the shared evidence/workspace buffers (two sets when
- * async_select != 0), and with async_select its stream and events. */
+ * async_select != 0; with a refinement each set adds its candidate lists and
+ * exclusivity counts), and with async_select its stream and events. */
 sfi_status sfi_ctx_create(const sfi_ctx_desc* desc, sfi_ctx** ctx_out);
 sfi_status sfi_ctx_destroy(sfi_ctx* ctx);
 

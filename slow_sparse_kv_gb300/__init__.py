@@ -47,7 +47,7 @@ class sfi_ctx_desc(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32),
                 ("head_dim", c_int32), ("dtype", c_int32), ("max_len", c_int32),
                 ("n_layers", c_int32), ("params", sfi_params), ("budget", c_int32),
-                ("async_select", c_int32)]
+                ("async_select", c_int32), ("refine", sfi_refine)]
 
 
 _L = POINTER(sfi_layout)
@@ -273,9 +273,10 @@ class DecodeContext:
 
     def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, dtype: torch.dtype,
                  max_len: int, n_layers: int, prm: sfi_params, budget: int,
-                 async_select: bool = True):
+                 async_select: bool = True, refine: Optional[sfi_refine] = None):
         desc = sfi_ctx_desc(batch, n_q_heads, n_kv_heads, head_dim, dtype_code(dtype), max_len,
-                            n_layers, prm, budget, int(bool(async_select)))
+                            n_layers, prm, budget, int(bool(async_select)),
+                            refine if refine is not None else sfi_refine(0, 0.0, 0.0))
         h = c_void_p()
         _check("sfi_ctx_create", lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)))
         self.h = h

@@ -11,6 +11,7 @@
 #include <new>
 #include <vector>
 
+#include "refine.h"
 #include "sfi_internal.h"
 
 // Overlapped selection (desc.async_select != 0): the selector of layer l runs
@@ -30,6 +31,13 @@ struct sfi_ctx {
   char* ws[2] = {nullptr, nullptr};        // attention / selector workspace
   float* knorm[2] = {nullptr, nullptr};    // [B*H_kv][max_len]
   int32_t* len_copy[2] = {nullptr, nullptr};  // [B]
+  // selector refinements (desc.refine): candidate lists, their counts and the
+  // exclusivity counts, per buffer set
+  bool refine = false;
+  long long n_cand = 0;
+  int32_t* cand[2] = {nullptr, nullptr};    // [B*H_kv][n_cand]
+  int32_t* ccount[2] = {nullptr, nullptr};  // [B*H_kv]
+  uint8_t* excl[2] = {nullptr, nullptr};    // [B][max_len]
   int32_t* idx = nullptr;      // [L][B*H_kv][k]
   int32_t* count = nullptr;    // [L][B*H_kv]
   int n_sets = 1;
@@ -63,6 +71,9 @@ void free_ctx(sfi_ctx* c) {
     cudaFree(c->ws[p]);
     cudaFree(c->knorm[p]);
     cudaFree(c->len_copy[p]);
+    cudaFree(c->cand[p]);
+    cudaFree(c->ccount[p]);
+    cudaFree(c->excl[p]);
   }
   if (c->side) cudaStreamDestroy(c->side);
   cudaFree(c->idx);
@@ -124,6 +135,8 @@ sfi_status sfi_ctx_create(const sfi_ctx_desc* d, sfi_ctx** out) {
   if (d->budget < 0) return fail(SFI_ERR_INVALID_ARG, "budget must be >= 0");
   if (d->max_len > kSelectMaxLen)
     return fail(SFI_ERR_CAPACITY, "the selector holds at most %d positions per row", kSelectMaxLen);
+  if ((s = check_refine(&L, &d->params, &d->refine)) != SFI_OK) return s;
+  const bool refine = refine_active(d->refine);
   sfi_ctx* c = new (std::nothrow) sfi_ctx();
   if (!c) return fail(SFI_ERR_CAPACITY, "out of host memory");
   c->desc = *d;
@@ -139,6 +152,13 @@ sfi_status sfi_ctx_create(const sfi_ctx_desc* d, sfi_ctx** out) {
     if (e == cudaSuccess) e = cudaMalloc(&c->len_copy[p], size_t(d->batch) * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->attn_done[p], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->sel_done[p], cudaEventDisableTiming);
+    if (refine) {
+      c->refine = true;
+      c->n_cand = refine_candidates(&L, &d->params, &d->refine);
+      if (e == cudaSuccess) e = cudaMalloc(&c->cand[p], units * size_t(c->n_cand) * sizeof(int32_t));
+      if (e == cudaSuccess) e = cudaMalloc(&c->ccount[p], units * sizeof(int32_t));
+      if (e == cudaSuccess) e = cudaMalloc(&c->excl[p], size_t(d->batch) * d->max_len);
+    }
   }
   if (e == cudaSuccess && d->async_select) {
     int lo = 0, hi = 0;  // numerically lowest value = highest priority
@@ -383,8 +403,16 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   sa.g_only = -1;
   sa.active = a.slow;
   sa.status = a.status;
-  e = launch_select(sa, ss);
-  if (e != cudaSuccess) return cuda_fail(e, "selector launch");
+  if (c->refine) {
+    // the refinement reads the fused scores back: they go to the workspace
+    sa.s = reinterpret_cast<float*>(c->ws[p] + c->plan.s_off);
+    if ((s = run_refined_select(sa, d.refine, d.params.k, c->n_cand, idx, count, c->cand[p],
+                                c->ccount[p], c->excl[p], ss)) != SFI_OK)
+      return s;
+  } else {
+    e = launch_select(sa, ss);
+    if (e != cudaSuccess) return cuda_fail(e, "selector launch");
+  }
   if (c->profiling) {
     e = record_pair(c->ev_sel, c->n_sel_pending, c->sel_ms, true, ss);
     if (e != cudaSuccess) return cuda_fail(e, "profiling event");

@@ -39,6 +39,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "refine.h"
 
 namespace sfi {
 
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
   __shared__ uint64_t red64[33];
   __shared__ uint32_t red32[33];
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t sh_digit, sh_above;
+  __shared__ uint32_t sh_digit, sh_above, sh_whole;
   __shared__ float wd[2 * kMaxNmsRadius + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool one_head = a.g_only >= 0;
@@ -268,9 +269,12 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
     return;
   }
 
-  // ---- the k-th largest key among the taken candidates, 8 bits at a time
+  // ---- the k-th largest key among the taken candidates, 8 bits at a time;
+  // the picks are the taken keys whose top bits are >= `prefix` (shifted by
+  // `cut`), and the search stops once the chosen bin is needed whole
   uint64_t prefix = 0;
   uint32_t krem = uint32_t(a.k);
+  int cut = 0;
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
     for (int i = tid; i < 256; i += kRefineCT) hist[i] = 0;
@@ -306,6 +310,7 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
           if (acc < krem && acc + cnt[q] >= krem) {
             sh_digit = uint32_t(255 - 8 * lane - q);
             sh_above = acc;
+            sh_whole = cnt[q] == krem - acc;
           }
           acc += cnt[q];
         }
@@ -314,48 +319,54 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
     __syncthreads();
     prefix = (prefix << 8) | sh_digit;
     krem -= sh_above;
+    cut = shift;
+    if (sh_whole) break;  // every key of the chosen bin is a pick
   }
-  const uint64_t kth = prefix;
 
-  // ---- the picks (keys >= the k-th) in ascending position order
-  uint32_t base = 0;
-  for (int t0 = 0; t0 < m; t0 += kRefineCT) {
-    const int i = t0 + tid;
-    bool sel = false;
-    uint32_t p = 0;
-    if (i < m) {
-      const uint32_t xi = ps[i];
-      p = xi & kPosMask;
-      sel = (xi & kTaken) && refine_key(vs[i], p) >= kth;
-    }
-    const unsigned bal = __ballot_sync(kFull, sel);
-    if (lane == 0) red32[warp] = uint32_t(__popc(bal));
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t v = red32[lane];
-      uint32_t incl = v;
+  // ---- the picks in ascending position order: thread t owns the candidates
+  // [t * per, (t + 1) * per); one block scan of the counts gives its offset
+  const int per = (m + kRefineCT - 1) / kRefineCT;
+  const int c0 = min(m, tid * per), c1 = min(m, c0 + per);
+  uint32_t mine = 0;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t xi = ps[i];
+    if ((xi & kTaken) && (refine_key(vs[i], xi & kPosMask) >> cut) >= prefix) ++mine;
+  }
+  uint32_t incl = mine;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-      }
-      red32[lane] = incl - v;
-      if (lane == 31) red32[32] = incl;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) red32[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t v = red32[lane];
+    uint32_t w_incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, w_incl, o);
+      if (lane >= o) w_incl += y;
     }
-    __syncthreads();
-    if (sel) {
-      const uint32_t at = base + red32[warp] + uint32_t(__popc(bal & ((1u << lane) - 1u)));
+    red32[lane] = w_incl - v;
+    if (lane == 31) red32[32] = w_incl;
+  }
+  __syncthreads();
+  uint32_t at = red32[warp] + incl - mine;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t xi = ps[i];
+    if ((xi & kTaken) && (refine_key(vs[i], xi & kPosMask) >> cut) >= prefix) {
       if (at < uint32_t(a.k)) {
-        out[at] = int32_t(p);
-        if (ex) excl_bump(ex, int(p));
+        out[at] = int32_t(xi & kPosMask);
+        if (ex) excl_bump(ex, int(xi & kPosMask));
       }
+      ++at;
     }
-    base += red32[32];
-    __syncthreads();
   }
   if (tid == 0) {
-    if (base != uint32_t(a.k)) set_status(a.status, SFI_DEV_REFINE);
-    a.count[u] = min(int(base), a.k);
+    const uint32_t total = red32[32];
+    if (total != uint32_t(a.k)) set_status(a.status, SFI_DEV_REFINE);
+    a.count[u] = min(int(total), a.k);
   }
 }
 
@@ -372,8 +383,6 @@ cudaError_t launch_refine(const RefineArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Candidates the selector keeps per (sequence, KV head): k without Soft-NMS,
-// else (k - 1)(4 rho + 1) + 1, at most max_len.
 long long refine_candidates(const sfi_layout* L, const sfi_params* P, const sfi_refine* R) {
   if (R->nms_radius <= 0) return P->k;
   const long long m = (long long)(P->k - 1) * (4LL * R->nms_radius + 1) + 1;
@@ -423,6 +432,60 @@ sfi_status check_refine(const sfi_layout* L, const sfi_params* P, const sfi_refi
   return SFI_OK;
 }
 
+sfi_status run_refined_select(SelectArgs sa, const sfi_refine& R, int k, long long M, int32_t* idx,
+                              int32_t* count, int32_t* cand, int32_t* ccount, uint8_t* excl,
+                              cudaStream_t st) {
+  const bool excl_on = R.excl_beta > 0.f;
+  cudaError_t e = cudaSuccess;
+  if (excl_on) {
+    e = cudaMemsetAsync(excl, 0, size_t(sa.B) * sa.max_len, st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the exclusivity counts");
+  }
+  sa.mode = SFI_SELECT_FUSED;
+  sa.idx = cand;
+  sa.count = ccount;
+  sa.k = int(M);
+  sa.excl = excl_on ? excl : nullptr;
+  sa.excl_beta = R.excl_beta;
+
+  RefineArgs ra;
+  std::memset(&ra, 0, sizeof(ra));
+  ra.cand = cand;
+  ra.cand_count = ccount;
+  ra.cstride = int(M);
+  ra.cap = R.nms_radius > 0 ? int(M) : 0;
+  ra.s = sa.s;
+  ra.excl = excl_on ? excl : nullptr;
+  ra.excl_beta = R.excl_beta;
+  ra.radius = R.nms_radius;
+  for (int d = 1; d <= 2 * R.nms_radius; ++d) {
+    const double box = 2.0 * R.nms_radius + 1.0;
+    const double iou = (box - d) / (box + d);
+    ra.wd[d] = float(iou * iou / double(R.nms_sigma));
+  }
+  ra.idx = idx;
+  ra.count = count;
+  ra.k = k;
+  ra.B = sa.B;
+  ra.H_kv = sa.H_kv;
+  ra.max_len = sa.max_len;
+  ra.active = sa.active;
+  ra.status = sa.status;
+
+  // With exclusivity the KV heads go one after another (each reads the
+  // earlier heads' picks); without it every unit runs in one pair of launches.
+  const int passes = excl_on ? sa.H_kv : 1;
+  for (int g = 0; g < passes; ++g) {
+    sa.g_only = excl_on ? g : -1;
+    ra.g_only = sa.g_only;
+    e = launch_select(sa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "selector launch");
+    e = launch_refine(ra, st);
+    if (e != cudaSuccess) return cuda_fail(e, "refinement launch");
+  }
+  return SFI_OK;
+}
+
 }  // namespace sfi
 
 using namespace sfi;
@@ -456,73 +519,22 @@ extern "C" sfi_status sfi_select_refined(const sfi_layout* L, const sfi_params* 
     return fail(SFI_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  uint32_t* status = reinterpret_cast<uint32_t*>(w + rp.base.status_off);
-  uint8_t* excl = reinterpret_cast<uint8_t*>(w + rp.excl_off);
-  int32_t* cand = reinterpret_cast<int32_t*>(w + rp.cand_off);
-  int32_t* ccount = reinterpret_cast<int32_t*>(w + rp.ccount_off);
-  float* srows = s_out ? s_out : reinterpret_cast<float*>(w + rp.base.s_off);
-  const bool excl_on = R->excl_beta > 0.f;
-  cudaError_t e = cudaSuccess;
-  if (excl_on) {
-    e = cudaMemsetAsync(excl, 0, size_t(L->batch) * L->max_len, st);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the exclusivity counts");
-  }
-
   SelectArgs sa{};
   sa.evidence = f;
   sa.knorm = knorm;
   sa.H_q = L->n_q_heads;
   sa.len = L->len;
-  sa.idx = cand;
-  sa.count = ccount;
-  sa.s = srows;
+  sa.s = s_out ? s_out : reinterpret_cast<float*>(w + rp.base.s_off);
   sa.B = L->batch;
   sa.H_kv = L->n_kv_heads;
   sa.max_len = L->max_len;
   sa.n_sink = P->n_sink;
   sa.window = P->window;
-  sa.k = int(rp.M);
   sa.lambda = P->lambda;
-  sa.mode = SFI_SELECT_FUSED;
-  sa.status = status;
-  sa.excl = excl_on ? excl : nullptr;
-  sa.excl_beta = R->excl_beta;
+  sa.status = reinterpret_cast<uint32_t*>(w + rp.base.status_off);
   for (int b = 0; b < L->batch; ++b) sa.active.bits[b >> 5] |= 1u << (b & 31);
-
-  RefineArgs ra;
-  std::memset(&ra, 0, sizeof(ra));
-  ra.cand = cand;
-  ra.cand_count = ccount;
-  ra.cstride = int(rp.M);
-  ra.cap = R->nms_radius > 0 ? int(rp.M) : 0;
-  ra.s = srows;
-  ra.excl = excl_on ? excl : nullptr;
-  ra.excl_beta = R->excl_beta;
-  ra.radius = R->nms_radius;
-  for (int d = 1; d <= 2 * R->nms_radius; ++d) {
-    const double box = 2.0 * R->nms_radius + 1.0;
-    const double iou = (box - d) / (box + d);
-    ra.wd[d] = float(iou * iou / double(R->nms_sigma));
-  }
-  ra.idx = idx_out;
-  ra.count = count_out;
-  ra.k = P->k;
-  ra.B = L->batch;
-  ra.H_kv = L->n_kv_heads;
-  ra.max_len = L->max_len;
-  ra.active = sa.active;
-  ra.status = status;
-
-  // With exclusivity the KV heads go one after another (each reads the
-  // earlier heads' picks); without it every unit runs in one pair of launches.
-  const int passes = excl_on ? L->n_kv_heads : 1;
-  for (int g = 0; g < passes; ++g) {
-    sa.g_only = excl_on ? g : -1;
-    ra.g_only = sa.g_only;
-    e = launch_select(sa, st);
-    if (e != cudaSuccess) return cuda_fail(e, "selector launch");
-    e = launch_refine(ra, st);
-    if (e != cudaSuccess) return cuda_fail(e, "refinement launch");
-  }
-  return SFI_OK;
+  return run_refined_select(sa, *R, P->k, rp.M, idx_out, count_out,
+                            reinterpret_cast<int32_t*>(w + rp.cand_off),
+                            reinterpret_cast<int32_t*>(w + rp.ccount_off),
+                            reinterpret_cast<uint8_t*>(w + rp.excl_off), st);
 }

@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "warp_hist.cuh"
 
 namespace sfi {
 
@@ -145,15 +146,6 @@ __device__ float sel_block_sum(float v, float* sh) {
   const float r = sh[32];
   __syncthreads();
   return r;
-}
-
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
-  const unsigned m = __ballot_sync(kFull, active);
-  if (active) {
-    const unsigned peers = __match_any_sync(m, bin);
-    const int leader = __ffs(peers) - 1;
-    if ((threadIdx.x & 31) == leader) atomicAdd(hist + bin, uint32_t(__popc(peers)));
-  }
 }
 
 // Exclusive block scan of one packed (gt << 16 | eq) count per thread; also

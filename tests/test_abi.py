@@ -108,6 +108,15 @@ def test_ctx_and_decode_validation(sfi):
     assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == sfi.SFI_ERR_INVALID_ARG  # 0 layers
     desc = sfi.sfi_ctx_desc(2, 8, 2, 64, sfi.SFI_F32, 100, 1, sfi.params(4, 16, 8, 0.3), -1)
     assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == sfi.SFI_ERR_INVALID_ARG  # budget < 0
+    # refinements are checked like sfi_select_refined's
+    for ref, code in [(sfi.sfi_refine(9, 0.5, 0.0), sfi.SFI_ERR_CAPACITY),
+                      (sfi.sfi_refine(1, 0.0, 0.0), sfi.SFI_ERR_INVALID_ARG),
+                      (sfi.sfi_refine(0, 1.0, -1.0), sfi.SFI_ERR_INVALID_ARG)]:
+        desc = sfi.sfi_ctx_desc(2, 8, 2, 64, sfi.SFI_F32, 100, 1, sfi.params(4, 16, 8, 0.3), 4, 0, ref)
+        assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == code
+    desc = sfi.sfi_ctx_desc(8, 32, 8, 128, sfi.SFI_BF16, 131072, 1, sfi.params(4, 256, 4096, 0.3), 32, 1,
+                            sfi.sfi_refine(2, 0.5, 0.0))
+    assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == sfi.SFI_ERR_CAPACITY  # 36856 candidates
     assert sfi.lib.sfi_decode_step(None, 0, None, None, FAKE, FAKE, FAKE, FAKE, None) == sfi.SFI_ERR_INVALID_ARG
 
 

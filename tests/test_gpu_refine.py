@@ -154,3 +154,63 @@ def test_refined_selection_full_context(sfi):
     # Soft-NMS spreads the picks: fewer adjacent pairs than the plain Top-K
     plain = O.top_k(s[0, 0].astype(np.float64), *O.eligible_range(lens[0], ns, win), k)
     assert np.sum(np.diff(idx[0, 0, :k]) <= 2) < np.sum(np.diff(plain) <= 2)
+
+
+@pytest.mark.parametrize("refine", [(2, 0.3, 0.5), (1, 0.5, 0.0)], ids=["nms2-excl", "nms1"])
+def test_decode_driver_refined(sfi, refine):
+    """The decode driver with a refinement: two layers, an all-slow step, a fast
+    step, then a mixed step (sequence 1 at a boundary).  The in-line and the
+    overlapped selector give the same bytes; every refreshed set matches the
+    oracle's refined selection, every output the oracle's attention (fast
+    steps over the sets the GPU held)."""
+    B, hq, hkv, d, ns, win, k = 2, 8, 4, 64, 4, 64, 40
+    lens = [900, 1300]
+    wl = W.small(B, hq, hkv, d, "f32", lens, 31, n_sink=ns, window=win, k=k, n_steps=4)
+    dl = DeviceLayer.build(wl)
+    prm = sfi.params(ns, win, k, wl.lam)
+    rho, sigma, beta = refine
+    bnd = [[0, 0], [0, 0], [0, 1]]
+    runs = {}
+    for async_select in (False, True):
+        ctx = sfi.DecodeContext(B, hq, hkv, d, torch.float32, max(wl.cap), 2, prm, 0,
+                                async_select=async_select, refine=sfi.sfi_refine(rho, sigma, beta))
+        lay = dl.layout(sfi, lens)
+        outs, sels, masks = [], [], []
+        for t in range(3):
+            lay.set_lens([n + t for n in lens])
+            qd, _ = dl.queries(t)
+            o_t = []
+            for layer in range(2):
+                out = torch.empty(B, hq, d, device="cuda")
+                ctx.step(layer, bnd[t], lay, qd, dl.k, dl.v, out)
+                o_t.append(out)
+            masks.append(ctx.slow_mask())
+            sel = [tuple(x.cpu().numpy() for x in ctx.selection(layer)) for layer in range(2)]
+            outs.append([o.cpu().numpy() for o in o_t])
+            sels.append(sel)
+        torch.cuda.synchronize()
+        assert ctx.read_status() == 0
+        ctx.close()
+        runs[async_select] = (outs, sels, masks)
+    (o0, s0, m0), (o1, s1, m1) = runs[False], runs[True]
+    assert m0 == m1 == [[1, 1], [0, 0], [0, 1]]
+    for t in range(3):
+        for layer in range(2):
+            np.testing.assert_array_equal(o0[t][layer], o1[t][layer])
+            for a, b in zip(s0[t][layer], s1[t][layer]):
+                np.testing.assert_array_equal(a, b)
+    held = {}
+    for t in range(3):
+        n_t = [n + t for n in lens]
+        _, q64 = dl.queries(t)
+        for b in range(B):
+            for layer in range(2):
+                idx, cnt = s0[t][layer]
+                if m0[t][b]:
+                    st = O.slow_step(q64[b], dl.K64[b], dl.V64[b], n_t[b], ns, win, k, wl.lam)
+                    assert max_abs(o0[t][layer][b], st["o"]) <= 2e-5
+                    check_refined(idx[b], cnt[b], st["s"], n_t[b], st["lo"], st["hi"], k, rho, sigma, beta)
+                    held[(b, layer)] = [idx[b, g, :cnt[b, g]].astype(np.int64) for g in range(hkv)]
+                else:
+                    ref = O.fast_step(q64[b], dl.K64[b], dl.V64[b], n_t[b], held[(b, layer)], ns, win)
+                    assert max_abs(o0[t][layer][b], ref) <= 2e-5
