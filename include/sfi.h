@@ -184,7 +184,7 @@ sfi_status sfi_select(const sfi_layout* layout, const sfi_params* params,
  * sfi_select_refined computes s exactly as sfi_select in SFI_SELECT_FUSED mode
  * (the only mode it takes) and writes each (b, g)'s selection to idx_out in
  * ascending order, count_out = min(k, |E|).  Limits: nms_radius <= 8; with
- * nms_radius > 0, (k - 1)(4 nms_radius + 1) + 1 <= 24576 (else
+ * nms_radius > 0, min(max_len, (k - 1)(4 nms_radius + 1) + 1) <= 98304 (else
  * SFI_ERR_CAPACITY).  With excl_beta > 0 the KV heads run one after another
  * (two launches each).  The workspace (sfi_select_refined_workspace_size,
  * 0 for invalid arguments) follows the shared rules; the call clears the part

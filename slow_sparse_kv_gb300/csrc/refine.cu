@@ -26,13 +26,16 @@
 // earlier picks (each lowers at most 4 rho positions), so the first k picks
 // lie in the top M = (k - 1)(4 rho + 1) + 1 of E by starting score.  The
 // cluster selector (with the exclusivity penalty) writes that top M in
-// ascending position order; one 1024-thread CTA per (sequence, KV head)
-// holds it in shared memory, 8 bytes a candidate (position with two flag
-// bits, current score).  On the decode workloads (k = 4096, rho = 1:
-// M = 20476) two to four rounds settle the selection.  A radix select over
-// 64-bit (score, position) keys of the taken candidates finds the k-th pick,
-// and an ordered compaction writes the picks in ascending position order and
+// ascending position order.  A cluster of 8 CTAs per (sequence, KV head)
+// holds it in shared memory, each CTA a contiguous slice at 8 bytes a
+// candidate (position with two flag bits, current score); the few
+// neighbours beyond a slice's ends are read from the next CTA's shared
+// memory.  On the decode workloads (k = 4096, rho = 1: M = 20476) two to
+// four rounds settle the selection.  A radix select over 64-bit (score,
+// position) keys of the taken candidates finds the k-th pick, and an
+// ordered compaction writes the picks in ascending position order and
 // counts them for the next KV head.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include <cmath>
@@ -43,15 +46,15 @@
 
 namespace sfi {
 
-constexpr int kRefineCT = 1024;
-constexpr int kRefinePer = kRefineCap / kRefineCT;  // candidates per thread (interleaved)
-static_assert(kRefineCap % kRefineCT == 0, "candidates split evenly over the threads");
+static_assert(kRefineSlice % kRefineCT == 0, "candidates split evenly over the threads");
 static_assert(kRefinePer <= 32, "per-thread winner masks are 32-bit");
 static_assert(kRefineCap <= 0x3fffffff, "positions keep two flag bits");
+static_assert(kRefineCT % 32 == 0 && kRefineCT / 32 <= 32, "block reductions");
 
 constexpr uint32_t kTaken = 0x80000000u;  // taken (in an earlier or this round)
 constexpr uint32_t kNew = 0x40000000u;    // taken in the current round
 constexpr uint32_t kPosMask = 0x3fffffffu;
+constexpr int kRefineWarps = kRefineCT / 32;
 
 // (score, position) key: larger score first, then the lower position.
 // Never 0 (the low word is 2^32 - 1 - position > 0).
@@ -69,7 +72,7 @@ __device__ __forceinline__ uint64_t refine_block_max(uint64_t x, uint64_t* sh) {
   if (lane == 0) sh[w] = x;
   __syncthreads();
   if (w == 0) {
-    x = sh[lane];
+    x = lane < kRefineWarps ? sh[lane] : 0ull;
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       const uint64_t y = __shfl_xor_sync(kFull, x, o);
@@ -90,7 +93,7 @@ __device__ __forceinline__ uint32_t refine_block_sum(uint32_t x, uint32_t* sh) {
   if (lane == 0) sh[w] = x;
   __syncthreads();
   if (w == 0) {
-    x = sh[lane];
+    x = lane < kRefineWarps ? sh[lane] : 0u;
 #pragma unroll
     for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
     if (lane == 0) sh[32] = x;
@@ -106,26 +109,44 @@ __device__ __forceinline__ void excl_bump(uint8_t* ex, int p) {
   ex[p] = c < 255 ? uint8_t(c + 1) : c;
 }
 
-__global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_constant__ RefineArgs a) {
-  static_assert(kRefineCT == 1024, "block reductions assume 32 warps");
+// One cluster of kRefineCluster CTAs per (sequence, KV head).  CTA `rank`
+// holds candidates [rank * slice, (rank + 1) * slice) (ascending positions)
+// in shared memory; the 2 rho neighbours of its first and last candidates
+// are read from the neighbouring CTAs' shared memory.  Per-round cluster
+// values (best remaining key, picks, picks above it) are published by each
+// CTA in its own shared memory and read by all after a cluster barrier;
+// histogram bins are added into rank 0.  Both come in two sets used by
+// alternate rounds or passes, so a set is written while the other may still
+// be read.
+__global__ void __cluster_dims__(kRefineCluster, 1, 1) __launch_bounds__(kRefineCT, 1)
+    refine_kernel(const __grid_constant__ RefineArgs a) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char rsm[];
   __shared__ uint64_t red64[33];
   __shared__ uint32_t red32[33];
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t sh_digit, sh_above, sh_whole;
+  __shared__ unsigned long long my_best[2];  // this CTA's per-round values,
+  __shared__ uint32_t my_new[2], my_above[2];  // read by every CTA of the cluster
+  __shared__ uint32_t c_hist[2][256];          // rank 0: cluster histogram
+  __shared__ uint32_t sh_digit, sh_above, sh_whole;  // rank 0: radix decision
+  __shared__ uint32_t cta_picks;                      // this CTA's picks
   __shared__ float wd[2 * kMaxNmsRadius + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = int(cl.block_rank());
   const bool one_head = a.g_only >= 0;
   const int ups = one_head ? 1 : a.H_kv;
-  const int b = active_seq(a.active, int(blockIdx.x) / ups);
-  if (b < 0 || b >= a.B) return;  // cannot happen for a valid grid
-  const int u = b * a.H_kv + (one_head ? a.g_only : int(blockIdx.x) % ups);
+  const int c = int(blockIdx.x) / kRefineCluster;
+  const int b = active_seq(a.active, c / ups);
+  if (b < 0 || b >= a.B) return;  // uniform over the cluster (cannot happen for a valid grid)
+  const int u = b * a.H_kv + (one_head ? a.g_only : c % ups);
   const int m = a.cand_count[u];
   int32_t* out = a.idx + size_t(u) * a.k;
   const int32_t* cp = a.cand + size_t(u) * a.cstride;
   uint8_t* ex = a.excl ? a.excl + size_t(b) * a.max_len : nullptr;
+  const bool lead = rank == 0 && tid == 0;
   if (m < 0 || m > a.cstride) {
-    if (tid == 0) {
+    if (lead) {
       set_status(a.status, SFI_DEV_REFINE);
       a.count[u] = 0;
     }
@@ -133,7 +154,7 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
   }
   if (m <= a.k) {
     // no more candidates than picks (|E| <= k, or no suppression): all of them
-    for (int i = tid; i < m; i += kRefineCT) {
+    for (int i = rank * kRefineCT + tid; i < m; i += kRefineCluster * kRefineCT) {
       int p = cp[i];
       if (p < 0 || p >= a.max_len) {
         set_status(a.status, SFI_DEV_REFINE);
@@ -142,130 +163,167 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
       out[i] = p;
       if (ex) excl_bump(ex, p);
     }
-    if (tid == 0) a.count[u] = m;
+    if (lead) a.count[u] = m;
     return;
   }
-  if (m > a.cap) {
-    if (tid == 0) {
+  const int slice = (m + kRefineCluster - 1) / kRefineCluster;
+  if (slice > a.slice_cap) {
+    if (lead) {
       set_status(a.status, SFI_DEV_REFINE);
       a.count[u] = 0;
     }
     return;
   }
   uint32_t* ps = reinterpret_cast<uint32_t*>(rsm);
-  float* vs = reinterpret_cast<float*>(rsm + size_t(a.cap) * 4);
+  float* vs = reinterpret_cast<float*>(rsm + size_t(a.slice_cap) * 4);
+  const int base = rank * slice;                   // first candidate of this CTA
+  const int mine = max(0, min(slice, m - base));  // candidates of this CTA
   const int reach = 2 * a.radius;
   if (tid <= reach) wd[tid] = a.wd[tid];
+  if (rank == 0)
+    for (int i = tid; i < 2 * 256; i += kRefineCT) (&c_hist[0][0])[i] = 0u;
+  // candidate j of the unit, wherever it lives in the cluster
+  auto at_ps = [&](int j) -> uint32_t {
+    const int l = j - base;
+    if (l >= 0 && l < slice) return ps[l];
+    const int r = j / slice;
+    return *cl.map_shared_rank(ps + (j - r * slice), r);
+  };
+  auto at_vs = [&](int j) -> float {
+    const int l = j - base;
+    if (l >= 0 && l < slice) return vs[l];
+    const int r = j / slice;
+    return *cl.map_shared_rank(vs + (j - r * slice), r);
+  };
 
-  // ---- candidates and their starting scores s_i * exp(-beta c_i)
+  // ---- this CTA's candidates and their starting scores s_i * exp(-beta c_i)
   const float* srow = a.s + size_t(u) * a.max_len;
 #pragma unroll 4
   for (int j = 0; j < kRefinePer; ++j) {
-    const int i = tid + j * kRefineCT;
-    if (i < m) {
-      int p = cp[i];
+    const int li = tid + j * kRefineCT;
+    if (li < mine) {
+      int p = cp[base + li];
       if (p < 0 || p >= a.max_len) {
         set_status(a.status, SFI_DEV_REFINE);
         p = 0;
       }
       float v = srow[p];
       if (ex) v *= excl_factor(ex[p], a.excl_beta);
-      ps[i] = uint32_t(p);
-      vs[i] = v;
+      ps[li] = uint32_t(p);
+      vs[li] = v;
     }
   }
-  __syncthreads();
+  cl.sync();  // every slice and the cleared totals are visible
 
   // ---- rounds: take every local winner, then apply the decays
   uint32_t prev = 0;  // this thread's winners of the previous round (bit j)
   uint32_t taken = 0;
   bool settled = false;
   for (int round = 0; round < m; ++round) {
+    const int par = round & 1;
     uint32_t win = 0;
     for (int j = 0; j < kRefinePer; ++j) {
-      const int i = tid + j * kRefineCT;
-      if (i >= m) break;
-      const uint32_t xi = ps[i];
+      const int li = tid + j * kRefineCT;
+      if (li >= mine) break;
+      const uint32_t xi = ps[li];
       if (xi & kTaken) continue;
+      const int gi = base + li;
       const int pi = int(xi & kPosMask);
-      const uint64_t ki = refine_key(vs[i], uint32_t(pi));
+      const uint64_t ki = refine_key(vs[li], uint32_t(pi));
       bool ok = true;
-      for (int t = 1; t <= reach && ok && i - t >= 0; ++t) {
-        const uint32_t y = ps[i - t];
+      for (int t = 1; t <= reach && ok && gi - t >= 0; ++t) {
+        const uint32_t y = at_ps(gi - t);
         if (pi - int(y & kPosMask) > reach) break;
-        if (!(y & kTaken) && refine_key(vs[i - t], y & kPosMask) > ki) ok = false;
+        if (!(y & kTaken) && refine_key(at_vs(gi - t), y & kPosMask) > ki) ok = false;
       }
-      for (int t = 1; t <= reach && ok && i + t < m; ++t) {
-        const uint32_t y = ps[i + t];
+      for (int t = 1; t <= reach && ok && gi + t < m; ++t) {
+        const uint32_t y = at_ps(gi + t);
         if (int(y & kPosMask) - pi > reach) break;
-        if (!(y & kTaken) && refine_key(vs[i + t], y & kPosMask) > ki) ok = false;
+        if (!(y & kTaken) && refine_key(at_vs(gi + t), y & kPosMask) > ki) ok = false;
       }
       if (ok) win |= 1u << j;
     }
-    __syncthreads();
+    cl.sync();  // every CTA has judged its candidates on the same state
     for (int j = 0; j < kRefinePer; ++j) {
-      const int i = tid + j * kRefineCT;
+      const int li = tid + j * kRefineCT;
       if ((win >> j) & 1u) {
-        ps[i] |= kTaken | kNew;
+        ps[li] |= kTaken | kNew;
       } else if ((prev >> j) & 1u) {
-        ps[i] &= ~kNew;
+        ps[li] &= ~kNew;
       }
     }
-    __syncthreads();
+    cl.sync();  // this round's picks are marked everywhere
     uint64_t best = 0;  // best remaining key after this round's decays
     for (int j = 0; j < kRefinePer; ++j) {
-      const int i = tid + j * kRefineCT;
-      if (i >= m) break;
-      const uint32_t xi = ps[i];
+      const int li = tid + j * kRefineCT;
+      if (li >= mine) break;
+      const uint32_t xi = ps[li];
       if (xi & kTaken) continue;
+      const int gi = base + li;
       const int pi = int(xi & kPosMask);
       float e = 0.f;
-      for (int t = 1; t <= reach && i - t >= 0; ++t) {
-        const uint32_t y = ps[i - t];
+      for (int t = 1; t <= reach && gi - t >= 0; ++t) {
+        const uint32_t y = at_ps(gi - t);
         const int d = pi - int(y & kPosMask);
         if (d > reach) break;
         if ((y & kNew) && d > 0) e += wd[d];
       }
-      for (int t = 1; t <= reach && i + t < m; ++t) {
-        const uint32_t y = ps[i + t];
+      for (int t = 1; t <= reach && gi + t < m; ++t) {
+        const uint32_t y = at_ps(gi + t);
         const int d = int(y & kPosMask) - pi;
         if (d > reach) break;
         if ((y & kNew) && d > 0) e += wd[d];
       }
-      float v = vs[i];
+      float v = vs[li];
       if (e > 0.f) {
         v *= expf(-e);
-        vs[i] = v;
+        vs[li] = v;
       }
       const uint64_t key = refine_key(v, uint32_t(pi));
       best = key > best ? key : best;
     }
-    const uint64_t best_all = refine_block_max(best, red64);
-    taken += refine_block_sum(uint32_t(__popc(win)), red32);
+    // cluster totals: each CTA publishes its values in its own shared memory
+    // (slot `par`; the other slot is still being read for the previous
+    // round) and every CTA reads all of them after the barrier
+    const uint64_t best_cta = refine_block_max(best, red64);
+    const uint32_t new_cta = refine_block_sum(uint32_t(__popc(win)), red32);
+    if (tid == 0) {
+      my_best[par] = best_cta;
+      my_new[par] = new_cta;
+    }
+    cl.sync();
+    uint64_t best_all = 0;
+    for (int r = 0; r < kRefineCluster; ++r) {
+      const uint64_t x = *cl.map_shared_rank(&my_best[par], r);
+      best_all = x > best_all ? x : best_all;
+      taken += *cl.map_shared_rank(&my_new[par], r);
+    }
     prev = win;
     if (best_all == 0) {  // every candidate is taken (m > k of them)
       settled = true;
-      break;
-    }
-    if (taken >= uint32_t(a.k)) {
+    } else if (taken >= uint32_t(a.k)) {
       uint32_t above = 0;
       for (int j = 0; j < kRefinePer; ++j) {
-        const int i = tid + j * kRefineCT;
-        if (i >= m) break;
-        const uint32_t xi = ps[i];
-        if ((xi & kTaken) && refine_key(vs[i], xi & kPosMask) > best_all) ++above;
+        const int li = tid + j * kRefineCT;
+        if (li >= mine) break;
+        const uint32_t xi = ps[li];
+        if ((xi & kTaken) && refine_key(vs[li], xi & kPosMask) > best_all) ++above;
       }
-      if (refine_block_sum(above, red32) >= uint32_t(a.k)) {
-        settled = true;
-        break;
-      }
+      above = refine_block_sum(above, red32);
+      if (tid == 0) my_above[par] = above;
+      cl.sync();
+      uint32_t above_all = 0;
+      for (int r = 0; r < kRefineCluster; ++r) above_all += *cl.map_shared_rank(&my_above[par], r);
+      if (above_all >= uint32_t(a.k)) settled = true;
     }
+    if (settled) break;
   }
   if (!settled) {  // cannot happen: every round takes the best remaining candidate
-    if (tid == 0) {
+    if (lead) {
       set_status(a.status, SFI_DEV_REFINE);
       a.count[u] = 0;
     }
+    cl.sync();  // no CTA leaves while another may read its shared memory
     return;
   }
 
@@ -277,62 +335,72 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
   int cut = 0;
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
+    const int par = pass & 1;
     for (int i = tid; i < 256; i += kRefineCT) hist[i] = 0;
     __syncthreads();
     for (int j = 0; j < kRefinePer; ++j) {
-      const int i = tid + j * kRefineCT;
-      if (i >= m) break;
-      const uint32_t xi = ps[i];
+      const int li = tid + j * kRefineCT;
+      if (li >= mine) break;
+      const uint32_t xi = ps[li];
       if (!(xi & kTaken)) continue;
-      const uint64_t key = refine_key(vs[i], xi & kPosMask);
+      const uint64_t key = refine_key(vs[li], xi & kPosMask);
       if (pass == 0 || (key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (warp == 0) {
-      // lane l holds bins 255 - 8 l down to 248 - 8 l
-      uint32_t cnt[8], tot = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        cnt[q] = hist[255 - 8 * lane - q];
-        tot += cnt[q];
-      }
-      uint32_t incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t above = incl - tot;
-      if (above < krem && krem <= incl) {
-        uint32_t acc = above;
+    for (int i = tid; i < 256; i += kRefineCT)
+      if (hist[i]) atomicAdd(cl.map_shared_rank(&c_hist[par][i], 0), hist[i]);
+    cl.sync();  // the cluster histogram of this pass is complete in rank 0
+    if (rank == 0) {
+      if (warp == 0) {
+        // lane l holds bins 255 - 8 l down to 248 - 8 l
+        uint32_t cnt[8], tot = 0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          if (acc < krem && acc + cnt[q] >= krem) {
-            sh_digit = uint32_t(255 - 8 * lane - q);
-            sh_above = acc;
-            sh_whole = cnt[q] == krem - acc;
+          cnt[q] = c_hist[par][255 - 8 * lane - q];
+          tot += cnt[q];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t above = incl - tot;
+        if (above < krem && krem <= incl) {
+          uint32_t acc = above;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (acc < krem && acc + cnt[q] >= krem) {
+              sh_digit = uint32_t(255 - 8 * lane - q);
+              sh_above = acc;
+              sh_whole = cnt[q] == krem - acc;
+            }
+            acc += cnt[q];
           }
-          acc += cnt[q];
         }
       }
+      // the other set was read in the previous pass: clear it for the next
+      for (int i = tid; i < 256; i += kRefineCT) c_hist[par ^ 1][i] = 0u;
     }
-    __syncthreads();
-    prefix = (prefix << 8) | sh_digit;
-    krem -= sh_above;
+    cl.sync();  // rank 0's decision is visible
+    const uint32_t digit = *cl.map_shared_rank(&sh_digit, 0);
+    const uint32_t whole = *cl.map_shared_rank(&sh_whole, 0);
+    krem -= *cl.map_shared_rank(&sh_above, 0);
+    prefix = (prefix << 8) | digit;
     cut = shift;
-    if (sh_whole) break;  // every key of the chosen bin is a pick
+    if (whole) break;  // every key of the chosen bin is a pick
   }
 
-  // ---- the picks in ascending position order: thread t owns the candidates
-  // [t * per, (t + 1) * per); one block scan of the counts gives its offset
-  const int per = (m + kRefineCT - 1) / kRefineCT;
-  const int c0 = min(m, tid * per), c1 = min(m, c0 + per);
-  uint32_t mine = 0;
+  // ---- the picks in ascending position order: thread t owns this CTA's
+  // candidates [t * per, (t + 1) * per); block and cluster offsets follow
+  const int per = (mine + kRefineCT - 1) / kRefineCT;
+  const int c0 = min(mine, tid * per), c1 = min(mine, c0 + per);
+  uint32_t own = 0;
   for (int i = c0; i < c1; ++i) {
     const uint32_t xi = ps[i];
-    if ((xi & kTaken) && (refine_key(vs[i], xi & kPosMask) >> cut) >= prefix) ++mine;
+    if ((xi & kTaken) && (refine_key(vs[i], xi & kPosMask) >> cut) >= prefix) ++own;
   }
-  uint32_t incl = mine;
+  uint32_t incl = own;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t y = __shfl_up_sync(kFull, incl, o);
@@ -341,18 +409,24 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
   if (lane == 31) red32[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const uint32_t v = red32[lane];
+    const uint32_t v = lane < kRefineWarps ? red32[lane] : 0u;
     uint32_t w_incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(kFull, w_incl, o);
       if (lane >= o) w_incl += y;
     }
-    red32[lane] = w_incl - v;
-    if (lane == 31) red32[32] = w_incl;
+    if (lane < kRefineWarps) red32[lane] = w_incl - v;
+    if (lane == 31) cta_picks = w_incl;
   }
-  __syncthreads();
-  uint32_t at = red32[warp] + incl - mine;
+  cl.sync();  // every CTA's pick count is visible
+  uint32_t before = 0, total = 0;
+  for (int r = 0; r < kRefineCluster; ++r) {
+    const uint32_t n = *cl.map_shared_rank(&cta_picks, r);
+    if (r < rank) before += n;
+    total += n;
+  }
+  uint32_t at = before + red32[warp] + incl - own;
   for (int i = c0; i < c1; ++i) {
     const uint32_t xi = ps[i];
     if ((xi & kTaken) && (refine_key(vs[i], xi & kPosMask) >> cut) >= prefix) {
@@ -363,15 +437,15 @@ __global__ void __launch_bounds__(kRefineCT, 1) refine_kernel(const __grid_const
       ++at;
     }
   }
-  if (tid == 0) {
-    const uint32_t total = red32[32];
+  if (lead) {
     if (total != uint32_t(a.k)) set_status(a.status, SFI_DEV_REFINE);
     a.count[u] = min(int(total), a.k);
   }
+  cl.sync();  // no CTA leaves while another may read its shared memory
 }
 
 cudaError_t launch_refine(const RefineArgs& a, cudaStream_t st) {
-  const size_t smem = size_t(a.cap) * 8;
+  const size_t smem = size_t(a.slice_cap) * 8;
   cudaError_t e = cudaFuncSetAttribute(refine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(smem));
   if (e != cudaSuccess) return e;
@@ -379,7 +453,7 @@ cudaError_t launch_refine(const RefineArgs& a, cudaStream_t st) {
   for (int b = 0; b < a.B; ++b) n_active += int((a.active.bits[b >> 5] >> (b & 31)) & 1u);
   const int units = n_active * (a.g_only >= 0 ? 1 : a.H_kv);
   if (units == 0) return cudaSuccess;
-  refine_kernel<<<units, kRefineCT, smem, st>>>(a);
+  refine_kernel<<<units * kRefineCluster, kRefineCT, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -453,7 +527,7 @@ sfi_status run_refined_select(SelectArgs sa, const sfi_refine& R, int k, long lo
   ra.cand = cand;
   ra.cand_count = ccount;
   ra.cstride = int(M);
-  ra.cap = R.nms_radius > 0 ? int(M) : 0;
+  ra.slice_cap = R.nms_radius > 0 ? int((M + kRefineCluster - 1) / kRefineCluster) : 0;
   ra.s = sa.s;
   ra.excl = excl_on ? excl : nullptr;
   ra.excl_beta = R.excl_beta;

@@ -6,6 +6,36 @@
 
 namespace sfi {
 
+// Soft-NMS / exclusivity refinement of a candidate selection: one cluster of
+// kRefineCluster CTAs per (sequence, KV head), each holding a contiguous
+// slice of the candidates in shared memory.
+constexpr int kMaxNmsRadius = 8;   // largest rho (boxes reach 2 rho positions)
+constexpr int kRefineCluster = 8;  // CTAs per unit
+constexpr int kRefineCT = 512;     // threads per CTA
+constexpr int kRefinePer = 24;     // candidates per thread
+constexpr int kRefineSlice = kRefineCT * kRefinePer;        // candidates per CTA
+constexpr int kRefineCap = kRefineCluster * kRefineSlice;   // candidates per unit (98304)
+
+struct RefineArgs {
+  const int32_t* cand;        // [B*H_kv][cstride] candidate positions, ascending
+  const int32_t* cand_count;  // [B*H_kv]
+  int32_t cstride;
+  int32_t slice_cap;          // candidates one CTA's shared memory holds in this launch
+  const float* s;             // [B*H_kv][max_len] fused scores
+  uint8_t* excl;              // [B][max_len] picks of earlier KV heads (or null)
+  float excl_beta;
+  int32_t radius;             // rho (0: no suppression)
+  float wd[2 * kMaxNmsRadius + 1];  // decay exponent IoU(d)^2 / sigma at distance d
+  int32_t* idx;               // [B*H_kv][k]
+  int32_t* count;             // [B*H_kv]
+  int32_t k;
+  int32_t B, H_kv, max_len;
+  int32_t g_only;             // >= 0: only the units of this KV head
+  SeqMask active;
+  uint32_t* status;
+};
+cudaError_t launch_refine(const RefineArgs& a, cudaStream_t st);
+
 // Candidates the selector keeps per (sequence, KV head): k without Soft-NMS,
 // else (k - 1)(4 rho + 1) + 1, at most max_len.
 long long refine_candidates(const sfi_layout* L, const sfi_params* P, const sfi_refine* R);

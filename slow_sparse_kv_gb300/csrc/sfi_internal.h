@@ -92,28 +92,6 @@ struct SelectArgs {
   int32_t g_only;  // >= 0: only the units of this KV head (fused mode)
 };
 
-// Soft-NMS / exclusivity refinement of a candidate selection (refine.cu).
-constexpr int kMaxNmsRadius = 8;     // largest rho (boxes reach 2 rho positions)
-constexpr int kRefineCap = 24576;    // candidates per unit held in shared memory
-struct RefineArgs {
-  const int32_t* cand;        // [B*H_kv][cstride] candidate positions, ascending
-  const int32_t* cand_count;  // [B*H_kv]
-  int32_t cstride;
-  int32_t cap;                // candidates the launch's shared memory holds
-  const float* s;             // [B*H_kv][max_len] fused scores
-  uint8_t* excl;              // [B][max_len] picks of earlier KV heads (or null)
-  float excl_beta;
-  int32_t radius;             // rho (0: no suppression)
-  float wd[2 * kMaxNmsRadius + 1];  // decay exponent IoU(d)^2 / sigma at distance d
-  int32_t* idx;               // [B*H_kv][k]
-  int32_t* count;             // [B*H_kv]
-  int32_t k;
-  int32_t B, H_kv, max_len;
-  int32_t g_only;             // >= 0: only the units of this KV head
-  SeqMask active;
-  uint32_t* status;
-};
-cudaError_t launch_refine(const RefineArgs& a, cudaStream_t st);
 
 // Verification attention (Vegas): R chain rows per head, collected logit sums.
 struct VerifyArgs {

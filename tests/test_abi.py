@@ -115,8 +115,8 @@ def test_ctx_and_decode_validation(sfi):
         desc = sfi.sfi_ctx_desc(2, 8, 2, 64, sfi.SFI_F32, 100, 1, sfi.params(4, 16, 8, 0.3), 4, 0, ref)
         assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == code
     desc = sfi.sfi_ctx_desc(8, 32, 8, 128, sfi.SFI_BF16, 131072, 1, sfi.params(4, 256, 4096, 0.3), 32, 1,
-                            sfi.sfi_refine(2, 0.5, 0.0))
-    assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == sfi.SFI_ERR_CAPACITY  # 36856 candidates
+                            sfi.sfi_refine(8, 0.5, 0.0))
+    assert sfi.lib.sfi_ctx_create(ctypes.byref(desc), ctypes.byref(h)) == sfi.SFI_ERR_CAPACITY  # 131072 candidates
     assert sfi.lib.sfi_decode_step(None, 0, None, None, FAKE, FAKE, FAKE, FAKE, None) == sfi.SFI_ERR_INVALID_ARG
 
 
@@ -178,9 +178,9 @@ def test_refine_validation_codes(sfi):
         assert ref(P, R(1, sig, 0.0)) == sfi.SFI_ERR_INVALID_ARG
     for beta in (-0.5, float("nan"), float("inf")):
         assert ref(P, R(0, 1.0, beta)) == sfi.SFI_ERR_INVALID_ARG
-    # (k - 1)(4 rho + 1) + 1 candidates must fit one CTA's shared memory
-    assert ref(sfi.params(4, 256, 4096, 0.3), R(2, 0.5, 0.0), lay=Lbig) == sfi.SFI_ERR_CAPACITY
-    assert ref(sfi.params(4, 256, 4096, 0.3), R(1, 0.5, 0.0), lay=Lbig, ws=None) == sfi.SFI_ERR_WORKSPACE
+    # min(max_len, (k - 1)(4 rho + 1) + 1) candidates must fit the cluster's shared memory (98304)
+    assert ref(sfi.params(4, 256, 4096, 0.3), R(8, 0.5, 0.0), lay=Lbig) == sfi.SFI_ERR_CAPACITY
+    assert ref(sfi.params(4, 256, 4096, 0.3), R(2, 0.5, 0.0), lay=Lbig, ws=None) == sfi.SFI_ERR_WORKSPACE
     assert ref(P, R(1, 0.5, 0.2), f=None) == sfi.SFI_ERR_INVALID_ARG
     assert ref(P, R(1, 0.5, 0.2), ws_bytes=16) == sfi.SFI_ERR_WORKSPACE
 

@@ -68,6 +68,7 @@ SMALL = [
     (3, 16, 4, 128, "bf16", [3000, 700, 300], 4, 64, 200, 12),  # third: M > |E| > k
     (2, 8, 4, 64, "f32", [40, 300], 4, 16, 50, 13),             # first: |E| <= k, all of E
     (2, 8, 2, 64, "f32", [10, 600], 4, 16, 8, 14),              # first: E empty
+    (1, 8, 2, 64, "f32", [60], 4, 16, 8, 15),  # 40 candidates: slices of 5 < 2 rho (rho = 8)
 ]
 REFINES = [(1, 0.5, 0.0), (2, 0.3, 0.7), (0, 1.0, 1.5), (4, 2.0, 0.2), (8, 0.1, 0.0)]
 
@@ -131,16 +132,18 @@ def synthetic_evidence(B, hkv, n_max, lens, seed):
     return f, kn
 
 
-def test_refined_selection_full_context(sfi):
+@pytest.mark.parametrize("refine", [(1, 0.5, 0.5), (2, 0.3, 0.0)], ids=["rho1-excl", "rho2"])
+def test_refined_selection_full_context(sfi, refine):
     """Two sequences at 131072 and 100000 positions, 8 KV heads, k = 4096,
-    window 256: rho = 1 (20476 candidates per unit) with exclusivity."""
+    window 256: rho = 1 (20476 candidates per unit) with exclusivity, and
+    rho = 2 (36856 candidates per unit)."""
     B, hkv, k, ns, win, lam = 2, 8, 4096, 4, 256, 0.3
     lens = [131072, 100000]
     n_max = 131072
     f, kn = synthetic_evidence(B, hkv, n_max, lens, 21)
     lay = sfi.Layout(32, hkv, 128, torch.bfloat16, [0, 0], [n_max, n_max], lens, n_max)
     prm = sfi.params(ns, win, k, lam)
-    rho, sigma, beta = 1, 0.5, 0.5
+    rho, sigma, beta = refine
     ref = sfi.sfi_refine(rho, sigma, beta)
     idx, cnt, s = run_refined(sfi, lay, prm, ref, torch.from_numpy(f).cuda(), torch.from_numpy(kn).cuda(),
                               B, hkv, k)
