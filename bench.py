@@ -204,10 +204,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir: str):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(log_dir, f"clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
@@ -405,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- timed region: K decode passes, inputs resident in HBM
     ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(T)]
     tok_ms_fast, tok_ms_mixed = [], []
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(local_rank, args.clock_log_dir)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -835,6 +835,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--cpu-budget", type=float, default=1.5, help="seconds per CPU worker")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log-dir", default=os.environ.get("SFI_CLOCK_LOG_DIR", os.path.join(ROOT, "bench_logs")),
+                    help="where the nvidia-smi clock samples of the timed region are written")
     ap.add_argument("--sync-select", action="store_true",
                     help="run each layer's selector on the decode stream instead of overlapping it "
                          "with the next layer's attention")
