@@ -1,7 +1,7 @@
-// Warp-aggregated shared-memory histogram update, shared by the selector
-// and the refinement kernels.  Score distributions are very skewed (many
-// lanes hit the same bin), so the lanes of a warp that share a bin add their
-// count with one atomic from the lowest of them.
+// Warp-aggregated shared-memory histogram update of the selector kernels.
+// Score distributions are very skewed (many lanes hit the same bin), so the
+// lanes of a warp that share a bin add their count with one atomic from the
+// lowest of them.
 #pragma once
 
 #include "common.cuh"
