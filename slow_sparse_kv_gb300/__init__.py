@@ -269,7 +269,10 @@ def sfi_read_status(ws: torch.Tensor, stream=None) -> int:
 
 
 class DecodeContext:
-    """sfi_ctx wrapper: per-layer selections plus the slow/fast schedule."""
+    """sfi_ctx wrapper: per-layer selections plus the slow/fast schedule.
+
+    ``refine`` (an ``sfi_refine``) applies Soft-NMS / cross-head exclusivity
+    at every refresh; None keeps the plain Top-K."""
 
     def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, dtype: torch.dtype,
                  max_len: int, n_layers: int, prm: sfi_params, budget: int,
