@@ -190,3 +190,26 @@ def test_refine_validation_codes(sfi):
     base = sfi.lib.sfi_select_workspace_size(ctypes.byref(L), ctypes.byref(P))
     # rho = 1: (8 - 1) * 5 + 1 = 36 candidates per unit, beside the counts and the plain plan
     assert size(P, R(1, 0.5, 0.0)) > size(P, R(0, 0.5, 0.0)) > base
+
+
+def test_header_compiles_as_c99(tmp_path):
+    """include/sfi.h is a C header: plain C99 (pedantic) compiles it, types and all."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "hdr.c"
+    src.write_text('#include "sfi.h"\n'
+                   "int main(void) {\n"
+                   "  sfi_refine r = {1, 0.5f, 0.0f};\n"
+                   "  sfi_ctx_desc d = {0};\n"
+                   "  sfi_params p = {4, 256, 4096, 0.3f, SFI_SELECT_FUSED};\n"
+                   "  d.params = p;\n"
+                   "  d.refine = r;\n"
+                   "  return (int)(sizeof d == 0) + (int)sfi_select_refined_workspace_size(0, &p, &r);\n"
+                   "}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        f"-I{os.path.join(ROOT, 'include')}", "-c", str(src), "-o", str(tmp_path / "hdr.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
