@@ -44,6 +44,11 @@
  *  - Per-position outputs (f, knorm, s, logit sums) of sequence b and KV head
  *    g are rows of length max_len at (b * H_kv + g) * max_len; entries at or
  *    past n_b are left untouched.
+ *  - Capacity limits (SFI_ERR_CAPACITY beyond them): batch <= 1024;
+ *    batch * n_kv_heads <= 4096; for every call that selects (sfi_select,
+ *    sfi_select_refined, a decode context) max_len <= 327680, the positions
+ *    one selector cluster holds in shared memory.  Further per-call limits
+ *    are stated with the call.
  */
 #ifndef SFI_H_
 #define SFI_H_
@@ -117,6 +122,16 @@ sfi_status sfi_read_status(void* ws, uint32_t* status_host, sfi_stream stream);
 
 /* Number of streaming multiprocessors of the current device (host query). */
 int32_t sfi_device_sm_count(void);
+
+/* Failure detection (no counterpart on the pages): every attention and
+ * verify launch gives each consumer warp's wait for a stage of cache rows a
+ * limit in SM clocks.  A wait that runs out sets SFI_DEV_WAIT_TIMEOUT; its
+ * CTA then skips the arithmetic of the stages it still holds, takes no
+ * further work and returns (its output is not meaningful; zero-fill the
+ * workspace before reusing it).  `cycles` applies to every later launch from
+ * any thread of the process; 0 restores the default of 4e9 clocks (about 2 s).
+ * SFI_ERR_INVALID_ARG for cycles < 0. */
+sfi_status sfi_set_wait_limit(int64_t cycles);
 
 /* ---------------------------------------------------------------- slow step */
 
@@ -263,9 +278,12 @@ sfi_status sfi_verify_attn(const sfi_layout* layout, int32_t n_rows, const int32
  *  - Scratch: a fixed 16 MiB device array inside the library, kept by every
  *    GPU that loads the library until the process exits.  It holds the
  *    status word, one counter per (sequence, KV head) and the split partial
- *    results of head_dim + 2 floats per query head and work piece.
- *    Geometries whose B * H_kv units do not fit even one piece each are
- *    rejected with SFI_ERR_CAPACITY and a message giving the bytes needed.
+ *    results of head_dim + 2 floats per query head and work piece.  Each
+ *    (sequence, KV head) is cut into at most 64 work pieces, and into no more
+ *    than the array holds for all of them.  Geometries whose B * H_kv units
+ *    do not fit even one piece each, or whose n_sink + k + window rows would
+ *    need more than 64 pieces per unit, are rejected with SFI_ERR_CAPACITY
+ *    and a message giving the sizes.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before capturing a stream
  *    into a CUDA graph.

@@ -57,6 +57,7 @@ EXPORTS = {
     "sfi_last_error": (c_char_p, []),
     "sfi_read_status": (c_int32, [c_void_p, POINTER(c_uint32), c_void_p]),
     "sfi_device_sm_count": (c_int32, []),
+    "sfi_set_wait_limit": (c_int32, [ctypes.c_int64]),
     "sfi_slow_attn_workspace_size": (c_size_t, [_L]),
     "sfi_slow_attn": (c_int32, [_L, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_size_t, c_void_p]),

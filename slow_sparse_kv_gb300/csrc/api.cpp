@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -26,6 +27,7 @@ int attn_stage_rows_bf16(int D);
 
 namespace {
 thread_local std::string g_err;
+std::atomic<long long> g_wait_cycles{0};  // 0: kDefaultWaitCycles
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 }  // namespace
@@ -42,6 +44,11 @@ sfi_status fail(sfi_status s, const char* fmt, ...) {
 
 sfi_status cuda_fail(cudaError_t e, const char* what) {
   return fail(SFI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+long long wait_limit_cycles() {
+  const long long v = g_wait_cycles.load(std::memory_order_relaxed);
+  return v > 0 ? v : kDefaultWaitCycles;
 }
 
 int device_sm_count() {
@@ -332,6 +339,7 @@ void fill_attn_common(AttnArgs& a, const sfi_layout* L, const void* q, const voi
   a.counters = reinterpret_cast<int32_t*>(ws + p.counters_off);
   a.work_ctr = reinterpret_cast<uint32_t*>(a.counters + size_t(L->batch) * L->n_kv_heads);
   a.status = reinterpret_cast<uint32_t*>(ws + p.status_off);
+  a.wait_cycles = wait_limit_cycles();
   a.logits = reinterpret_cast<float*>(ws + p.logits_off);
   a.stats = reinterpret_cast<float*>(ws + p.stats_off);
   attach_tensor_maps(a, L);
@@ -365,6 +373,12 @@ extern "C" {
 const char* sfi_last_error(void) { return sfi::g_err.c_str(); }
 
 int32_t sfi_device_sm_count(void) { return device_sm_count(); }
+
+sfi_status sfi_set_wait_limit(int64_t cycles) {
+  if (cycles < 0) return fail(SFI_ERR_INVALID_ARG, "wait limit must be >= 0 (got %lld)", (long long)cycles);
+  g_wait_cycles.store(cycles, std::memory_order_relaxed);
+  return SFI_OK;
+}
 
 sfi_status sfi_read_status(void* ws, uint32_t* status_host, sfi_stream stream) {
   if (!ws || !status_host) return fail(SFI_ERR_INVALID_ARG, "workspace and status_host must be set");

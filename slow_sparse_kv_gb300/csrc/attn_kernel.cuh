@@ -131,7 +131,9 @@ __device__ __forceinline__ int ring_fetch_publish(const AttnArgs& a, int total, 
                                                   int lane, unsigned first_id) {
   int it = -1;
   bool fetched_end = false;
-  if (lane == 0) {
+  // after an abort the CTA takes no further items (the work counters are
+  // then left mid-count: the caller zero-fills the workspace again)
+  if (lane == 0 && !(seq > 0 && *abort_flag)) {
     const unsigned x = seq == 0 ? first_id : atomicAdd(a.work_ctr, 1u);
     if (x < unsigned(total)) {
       it = int(x);
@@ -152,7 +154,7 @@ __device__ __forceinline__ int ring_fetch_publish(const AttnArgs& a, int total, 
   }
   const int slot = seq % kItemRing;
   const uint32_t ph = (seq / kItemRing) & 1u;
-  if (!warp_pipe_wait(r.empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) it = -1;
+  if (!warp_ctrl_wait(r.empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) it = -1;
   if (lane == 0) {
     r.slot[slot] = it;
     mbar_arrive(r.full + 8 * slot);
@@ -166,7 +168,7 @@ __device__ __forceinline__ int ring_read(const AttnArgs& a, const ItemRing& r, u
   const int slot = seq % kItemRing;
   const uint32_t ph = (seq / kItemRing) & 1u;
   int it = -1;
-  if (warp_pipe_wait(r.full + 8 * slot, ph, abort_flag, a.status)) it = r.slot[slot];
+  if (warp_ctrl_wait(r.full + 8 * slot, ph, abort_flag, a.status)) it = r.slot[slot];
   __syncwarp();
   if (lane == 0) mbar_arrive(r.empty + 8 * slot);
   return it;
@@ -232,8 +234,11 @@ __device__ __forceinline__ int unit_at(const AttnArgs& a, const int* rank, int v
   return seq_of_rank(a, rank, v / a.H_kv) * a.H_kv + v % a.H_kv;
 }
 
+// Returns false (in every thread) when some unit needs more than
+// kItemSlotsPerUnit items: the merge of a split unit holds that many partial
+// results, so such a launch must not run.
 template <int NT>
-__device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int* scratch) {
+__device__ bool attn_build_units(const AttnArgs& a, int* units, int n_units, int* scratch) {
   // units[v] = first item of the unit at position v, units[n_units] = total items.
   const int t = threadIdx.x;
   int* rank = units + n_units + 1;
@@ -250,11 +255,13 @@ __device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int
   const int per = (n_units + NT - 1) / NT;
   const int u0 = min(t * per, n_units), u1 = min(u0 + per, n_units);
   int local = 0;
+  int over = 0;
   for (int u = u0; u < u1; ++u) {
     const int uu = unit_at(a, rank, u);
     const int rows = attn_unit_rows(a, uu, blockIdx.x == 0);
     const int rpi = seq_is_slow(a.slow, uu / a.H_kv) ? a.rpi_slow : a.rpi_fast;
     const int it = (rows + rpi - 1) / rpi;
+    over |= it > kItemSlotsPerUnit;
     units[u] = it;
     local += it;
   }
@@ -267,7 +274,7 @@ __device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int
     if (lane >= o) incl += y;
   }
   if (lane == 31) scratch[w] = incl;
-  __syncthreads();
+  over = __syncthreads_or(over);
   if (t == 0) {
     int s = 0;
     for (int i = 0; i < NT / 32; ++i) {
@@ -286,6 +293,7 @@ __device__ void attn_build_units(const AttnArgs& a, int* units, int n_units, int
   }
   if (t == 0) units[n_units] = scratch[NT / 32];
   __syncthreads();
+  return over == 0;
 }
 
 __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* units, int n_units,
@@ -398,7 +406,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
         pos[j] = p;
       }
       if (si + 1 < I.n_st) resolve_pos(c0 + I.c_step, pos_next);
-      if (!warp_pipe_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
+      if (!warp_ctrl_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
         ok = false;
         break;
       }
@@ -492,7 +500,7 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
       const uint32_t ph = (stage / C::NS) & 1u;
       // On a failed wait the warp skips the stage but keeps walking the
       // schedule, so every consumer warp reaches every named barrier.
-      const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
+      const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status, a.wait_cycles);
       const int wr0 = warp * C::RB;
       if (have && wr0 < nr) {
         const int nw = min(C::RB, nr - wr0);
@@ -600,6 +608,9 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
           }
         }
       }
+      // a stage given up on is released only once its rows have landed, so
+      // no copy into the slot is still in flight when it is refilled
+      if (!have) mbar_wait(bar_full + 8 * slot, ph);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
       ++stage;
@@ -678,7 +689,7 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
     const int nr = min(C::SR, I.rows - c0);
     const int slot = stage % C::NS;
     const uint32_t ph = (stage / C::NS) & 1u;
-    const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
+    const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status, a.wait_cycles);
     const int r0 = wslot * C::MW;
     const int nw = min(C::MW, nr - r0);  // valid rows of this warp (may be <= 0)
     if (have && nw > 0) {
@@ -778,6 +789,9 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
         mma_bf16_16816(acc[dt], v0 & m_lo, v1 & m_lo, v2 & m_hi, v3 & m_hi, pb0, pb1);
       }
     }
+    // a stage given up on is released only once its rows have landed, so
+    // no copy into the slot is still in flight when it is refilled
+    if (!have) mbar_wait(bar_full + 8 * slot, ph);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
   }
@@ -895,9 +909,9 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
   if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
   if (a.len_copy && blockIdx.x == 0)
     for (int b = tid; b < a.B; b += C::NT) a.len_copy[b] = a.len[b];
-  attn_build_units<C::NT>(a, units, n_units, misc);
+  const bool units_fit = attn_build_units<C::NT>(a, units, n_units, misc);
   const int total = units[n_units];
-  if (total > a.max_items) {
+  if (total > a.max_items || !units_fit) {
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
     // leave the work counters at zero for the next launch
     if (fetcher && atomicAdd(a.work_ctr + 1, 1u) == gridDim.x - 1) {

@@ -11,9 +11,9 @@
 namespace sfi {
 
 constexpr unsigned kFull = 0xffffffffu;
-// A pipeline wait gives up after this many SM clocks (about 2 s) and reports
-// SFI_DEV_WAIT_TIMEOUT instead of spinning forever.
-constexpr long long kWaitCycles = 4000000000LL;
+// Default limit of a pipeline wait, in SM clocks (about 2 s); a launch may
+// set a shorter one for its consumers' data waits (AttnArgs::wait_cycles).
+constexpr long long kWaitCycles = kDefaultWaitCycles;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,22 +52,28 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
-// Wait for the phase of parity `parity` to complete; false after kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of parity `parity` to complete; false after `limit`
+// SM clocks.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }
 
-// Pipeline wait of a whole warp.  Gives up when the CTA's abort flag is set
-// or after kWaitCycles (then it sets the flag and the status bit).  The
-// result is the same in every lane: true only if every lane saw the phase
-// complete, so the warp never diverges around the data it guards.
+// Data wait of a whole consumer warp (a stage's rows have landed).  Gives up
+// when the CTA's abort flag is set or after `limit` SM clocks (then it sets
+// the flag and the status bit).  The result is the same in every lane: true
+// only if every lane saw the phase complete, so the warp never diverges
+// around the data it guards.  A warp whose wait failed skips the stage's
+// arithmetic but still releases the stage and walks the rest of the
+// schedule, so the producers and the named barriers never wait for it.
 __device__ __forceinline__ bool warp_pipe_wait(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, uint32_t* status) {
+                                               volatile int* abort_flag, uint32_t* status,
+                                               long long limit) {
   bool ok = mbar_try_wait(bar, parity);
   if (!ok) {
     const long long t0 = clock64();
@@ -77,6 +83,33 @@ __device__ __forceinline__ bool warp_pipe_wait(uint32_t bar, uint32_t parity,
         break;
       }
       if (*abort_flag) break;
+      if (clock64() - t0 > limit) {
+        *abort_flag = 1;
+        set_status(status, SFI_DEV_WAIT_TIMEOUT);
+        break;
+      }
+    }
+  }
+  return __all_sync(kFull, ok);
+}
+
+// Control wait of a whole warp: a free stage slot (producers) or a published
+// work-item id.  These phases always complete, because the consumers release
+// every stage of every item they walk (even after an abort), so the wait
+// ignores the abort flag -- every warp of the CTA then walks the same items
+// and stages, and no copy is left in flight when the CTA exits.  It still
+// gives up after kWaitCycles (then it sets the abort flag and the status
+// bit).
+__device__ __forceinline__ bool warp_ctrl_wait(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, uint32_t* status) {
+  bool ok = mbar_try_wait(bar, parity);
+  if (!ok) {
+    const long long t0 = clock64();
+    while (true) {
+      if (mbar_try_wait(bar, parity)) {
+        ok = true;
+        break;
+      }
       if (clock64() - t0 > kWaitCycles) {
         *abort_flag = 1;
         set_status(status, SFI_DEV_WAIT_TIMEOUT);

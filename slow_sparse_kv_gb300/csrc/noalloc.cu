@@ -11,6 +11,7 @@
 // the process exits.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -81,6 +82,29 @@ extern "C" sfi_status sfi_fast_attn_noalloc(const sfi_layout* L, const sfi_param
                 "the fixed scratch holds %zu",
                 units, size_t(units) * item_bytes + counters_bytes + kHeaderBytes,
                 kNoAllocScratchBytes);
+  // Work items.  A unit's rows never exceed n_sink + k + window (the
+  // selected count is clamped to k and the window to the length), so sizing
+  // on that bound -- not on max_len -- keeps every unit within its share.
+  // The share is at most kItemSlotsPerUnit items: the merge of a split unit
+  // holds that many partial results.  Both limits are checked here, before
+  // the launch, so the kernel never meets a unit it cannot merge.
+  const long long bound = std::max<long long>(
+      1, (long long)P->n_sink + (long long)P->k + (long long)P->window);
+  const int sr = L->dtype == SFI_F32 ? attn_stage_rows_f32(L->head_dim)
+                                     : attn_stage_rows_bf16(L->head_dim);
+  const long long per_unit = std::min<long long>(max_items / units, kItemSlotsPerUnit);
+  long long rpi = (bound + per_unit - 1) / per_unit;
+  const long long grid = device_sm_count();
+  const long long balanced = (units * bound + grid - 1) / grid;
+  if (rpi < balanced) rpi = balanced;
+  rpi = (rpi + sr - 1) / sr * sr;
+  if (rpi > 0x7fffffffLL) rpi = 0x7fffffffLL / sr * sr;
+  const long long items_per_unit = (bound + rpi - 1) / rpi;
+  if (items_per_unit > kItemSlotsPerUnit || items_per_unit * units > max_items)
+    return fail(SFI_ERR_CAPACITY,
+                "sfi_fast_attn_noalloc: %lld work items per unit for %lld units exceed the "
+                "fixed scratch (%lld items, at most %d per unit)",
+                items_per_unit, units, max_items, kItemSlotsPerUnit);
   void* base = nullptr;
   if ((s = scratch_address(&base)) != SFI_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -110,20 +134,11 @@ extern "C" sfi_status sfi_fast_attn_noalloc(const sfi_layout* L, const sfi_param
   a.max_len = L->max_len;
   a.qscale = float(1.4426950408889634 / std::sqrt(double(L->head_dim)));
   a.status = reinterpret_cast<uint32_t*>(w);
+  a.wait_cycles = wait_limit_cycles();
   a.counters = reinterpret_cast<int32_t*>(w + kHeaderBytes);
   a.work_ctr = reinterpret_cast<uint32_t*>(a.counters + units);
   a.partials = reinterpret_cast<float*>(w + kHeaderBytes + counters_bytes);
   a.max_items = int(max_items < 0x7fffffff ? max_items : 0x7fffffff);
-  // Work items: every unit's rows in at most max_items / units pieces.
-  const long long bound = fast_unit_rows_bound(L, P);
-  const int sr = L->dtype == SFI_F32 ? attn_stage_rows_f32(L->head_dim)
-                                     : attn_stage_rows_bf16(L->head_dim);
-  const long long per_unit = max_items / units;
-  long long rpi = (bound + per_unit - 1) / per_unit;
-  const long long grid = device_sm_count();
-  const long long balanced = (units * bound + grid - 1) / grid;
-  if (rpi < balanced) rpi = balanced;
-  rpi = (rpi + sr - 1) / sr * sr;
   a.rpi_slow = a.rpi_fast = int(rpi);
   e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st, true)
                           : launch_attn_bf16(a, L->head_dim, G, st, true);

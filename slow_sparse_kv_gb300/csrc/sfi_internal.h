@@ -14,6 +14,8 @@ namespace sfi {
 constexpr int kMaxBatch = 1024;  // sequences per launch (bit mask capacity)
 constexpr int kMaxUnits = 4096;  // (sequence, KV head) pairs per launch
 constexpr int kItemSlotsPerUnit = 64;  // split-K partial slots per (sequence, KV head)
+// Default limit of a pipeline wait, in SM clocks (about 2 s at 2 GHz).
+constexpr long long kDefaultWaitCycles = 4000000000LL;
 
 // Bit b set: sequence b runs a slow (dense) step in this launch.
 struct SeqMask {
@@ -54,6 +56,9 @@ struct AttnArgs {
   uint32_t* work_ctr;  // [2]: next item, CTAs done fetching; zero between launches
   int32_t* len_copy;   // optional [B]: the kernel copies len here (for a later selector)
   uint32_t* status;
+  // limit of a consumer's wait for a stage's rows, in SM clocks; after it the
+  // CTA aborts and sets SFI_DEV_WAIT_TIMEOUT (wait_limit_cycles() by default)
+  long long wait_cycles;
 };
 
 struct FpassArgs {
@@ -118,6 +123,9 @@ cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
 int device_sm_count();
+// Pipeline-wait limit given to every attention and verify launch (SM clocks;
+// sfi_set_wait_limit changes it for the whole process).
+long long wait_limit_cycles();
 
 // Host helpers of the C-ABI layer (api.cpp), shared with the decode driver.
 sfi_status check_layout(const sfi_layout* L);

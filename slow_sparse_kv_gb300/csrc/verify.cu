@@ -111,7 +111,7 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
     const int nr = min(C::SR, I.rows - c0);
     const int slot = stage % C::NS;
     const uint32_t ph = (stage / C::NS) & 1u;
-    const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status);
+    const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status, a.wait_cycles);
     const int r0 = wslot * C::MW;
     const int nw = min(C::MW, nr - r0);
     float lsv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -230,6 +230,9 @@ __device__ __forceinline__ void verify_item(const VerifyArgs& va, const ItemInfo
           if (rr < nw && pos < n_pre) va.lsum[size_t(I.u) * a.max_len + pos] = lsv[nt][j] * va.lscale;
         }
     }
+    // a stage given up on is released only once its rows have landed, so
+    // no copy into the slot is still in flight when it is refilled
+    if (!have) mbar_wait(bar_full + 8 * slot, ph);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
   }
@@ -267,9 +270,9 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
   unsigned first_id = 0;
   const bool fetcher = warp == C::NCW && lane == 0;
   if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
-  attn_build_units<C::NT>(a, units, n_units, misc);
+  const bool units_fit = attn_build_units<C::NT>(a, units, n_units, misc);
   const int total = units[n_units];
-  if (total > a.max_items) {
+  if (total > a.max_items || !units_fit) {
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
     if (fetcher && atomicAdd(a.work_ctr + 1, 1u) == gridDim.x - 1) {
       atomicExch(a.work_ctr, 0u);

@@ -213,3 +213,10 @@ def test_header_compiles_as_c99(tmp_path):
                         f"-I{os.path.join(ROOT, 'include')}", "-c", str(src), "-o", str(tmp_path / "hdr.o")],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_wait_limit_setter(sfi):
+    assert sfi.lib.sfi_set_wait_limit(-1) == sfi.SFI_ERR_INVALID_ARG
+    assert "wait limit" in sfi.lib.sfi_last_error().decode()
+    assert sfi.lib.sfi_set_wait_limit(12345) == sfi.SFI_OK
+    assert sfi.lib.sfi_set_wait_limit(0) == sfi.SFI_OK  # back to the default
