@@ -48,6 +48,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of the same condition (mbarrier.test_wait never
+// suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
@@ -71,21 +85,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 // around the data it guards.  A warp whose wait failed skips the stage's
 // arithmetic but still releases the stage and walks the rest of the
 // schedule, so the producers and the named barriers never wait for it.
+// The first probe does not suspend, and the limit is checked before every
+// suspending try, so a wait whose phase is not complete on entry runs out
+// after `limit` clocks even when that is shorter than one suspension.
 __device__ __forceinline__ bool warp_pipe_wait(uint32_t bar, uint32_t parity,
                                                volatile int* abort_flag, uint32_t* status,
                                                long long limit) {
-  bool ok = mbar_try_wait(bar, parity);
+  bool ok = mbar_test_wait(bar, parity);
   if (!ok) {
     const long long t0 = clock64();
     while (true) {
-      if (mbar_try_wait(bar, parity)) {
-        ok = true;
-        break;
-      }
       if (*abort_flag) break;
       if (clock64() - t0 > limit) {
         *abort_flag = 1;
         set_status(status, SFI_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      if (mbar_try_wait(bar, parity)) {
+        ok = true;
         break;
       }
     }

@@ -209,11 +209,18 @@ def test_decode_loop_cfg0(sfi, async_select):
     ctx.close()
 
 
-def test_cfg1_slow_select_fast(sfi):
+@pytest.fixture(scope="module")
+def cfg1_layer():
+    """The 32K-context Llama-3-8B layer of the cfg1 workload on the device (and
+    its exact fp64 values for the oracle)."""
+    return DeviceLayer.build(W.cfg1())
+
+
+def test_cfg1_slow_select_fast(sfi, cfg1_layer):
     """Llama-3-8B layer, bf16, 32K context: slow step, selection and fast steps."""
-    wl = W.cfg1()
+    dl = cfg1_layer
+    wl = dl.wl
     sh = wl.shape
-    dl = DeviceLayer.build(wl)
     n = wl.n0[0]
     lay, ws, q64, out, f, kn = run_slow(sfi, dl, [n])
     st = O.slow_step(q64[0], dl.K64[0], dl.V64[0], n, wl.n_sink, wl.window, wl.k, wl.lam)
@@ -241,3 +248,93 @@ def test_cfg1_slow_select_fast(sfi):
         ref = O.fast_step(qf[0], dl.K64[0], dl.V64[0], n + t, sel, wl.n_sink, wl.window)
         assert max_abs(o2.cpu().numpy()[0], ref) <= O_TOL["bf16"]
     assert sfi.sfi_read_status(ws) == 0
+
+
+def test_cfg1_decode_loop_64_steps(sfi, cfg1_layer):
+    """The whole 64-step cfg1 loop through the decode driver: refreshes at
+    steps 0, 24 and 48 (fixed boundary trace), fast steps between them.  Each
+    refreshed selection must match the oracle's slow step (tie rule), each
+    slow output its dense attention, and each fast output the oracle's fast
+    step over the set the GPU held at that step."""
+    dl = cfg1_layer
+    wl = dl.wl
+    sh = wl.shape
+    trace = wl.boundary_trace()
+    slow_ref = O.schedule(trace, wl.budget)
+    assert [t for t in range(wl.n_steps) if slow_ref[t, 0]] == [0, 24, 48]
+    ctx = sfi.DecodeContext(sh.batch, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16,
+                            max(wl.cap), 1, sfi.params(wl.n_sink, wl.window, wl.k, wl.lam),
+                            wl.budget, async_select=True)
+    lay = dl.layout(sfi, wl.n0)
+    outs, q64s, sels = [], [], {}
+    for t in range(wl.n_steps):
+        lay.set_lens([n + t for n in wl.n0])
+        qd, q64 = dl.queries(t)
+        q64s.append(q64[0])
+        out = torch.empty(sh.batch, sh.n_q_heads, sh.head_dim, device="cuda")
+        ctx.step(0, trace[t], lay, qd, dl.k, dl.v, out)
+        assert ctx.slow_mask() == [int(x) for x in slow_ref[t]]
+        if slow_ref[t, 0]:
+            idx_g, cnt_g = ctx.selection(0)
+            sels[t] = (idx_g.cpu().numpy(), cnt_g.cpu().numpy())
+        outs.append(out.cpu().numpy()[0])
+    torch.cuda.synchronize()
+    assert ctx.read_status() == 0
+    ctx.close()
+    K64, V64 = dl.K64[0], dl.V64[0]
+    held = None
+    for t in range(wl.n_steps):
+        n = wl.n0[0] + t
+        if slow_ref[t, 0]:
+            st = O.slow_step(q64s[t], K64, V64, n, wl.n_sink, wl.window, wl.k, wl.lam)
+            assert max_abs(outs[t], st["o"]) <= O_TOL["bf16"], t
+            idx_g, cnt_g = sels[t]
+            for g in range(sh.n_kv_heads):
+                check_selection(idx_g[0, g, :cnt_g[0, g]], st["s"][g], st["lo"], st["hi"], wl.k)
+            held = [idx_g[0, g, :cnt_g[0, g]].astype(np.int64) for g in range(sh.n_kv_heads)]
+        else:
+            exp = O.fast_step(q64s[t], K64, V64, n, held, wl.n_sink, wl.window)
+            assert max_abs(outs[t], exp) <= O_TOL["bf16"], (t, max_abs(outs[t], exp))
+
+
+def test_select_top_bin_over_candidate_cap(sfi):
+    """More than 4096 keys of E share the k-th key's top radix digit (the top 11
+    bits of the fp32 order key), so the selector finishes the lower digits
+    with passes over every CTA's keys instead of a gathered candidate list.
+    KV head 0: 12000 distinct-or-tied scores in one narrow band; KV head 1:
+    every score equal (the set is the lowest k positions of E)."""
+    ns, win, k = 4, 256, 6000
+    n = ns + 12000 + win
+    wl = W.small(1, 8, 2, 64, "f32", [n], 21, n_sink=ns, window=win, k=k)
+    dl = DeviceLayer.build(wl)
+    lay = dl.layout(sfi, [n])
+    ws = sfi.alloc_workspace(lay)
+    rng = np.random.default_rng(21)
+    f = np.zeros((1, 2, lay.max_len), np.float32)
+    u = np.floor(rng.random(n) * 3000.0) / 3000.0  # about four keys per value: exact ties
+    f[0, 0, :n] = (1e-4 * (1.0 + 0.1 * u)).astype(np.float32)
+    f[0, 1, :n] = np.float32(1.0 / n)
+    kn = np.zeros_like(f)
+    kn[0, :, :n] = np.float32(2.0)
+    prm = sfi.params(ns, win, k, wl.lam)
+    idx = torch.full((1, 2, k), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.full((1, 2), -1, dtype=torch.int32, device="cuda")
+    s_out = torch.full((1, 2, lay.max_len), -7.0, device="cuda")
+    sfi.sfi_select(lay, prm, torch.from_numpy(f).cuda(), torch.from_numpy(kn).cuda(), idx, cnt, s_out, ws)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws) == 0
+    idx, cnt, s_gpu = idx.cpu().numpy(), cnt.cpu().numpy(), s_out.cpu().numpy()
+    lo, hi = O.eligible_range(n, ns, win)
+    f64, kn64 = f[0, :, :n].astype(np.float64), kn[0, :, :n].astype(np.float64)
+    s_ref = O.fuse(f64, O.prior_r(kn64, lo, hi), wl.lam)
+    assert max_abs(s_gpu[0, :, :n], s_ref) <= S_TOL
+    # the premise: the k-th key's top digit holds more than 4096 keys of E
+    for g in range(2):
+        keys = s_gpu[0, g, lo:hi].astype(np.float32).view(np.uint32)
+        keys = np.where(keys & 0x80000000, ~keys, keys | 0x80000000) >> 21
+        kth = np.sort(keys)[::-1][k - 1]
+        assert int(np.sum(keys == kth)) > 4096
+        sel = idx[0, g, :cnt[0, g]]
+        check_selection(sel, s_ref[g], lo, hi, k)
+        assert np.array_equal(sel, O.top_k(s_gpu[0, g].astype(np.float64), lo, hi, k))
+    assert np.array_equal(idx[0, 1, :k], np.arange(lo, lo + k))

@@ -217,3 +217,85 @@ def test_decode_driver_refined(sfi, refine):
                 else:
                     ref = O.fast_step(q64[b], dl.K64[b], dl.V64[b], n_t[b], held[(b, layer)], ns, win)
                     assert max_abs(o0[t][layer][b], ref) <= 2e-5
+
+
+# Relative near-tie band of the chained comparison.  The GPU's fused scores
+# carry the fp32 error of logits accumulated over head_dim products (about
+# 1e-6 relative near the selection boundary, checked below against a quarter
+# of the band) and fp32 decay factors (about 1e-7).
+CHAIN_EPS = 1e-5
+
+
+def chain_allowance(sh_or, c_or, c_gpu, lo, hi, k, rho, sigma, eps):
+    """Positions where the oracle's chain and the GPU's may legitimately differ
+    for one KV head: (1) picks whose score at the pick lies within eps of the
+    k-th pick's (the set boundary); (2) interacting neighbours (|i - j| <= 2 rho)
+    whose starting scores are within eps of each other (the greedy may take
+    either first); (3) positions whose exclusivity count differs between the
+    two chains (earlier heads differed there).  Each with its 2 rho neighbours."""
+    ext = min(hi - lo, k + 64)
+    if rho > 0:
+        taken, at = O.soft_nms(sh_or, lo, hi, ext, rho, sigma)
+    else:
+        taken = O.top_k(sh_or, lo, hi, ext)
+        taken = taken[np.lexsort((taken, -sh_or[taken]))]
+        at = sh_or[taken]
+    tau = at[min(k, hi - lo) - 1]
+    seeds = set(int(i) for i, a in zip(taken, at) if abs(a - tau) <= eps * abs(tau))
+    e = sh_or[lo:hi]
+    for d in range(1, 2 * rho + 1):
+        close = np.abs(e[d:] - e[:-d]) <= eps * np.maximum(e[d:], e[:-d])
+        for i in np.nonzero(close)[0]:
+            seeds.update((lo + int(i), lo + int(i) + d))
+    seeds.update(int(i) for i in np.nonzero(c_or != c_gpu)[0])
+    allowed = set()
+    for i in seeds:
+        allowed.update(range(i - 2 * rho, i + 2 * rho + 1))
+    return allowed
+
+
+@pytest.mark.parametrize("refine", [(1, 0.5, 0.0), (2, 0.3, 0.5)], ids=["nms1", "nms2-excl"])
+def test_refined_chain_vs_oracle_chain(sfi, refine):
+    """What a user of the refined selection gets, end to end: the GPU's slow
+    step -> f and key norms -> refined selection, against the oracle's own
+    chain (slow step -> refined selection in fp64), with nothing from the GPU
+    fed to the oracle.  The sets may differ only inside the stated near-tie
+    band (chain_allowance), and by at most 1% of k per KV head."""
+    B, hq, hkv, d, ns, win, k = 2, 32, 8, 128, 4, 256, 1024
+    lens = [20000, 13001]
+    wl = W.small(B, hq, hkv, d, "bf16", lens, 61, n_sink=ns, window=win, k=k)
+    dl = DeviceLayer.build(wl)
+    lay = dl.layout(sfi, lens)
+    ws = sfi.alloc_workspace(lay)
+    qd, q64 = dl.queries(0)
+    out = torch.empty(B, hq, d, device="cuda")
+    f_d = torch.zeros(B, hkv, lay.max_len, device="cuda")
+    kn_d = torch.zeros_like(f_d)
+    sfi.sfi_slow_attn(lay, qd, dl.k, dl.v, out, f_d, kn_d, ws)
+    prm = sfi.params(ns, win, k, wl.lam)
+    rho, sigma, beta = refine
+    idx, cnt, s_gpu = run_refined(sfi, lay, prm, sfi.sfi_refine(rho, sigma, beta), f_d, kn_d, B, hkv, k)
+    for b in range(B):
+        n = lens[b]
+        st = O.slow_step(q64[b], dl.K64[b], dl.V64[b], n, ns, win, k, wl.lam)
+        lo, hi = st["lo"], st["hi"]
+        s_or = st["s"]
+        sets_or = O.refined_select(s_or, lo, hi, k, rho, sigma, beta)
+        c_or = np.zeros(n)
+        c_gpu = np.zeros(n)
+        for g in range(hkv):
+            got = idx[b, g, :cnt[b, g]].astype(np.int64)
+            exp = sets_or[g]
+            assert len(got) == len(exp) == min(k, hi - lo)
+            sh_or = s_or[g] * np.exp(-beta * c_or)
+            # the premise of the band: the GPU's scores are within it where it matters
+            top = sh_or[lo:hi] >= 0.1 * np.sort(sh_or[lo:hi])[::-1][len(exp) - 1]
+            rel = np.abs(s_gpu[b, g, lo:hi] - s_or[g, lo:hi]) / s_or[g, lo:hi]
+            assert float(rel[top].max()) <= 0.25 * CHAIN_EPS
+            diff = set(got.tolist()) ^ set(exp.tolist())
+            allowed = chain_allowance(sh_or, c_or, c_gpu, lo, hi, k, rho, sigma, CHAIN_EPS)
+            outside = sorted(diff - allowed)
+            assert not outside, f"seq {b} head {g}: {len(outside)} positions differ outside the band: {outside[:6]}"
+            assert len(diff) <= max(4, k // 100), (b, g, len(diff))
+            c_or[exp] += 1
+            c_gpu[got] += 1

@@ -11,11 +11,15 @@ from tests.sfi_testlib import DeviceLayer, O_TOL, check_selection, load_sfi, max
 
 pytestmark = pytest.mark.gpu
 
-# Collected logit sums: each is a sum of 2*G logits of size O(1), accumulated
-# in fp32 on the tensor cores from exact bf16 products; 1e-4 * (1 + |L|)
-# bounds that accumulation with a wide margin.  The selection tie band is the
-# same absolute term: positions closer than that to the k-th sum are ambiguous.
-L_TOL = 1e-4
+# Collected logit sums, from exact bf16 products accumulated in fp32 on the
+# tensor cores.  Measured against the oracle over every shape below and the
+# full batch-4 x 65536 configuration: max |L_gpu - L| = 5.2e-6 for one KV
+# head's sum (|L| up to 122) and 1.6e-5 for the sum over the 8 KV heads that
+# the per-sequence selection ranks.  The bounds are about 4x and 3x those.
+L_TOL = 2e-5     # one KV head's collected sum
+LSUM_TOL = 5e-5  # the sum over KV heads
+# Selection tie band: 1e-6 relative of the k-th value (the stated rule) plus
+# the bound on the error of the values ranked.
 
 
 @pytest.fixture(scope="module")
@@ -60,7 +64,8 @@ def run_vegas(sfi, wl, n_pre, gamma, k, collect, per_head=False):
         assert max_abs(out[b], o_ref) <= O_TOL[sh.dtype], max_abs(out[b], o_ref)
         Lg = O.collected_logit_sum(logits, collect, n_pre[b], n_kv_heads=sh.n_kv_heads)
         got = lsum_np[b, :, :n_pre[b]]
-        assert np.all(np.abs(got - Lg) <= L_TOL * (1 + np.abs(Lg))), float(np.max(np.abs(got - Lg)))
+        assert np.all(np.abs(got - Lg) <= L_TOL), float(np.max(np.abs(got - Lg)))
+        assert np.all(np.abs(got.sum(0) - Lg.sum(0)) <= LSUM_TOL), float(np.max(np.abs(got.sum(0) - Lg.sum(0))))
         assert np.all(lsum_np[b, :, n_pre[b]:] == -7.0), "wrote past the prefix"
         ke = min(k, n_pre[b])
         assert np.all(cnt[b] == ke)
@@ -68,7 +73,7 @@ def run_vegas(sfi, wl, n_pre, gamma, k, collect, per_head=False):
             sets = []
             for g in range(sh.n_kv_heads):
                 sel = idx[b, g, :ke]
-                check_selection(sel, Lg[g], 0, n_pre[b], k, rtol=1e-6, atol=L_TOL * (1 + np.abs(Lg[g]).max()))
+                check_selection(sel, Lg[g], 0, n_pre[b], k, rtol=1e-6, atol=L_TOL)
                 assert np.array_equal(sel, O.top_k(s_np[b, g].astype(np.float64), 0, n_pre[b], k))
                 sets.append(sel.astype(np.int64))
             T.append(sets)
@@ -77,7 +82,7 @@ def run_vegas(sfi, wl, n_pre, gamma, k, collect, per_head=False):
         sel = idx[b, 0, :ke]
         for g in range(1, sh.n_kv_heads):
             assert np.array_equal(idx[b, g, :ke], sel)
-        check_selection(sel, L, 0, n_pre[b], k, rtol=1e-6, atol=L_TOL * (1 + np.abs(L).max()))
+        check_selection(sel, L, 0, n_pre[b], k, rtol=1e-6, atol=LSUM_TOL)
         assert np.array_equal(sel, O.top_k(s_np[b, 0].astype(np.float64), 0, n_pre[b], k))
         T.append(sel.astype(np.int64))
     # draft steps j = 1..gamma at length n_pre + gamma + j: T plus the tail since the prefix

@@ -2,7 +2,8 @@
 
 Every consumer wait of the attention kernel for a stage of cache rows has a
 limit (sfi_set_wait_limit; about 2 s by default).  Here the limit is set to a
-single SM clock, so the first wait for rows that have not landed yet gives up:
+single SM clock, so the first wait for rows that have not landed yet gives up
+(a CTA's first stage is never in shared memory when its consumers first look):
 the kernel must set SFI_DEV_WAIT_TIMEOUT, return (the stream completes), and
 leave the context usable -- after the workspace is zero-filled again, the same
 call with the default limit must reproduce the oracle's dense output and the
