@@ -321,9 +321,15 @@ typedef struct {
 } sfi_ctx_desc;
 
 /* Create a decode context: allocates (with cudaMalloc, once) each layer's
- * selection buffers and the shared evidence/workspace buffers (two sets when
- * async_select != 0; with a refinement each set adds its candidate lists and
- * exclusivity counts), and with async_select its stream and events. */
+ * selection buffers and key-norm store, and the shared evidence/workspace
+ * buffers (two sets when async_select != 0; with a refinement each set adds
+ * its candidate lists and exclusivity counts), and with async_select its
+ * stream and events.
+ * The key norms (the prior's cache statistic) of every (layer, sequence, KV
+ * head) are kept across steps: a refresh computes only the norms of cache
+ * rows appended since that layer's last refresh, since a cache row never
+ * changes once written.  If a sequence's cache rows are replaced (a new
+ * request in its batch slot, a rewritten cache), call sfi_ctx_reset. */
 sfi_status sfi_ctx_create(const sfi_ctx_desc* desc, sfi_ctx** ctx_out);
 sfi_status sfi_ctx_destroy(sfi_ctx* ctx);
 
@@ -356,8 +362,8 @@ sfi_status sfi_schedule(int32_t batch, int32_t budget, const uint8_t* is_boundar
                         uint8_t* have_sel, int32_t* since, uint8_t* slow_out);
 
 /* Forget the schedule state (every sequence starts again without a
- * selection, so its next step is slow) and zero-fill the context's
- * workspace, clearing its device status.  Synchronous: waits for the
+ * selection, so its next step is slow) and the stored key norms, and
+ * zero-fill the context's workspace, clearing its device status.  Synchronous: waits for the
  * device (cudaMemset), so no decode step of this context may be in flight
  * on another thread. */
 sfi_status sfi_ctx_reset(sfi_ctx* ctx);

@@ -83,8 +83,29 @@ WsPlan plan_workspace(int B, int H_q, int H_kv, int D, int max_len) {
   off += align256(size_t(B) * H_q * 2 * 4);
   p.s_off = off;
   off += align256(units * size_t(max_len) * 4);
+  p.sel_nu_off = off;
+  off += align256(units * kSelMaxChunks * 4);
+  p.sel_cnt_off = off;
+  off += align256(units * kSelMaxChunks * 4);
+  p.sel_hist_off = off;
+  off += align256(units * 2048 * 4);
+  p.sel_done_off = off;
+  off += align256(units * 4);
+  p.sel_keys_off = off;
+  off += align256(units * size_t(max_len) * 4);
+  p.sel_list_off = off;
+  off += align256(units * size_t(max_len) * 8);
   p.total = off;
   return p;
+}
+
+void attach_select_scratch(SelectArgs& a, char* ws, const WsPlan& p) {
+  a.sel_nu = reinterpret_cast<float*>(ws + p.sel_nu_off);
+  a.sel_cnt = reinterpret_cast<uint32_t*>(ws + p.sel_cnt_off);
+  a.sel_hist = reinterpret_cast<uint32_t*>(ws + p.sel_hist_off);
+  a.sel_done = reinterpret_cast<uint32_t*>(ws + p.sel_done_off);
+  a.sel_keys = reinterpret_cast<uint32_t*>(ws + p.sel_keys_off);
+  a.sel_list = reinterpret_cast<unsigned long long*>(ws + p.sel_list_off);
 }
 
 sfi_status check_layout(const sfi_layout* L) {
@@ -353,6 +374,11 @@ sfi_status run_attn(AttnArgs& a, const sfi_layout* L, long long n_slow_units, in
                                         a.emit != 0 && n_slow_units > 0);
   a.rpi_slow = sp.rpi_a;
   a.rpi_fast = sp.rpi_b;
+  // fast units only: every unit gets the items of the row bound, and the
+  // kernel maps item ids to units without a unit table
+  a.fast_items = n_slow_units == 0 && n_fast_units > 0 && fast_rows > 0
+                     ? int((fast_rows + sp.rpi_b - 1) / sp.rpi_b)
+                     : 0;
   const cudaError_t e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st, pdl)
                                             : launch_attn_bf16(a, L->head_dim, G, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -474,6 +500,7 @@ sfi_status sfi_select(const sfi_layout* L, const sfi_params* P, const float* evi
   a.g_only = -1;
   for (int b = 0; b < L->batch; ++b) a.active.bits[b >> 5] |= 1u << (b & 31);
   a.status = reinterpret_cast<uint32_t*>(w + p.status_off);
+  attach_select_scratch(a, w, p);
   const cudaError_t e = launch_select(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "selector launch");
   return SFI_OK;

@@ -296,22 +296,33 @@ __device__ bool attn_build_units(const AttnArgs& a, int* units, int n_units, int
   return over == 0;
 }
 
+// report: flag an invalid length (launches without a unit table report it
+// from the producer of each unit's first item).
 __device__ __forceinline__ ItemInfo attn_resolve(const AttnArgs& a, const int* units, int n_units,
-                                                 int it, int sr) {
-  // largest u with units[u] <= it
-  int lo = 0, hi = n_units - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (units[mid] <= it) lo = mid;
-    else hi = mid - 1;
-  }
+                                                 int it, int sr, bool report = false) {
   ItemInfo I;
-  I.u = unit_at(a, units + n_units + 1, lo);
+  if (a.fast_items > 0) {
+    // every unit is fast and has exactly fast_items items: item it belongs to
+    // unit it / fast_items (the fast units of a launch without slow ones are
+    // in unit order)
+    I.u = it / a.fast_items;
+    I.first = I.u * a.fast_items;
+    I.n_items = a.fast_items;
+  } else {
+    // largest u with units[u] <= it
+    int lo = 0, hi = n_units - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (units[mid] <= it) lo = mid;
+      else hi = mid - 1;
+    }
+    I.u = unit_at(a, units + n_units + 1, lo);
+    I.first = units[lo];
+    I.n_items = units[lo + 1] - units[lo];
+  }
   I.b = I.u / a.H_kv;
   I.g = I.u % a.H_kv;
-  I.first = units[lo];
-  I.n_items = units[lo + 1] - units[lo];
-  I.rows = attn_unit_rows(a, I.u, false);
+  I.rows = attn_unit_rows(a, I.u, report && it == I.first);
   const int i = it - I.first, k = I.n_items;
   const int n_stages = (I.rows + sr - 1) / sr;
   I.c_first = i * sr;
@@ -348,8 +359,28 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
     const int it = pw == 0 ? ring_fetch_publish(a, total, ring, iseq, abort_flag, lane, first_id)
                            : ring_read(a, ring, iseq, abort_flag, lane);
     if (it < 0) break;
-    const ItemInfo I = attn_resolve(a, units, n_units, it, C::SR);
-    const size_t head0 = size_t(a.kv_offset[I.b]) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
+    // Without a unit table the item's unit is known from its id, so the
+    // index entries of its first stage (item i starts at stage i) and the
+    // sequence's cache offset are loaded together with the unit's length and
+    // count: one round trip to global memory instead of three before the
+    // first rows are requested.  An entry is used only if the row turns out
+    // to be a selected one (sinks = n_sink, which holds unless n < n_sink).
+    int spec[PJ];
+    long long kvo_spec = 0;
+    const bool spec_ok = a.fast_items > 0;
+    if (spec_ok) {
+      const int su = it / a.fast_items, si = it - su * a.fast_items;
+      const int32_t* ixs = a.idx + size_t(su) * a.idx_stride;
+      kvo_spec = a.kv_offset[su / a.H_kv];
+#pragma unroll
+      for (int j = 0; j < PJ; ++j) {
+        const int e = si * C::SR + rbase + lane + 32 * j - a.n_sink;
+        spec[j] = (lane + 32 * j < RPW && e >= 0 && e < a.idx_stride) ? __ldg(ixs + e) : 0;
+      }
+    }
+    const ItemInfo I = attn_resolve(a, units, n_units, it, C::SR, spec_ok && pw == 0);
+    const long long kvo = spec_ok ? kvo_spec : (long long)a.kv_offset[I.b];
+    const size_t head0 = size_t(kvo) + size_t(I.g) * size_t(a.kv_cap[I.b]) * D;
     const char* kb = reinterpret_cast<const char*>(a.k) + head0 * C::ES;
     const char* vb = reinterpret_cast<const char*>(a.v) + head0 * C::ES;
     const int n = I.n;
@@ -362,14 +393,14 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
     long long row0 = 0;
     bool tma_unit = false;
     if constexpr (C::MMA) {
-      const long long off = a.kv_offset[I.b];
+      const long long off = kvo;
       row0 = off / D + (long long)I.g * a.kv_cap[I.b];
       tma_unit = a.use_tma && tma_ok && I.slow && off % D == 0 && row0 + I.rows < (1LL << 31);
     }
     // Row positions of stage c0 (lane l: rows l, l + 32, ...).  Gathered
     // positions come from the index list in global memory, so the loads
     // for the next stage are issued one stage ahead of their use.
-    auto resolve_pos = [&](int c0s, int (&out)[PJ]) {
+    auto resolve_pos = [&](int c0s, int (&out)[PJ], bool use_spec) {
       const int nrs = min(C::SR, I.rows - c0s);
 #pragma unroll
       for (int j = 0; j < PJ; ++j) {
@@ -380,7 +411,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
           if (lp < ns) {
             p = lp;
           } else if (lp < ns + cnt) {
-            p = __ldg(ix + (lp - ns));
+            p = use_spec ? spec[j] : __ldg(ix + (lp - ns));
           } else {
             p = wlo + (lp - ns - cnt);
           }
@@ -389,7 +420,8 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
       }
     };
     int pos_next[PJ];
-    resolve_pos(I.c_first, pos_next);
+    // the speculative entries hold ix[lp - n_sink] for the first stage's rows
+    resolve_pos(I.c_first, pos_next, spec_ok && ns == a.n_sink);
     for (int si = 0; si < I.n_st; ++si) {
       const int c0 = I.c_first + si * I.c_step;
       const int nr = min(C::SR, I.rows - c0);
@@ -405,7 +437,7 @@ __device__ __forceinline__ void attn_produce(const AttnArgs& a, const int* units
         }
         pos[j] = p;
       }
-      if (si + 1 < I.n_st) resolve_pos(c0 + I.c_step, pos_next);
+      if (si + 1 < I.n_st) resolve_pos(c0 + I.c_step, pos_next, false);
       if (!warp_ctrl_wait(bar_empty + 8 * slot, ph ^ 1u, abort_flag, a.status)) {
         ok = false;
         break;
@@ -473,6 +505,8 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
   const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
   const bool emit = a.emit && I.slow;
   const bool emit_norm = emit && a.knorm != nullptr;
+  // key norms of rows below nv are already stored (they never change)
+  const int nv = emit_norm && a.knorm_valid ? a.knorm_valid[I.u] : 0;
     float qf[G][C::EPL];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -502,6 +536,7 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
       // schedule, so every consumer warp reaches every named barrier.
       const bool have = warp_pipe_wait(bar_full + 8 * slot, ph, abort_flag, a.status, a.wait_cycles);
       const int wr0 = warp * C::RB;
+      const bool norm_stage = emit_norm && c0 + nr > nv;
       if (have && wr0 < nr) {
         const int nw = min(C::RB, nr - wr0);
         const uint32_t krow = kbase + slot * C::STAGE_B + (wr0 + lg * C::R) * C::ROWB + li * 16;
@@ -533,7 +568,7 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
           const int hh = j / C::R, row = lg * C::R + (j % C::R);
           sl[row * G + hh] = row < nw ? x[i] : -INFINITY;
         }
-        if (emit_norm) {
+        if (norm_stage) {
           const int jn = transpose_reduce<C::LPR>(nn, li);
           const int row = lg * C::R + jn;
           if (row < nw) sn[row] = sqrtf(nn[0]);
@@ -555,7 +590,7 @@ __device__ __forceinline__ void attn_item_simt(const AttnArgs& a, const ItemInfo
             const int e = lane + 32 * t;
             if (e < nw * G) lg_out[e] = lv[t];
           }
-          if (emit_norm && lane < nw) a.knorm[size_t(I.u) * a.max_len + c0 + wr0 + lane] = sn[lane];
+          if (norm_stage && lane < nw) a.knorm[size_t(I.u) * a.max_len + c0 + wr0 + lane] = sn[lane];
         }
 #pragma unroll
         for (int o = G; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
@@ -661,6 +696,8 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
   const uint32_t kbase = smem_addr(smem + C::OFF_K), vbase = smem_addr(smem + C::OFF_V);
   const bool emit = a.emit && I.slow;
   const bool emit_norm = emit && a.knorm != nullptr;
+  // key norms of rows below nv are already stored (they never change)
+  const int nv = emit_norm && a.knorm_valid ? a.knorm_valid[I.u] : 0;
   const float qs = a.qscale;
 
   // B operand of S^T: q of head g (zero for heads >= G), bf16 pairs at
@@ -716,7 +753,8 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
           }
         }
       };
-      if (emit_norm) {
+      const bool norm_stage = emit_norm && c0 + nr > nv;
+      if (norm_stage) {
         qk(std::true_type{});
       } else {
         qk(std::false_type{});
@@ -739,7 +777,7 @@ __device__ __forceinline__ void attn_item_mma(const AttnArgs& a, const ItemInfo&
               if (2 * t + h < G) lo[2 * t + h] = l[r][h];
           }
         }
-        if (emit_norm && t == (g >> 1)) {
+        if (norm_stage && t == (g >> 1)) {
           // lane (g, g / 2) holds the diagonal entries (g, g) and (g + 8, g + 8)
           const float n0 = (g & 1) ? gram[0][1] : gram[0][0];
           const float n1 = (g & 1) ? gram[1][3] : gram[1][2];
@@ -851,7 +889,7 @@ __device__ __forceinline__ void attn_merge_items(const AttnArgs& a, const ItemIn
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int i = lane + 32 * r;
-      const float f = i < n ? exp2f(m[r] - M) : 0.f;
+      const float f = i < n && m[r] != -INFINITY ? exp2f(m[r] - M) : 0.f;  // empty items: 0
       if (i < n) sc[i * G + hh] = f;
       Z = fmaf(z[r], f, Z);
     }
@@ -909,8 +947,18 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
   if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
   if (a.len_copy && blockIdx.x == 0)
     for (int b = tid; b < a.B; b += C::NT) a.len_copy[b] = a.len[b];
-  const bool units_fit = attn_build_units<C::NT>(a, units, n_units, misc);
-  const int total = units[n_units];
+  // A launch of fast units only, each cut into exactly fast_items items (the
+  // host checked both item limits), needs no unit table: an item's unit
+  // follows from its id, and the first item starts without waiting for the
+  // table's loads.
+  bool units_fit = true;
+  int total;
+  if (a.fast_items > 0) {
+    total = n_units * a.fast_items;
+  } else {
+    units_fit = attn_build_units<C::NT>(a, units, n_units, misc);
+    total = units[n_units];
+  }
   if (total > a.max_items || !units_fit) {
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);
     // leave the work counters at zero for the next launch
@@ -988,7 +1036,8 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
 #pragma unroll
       for (int w = 0; w < C::NCW; ++w) {
         const float* rw = red_all + ((w ^ wflip) * G + hh) * (D + 2);
-        const float sc = exp2f(rw[0] - M);
+        // a warp (or a whole item) without rows holds m = -inf: weight 0
+        const float sc = rw[0] == -INFINITY ? 0.f : exp2f(rw[0] - M);
         Z = fmaf(rw[1], sc, Z);
         A = fmaf(rw[2 + dim], sc, A);
       }
@@ -1007,6 +1056,9 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
         }
       }
     }
+    // a refreshing unit whose rows all have their key norms stored now
+    const bool norms_done = emit && a.knorm != nullptr && a.knorm_valid != nullptr;
+    if (single && norms_done && tid == 0) a.knorm_valid[I.u] = I.n;
     if (!single) {
       __threadfence();
       named_bar_sync(1, nct);
@@ -1015,7 +1067,10 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
       if (misc[kMiscLast]) {
         __threadfence();
         attn_merge_items<D, G>(a, I, emit, red_all, tid, nct);
-        if (tid == 0) a.counters[I.u] = 0;
+        if (tid == 0) {
+          a.counters[I.u] = 0;
+          if (norms_done) a.knorm_valid[I.u] = I.n;
+        }
       }
     }
     named_bar_sync(1, nct);

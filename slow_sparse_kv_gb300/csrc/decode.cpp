@@ -29,8 +29,12 @@ struct sfi_ctx {
   sfi::WsPlan plan;
   // device, per buffer set
   char* ws[2] = {nullptr, nullptr};        // attention / selector workspace
-  float* knorm[2] = {nullptr, nullptr};    // [B*H_kv][max_len]
   int32_t* len_copy[2] = {nullptr, nullptr};  // [B]
+  // Key norms of every layer's cache rows, kept across steps: a cache row
+  // never changes, so a refresh computes only the norms of the rows appended
+  // since the layer's last refresh (knorm_valid[layer][u] rows are stored).
+  float* knorm = nullptr;          // [L][B*H_kv][max_len]
+  int32_t* knorm_valid = nullptr;  // [L][B*H_kv]
   // selector refinements (desc.refine): candidate lists, their counts and the
   // exclusivity counts, per buffer set
   bool refine = false;
@@ -69,7 +73,6 @@ void free_ctx(sfi_ctx* c) {
     if (c->attn_done[p]) cudaEventDestroy(c->attn_done[p]);
     if (c->sel_done[p]) cudaEventDestroy(c->sel_done[p]);
     cudaFree(c->ws[p]);
-    cudaFree(c->knorm[p]);
     cudaFree(c->len_copy[p]);
     cudaFree(c->cand[p]);
     cudaFree(c->ccount[p]);
@@ -78,6 +81,8 @@ void free_ctx(sfi_ctx* c) {
   if (c->side) cudaStreamDestroy(c->side);
   cudaFree(c->idx);
   cudaFree(c->count);
+  cudaFree(c->knorm);
+  cudaFree(c->knorm_valid);
   delete c;
 }
 
@@ -148,7 +153,6 @@ sfi_status sfi_ctx_create(const sfi_ctx_desc* d, sfi_ctx** out) {
   for (int p = 0; p < c->n_sets && e == cudaSuccess; ++p) {
     e = cudaMalloc(&c->ws[p], c->plan.total);
     if (e == cudaSuccess) e = cudaMemset(c->ws[p], 0, c->plan.total);
-    if (e == cudaSuccess) e = cudaMalloc(&c->knorm[p], row);
     if (e == cudaSuccess) e = cudaMalloc(&c->len_copy[p], size_t(d->batch) * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->attn_done[p], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->sel_done[p], cudaEventDisableTiming);
@@ -169,6 +173,11 @@ sfi_status sfi_ctx_create(const sfi_ctx_desc* d, sfi_ctx** out) {
     e = cudaMalloc(&c->idx, size_t(d->n_layers) * units * d->params.k * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&c->count, size_t(d->n_layers) * units * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->count, 0, size_t(d->n_layers) * units * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&c->knorm, size_t(d->n_layers) * row);
+  if (e == cudaSuccess)
+    e = cudaMalloc(&c->knorm_valid, size_t(d->n_layers) * units * sizeof(int32_t));
+  if (e == cudaSuccess)
+    e = cudaMemset(c->knorm_valid, 0, size_t(d->n_layers) * units * sizeof(int32_t));
   if (e != cudaSuccess) {
     free_ctx(c);
     return cuda_fail(e, "allocating the decode context");
@@ -212,6 +221,9 @@ sfi_status sfi_ctx_reset(sfi_ctx* c) {
   cudaError_t e = c->side ? cudaStreamSynchronize(c->side) : cudaSuccess;
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   for (int p = 0; p < c->n_sets && e == cudaSuccess; ++p) e = cudaMemset(c->ws[p], 0, c->plan.total);
+  if (e == cudaSuccess)
+    e = cudaMemset(c->knorm_valid, 0,
+                   size_t(c->desc.n_layers) * c->desc.batch * c->desc.n_kv_heads * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "zero-filling the context workspace");
   return SFI_OK;
@@ -344,7 +356,8 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
       ++n_slow;
     }
   a.emit = 1;
-  a.knorm = c->knorm[p];
+  a.knorm = c->knorm + size_t(layer) * units * d.max_len;
+  a.knorm_valid = c->knorm_valid + size_t(layer) * units;
   a.idx = idx;
   a.count = count;
   a.idx_stride = d.params.k;
@@ -387,7 +400,7 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   sa.logits = a.logits;
   sa.stats = a.stats;
   sa.H_q = d.n_q_heads;
-  sa.knorm = c->knorm[p];
+  sa.knorm = a.knorm;
   sa.len = c->len_copy[p];
   sa.idx = idx;
   sa.count = count;
@@ -403,6 +416,7 @@ sfi_status sfi_decode_step(sfi_ctx* c, int32_t layer, const uint8_t* is_boundary
   sa.g_only = -1;
   sa.active = a.slow;
   sa.status = a.status;
+  attach_select_scratch(sa, c->ws[p], c->plan);
   if (c->refine) {
     // the refinement reads the fused scores back: they go to the workspace
     sa.s = reinterpret_cast<float*>(c->ws[p] + c->plan.s_off);

@@ -140,6 +140,7 @@ extern "C" sfi_status sfi_fast_attn_noalloc(const sfi_layout* L, const sfi_param
   a.partials = reinterpret_cast<float*>(w + kHeaderBytes + counters_bytes);
   a.max_items = int(max_items < 0x7fffffff ? max_items : 0x7fffffff);
   a.rpi_slow = a.rpi_fast = int(rpi);
+  a.fast_items = int(items_per_unit);
   e = L->dtype == SFI_F32 ? launch_attn_f32(a, L->head_dim, G, st, true)
                           : launch_attn_bf16(a, L->head_dim, G, st, true);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");

@@ -606,6 +606,7 @@ extern "C" sfi_status sfi_select_refined(const sfi_layout* L, const sfi_params* 
   sa.window = P->window;
   sa.lambda = P->lambda;
   sa.status = reinterpret_cast<uint32_t*>(w + rp.base.status_off);
+  attach_select_scratch(sa, w, rp.base);
   for (int b = 0; b < L->batch; ++b) sa.active.bits[b >> 5] |= 1u << (b & 31);
   return run_refined_select(sa, *R, P->k, rp.M, idx_out, count_out,
                             reinterpret_cast<int32_t*>(w + rp.cand_off),

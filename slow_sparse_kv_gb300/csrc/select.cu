@@ -12,23 +12,27 @@
 // Evidence pass: f[b][g][i] = (1/G) sum_h 2^(l_{h,i} - M_h) / Z_h from the
 // log2-scaled logits and per-head (M, Z) the attention kernel stored.
 //
-// Selector: one thread-block cluster of 8 CTAs (512 threads each) per
-// (sequence, KV head) -- or per sequence in the per-sequence logit-sum mode
-// -- launched for the refreshing sequences only.  Each CTA holds the scores
-// of one eighth of the positions in shared memory.  The evidence pass forms
-// f (from the logits on the decode path) and the CTA's part of the key-norm
-// sum over E; after a cluster barrier every CTA writes s and the histogram of
-// the top 11 bits of the order key of s over E.  The cluster total of that
-// histogram fixes the top digit of the k-th largest key; the keys in that
-// bin (few, at the decode workloads) are gathered in rank 0, which finds the
-// two lower digits (11 and 10 bits) alone -- or, when the bin holds more than
-// kCandCap keys, every CTA runs the two passes over all its keys.  A final
-// ordered compaction writes the keys above tau, then the lowest-positioned
-// keys equal to tau, in ascending position order, so ties go to the lower
-// position exactly as the definition says.  Histograms use warp-aggregated
-// shared-memory atomics (the score distribution is very skewed, so many
-// lanes hit the same bin).
-#include <cooperative_groups.h>
+// Selector.  Each selecting unit -- a (sequence, KV head), or a sequence in
+// the per-sequence logit-sum mode -- is cut into C chunks of consecutive
+// positions, and C is chosen so that all units together give about two CTAs
+// per SM: every SM works on the few units of a decode step.  No CTA ever
+// waits for another; three launches, each a programmatic dependent of the
+// one before it, pass their results through the workspace:
+//  1. (fused mode) each chunk sums its key norms over E;
+//  2. each chunk forms the scores (f from the logits on the decode path),
+//     writes s when asked, the order key of every position of E and adds
+//     its histogram of the keys' top 11 bits to the unit's (integer atomics);
+//  3. each chunk reads the unit's histogram, which fixes the top digit d0 of
+//     the k-th largest key, and writes its keys at or above d0 -- as
+//     (key, position), in position order -- to its own region of a list.  The
+//     last chunk CTA of the unit to finish (an atomic counter) finds the two
+//     lower digits among the keys of bin d0 (few: about 2% of E at the decode
+//     workloads) and writes the keys above the k-th, then the lowest-
+//     positioned keys equal to it, in ascending position order, so ties go to
+//     the lower position exactly as the definition says.  It leaves the
+//     histogram and the counter at zero for the next launch.
+// All sums run in a fixed order, so the selection does not depend on the
+// schedule.
 #include <math.h>
 
 #include "common.cuh"
@@ -37,42 +41,15 @@
 namespace sfi {
 
 constexpr int kFpassThreads = 256;
-constexpr int kSelCluster = 8;   // CTAs per unit
-constexpr int kSelCT = 512;      // threads per selector CTA
-
-constexpr int kSelU = 8;         // positions in flight per selector thread
-constexpr int kRadixPasses = 3;  // digits of 11, 11 and 10 bits
+constexpr int kSelT = 512;      // threads of a score or list CTA
+constexpr int kSelNuT = 256;    // threads of a key-norm sum CTA
+constexpr int kSelU = 8;        // positions in flight per thread
 constexpr int kRadixBins = 2048;
-constexpr int kRadixShift0 = 21;
+constexpr int kRadixShift0 = 21;  // digits: bits 31..21, 20..10, 9..0 of the order key
 constexpr int kRadixShift1 = 10;
-// Largest cluster-wide count of keys in the k-th key's top bin for which the
-// two lower digits are found on a gathered list (it must fit two rows of the
-// total histograms).
-constexpr int kCandCap = 4096;
-static_assert(kCandCap <= (kRadixPasses - 1) * kRadixBins, "gathered list fits hist_g rows 1..2");
-
-// Dynamic shared memory of a selector CTA: its scores (ceil(max_len / 8)
-// floats), the candidate list, and, when it fits, a copy of its key norms.
-__host__ __device__ constexpr size_t select_cand_offset(int max_len) {
-  return (size_t((max_len + kSelCluster - 1) / kSelCluster) * sizeof(float) + 15) / 16 * 16;
-}
-__host__ __device__ constexpr size_t select_kn_offset(int max_len) {
-  return select_cand_offset(max_len) + size_t(kCandCap) * sizeof(uint32_t);
-}
-
-// Eight consecutive scores sc[o .. o+7] (o a multiple of 8, scores past `lim`
-// read as 0); two 16-byte shared-memory loads when the block is in range.
-__device__ __forceinline__ void load8(const float* sc, int o, int lim, float (&v)[8]) {
-  if (o + 8 <= lim) {
-    const float4 a = *reinterpret_cast<const float4*>(sc + o);
-    const float4 b = *reinterpret_cast<const float4*>(sc + o + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = o + j < lim ? sc[o + j] : 0.f;
-  }
-}
+constexpr int kCandCap = 8192;  // keys of bin d0 the finisher gathers in shared memory
+constexpr int kSelMinChunk = 2048;  // positions per chunk, at least
+constexpr int kRun = 8;             // consecutive list positions or entries per thread and tile
 
 // The G logits of one position ([pos][G] rows are 4*G-byte aligned).
 template <int G>
@@ -133,13 +110,13 @@ __global__ void __launch_bounds__(kFpassThreads) fpass_kernel(const FpassArgs a)
 __device__ float sel_block_sum(float v, float* sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(kFull, v, o);
   if (lane == 0) sh[w] = v;
   __syncthreads();
   if (w == 0) {
     v = lane < int(blockDim.x >> 5) ? sh[lane] : 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(kFull, v, o);
     if (lane == 0) sh[32] = v;
   }
   __syncthreads();
@@ -181,14 +158,14 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, ui
 
 // Pick the digit d with above(d) < krem <= above(d) + hist[d] (above(d)
 // counts the keys in higher bins), with the whole block: thread t sums
-// NB / kSelCT consecutive bins from the top, a block scan gives the count
+// NB / kSelT consecutive bins from the top, a block scan gives the count
 // above its range, and the one thread whose range holds the krem-th key
 // walks its bins.  0 < krem <= the histogram's total.  Ends with a barrier.
 template <int NB>
 __device__ void block_pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_digit,
                                  uint32_t* out_above, uint32_t* scan_sh) {
-  constexpr int PER = NB / kSelCT;
-  static_assert(PER * kSelCT == NB, "bins split evenly over the block");
+  constexpr int PER = NB / kSelT;
+  static_assert(PER * kSelT == NB, "bins split evenly over the block");
   const int top = NB - 1 - PER * int(threadIdx.x);  // bins top, top - 1, ..., top - PER + 1
   uint32_t c[PER];
   uint32_t sum = 0;
@@ -214,350 +191,389 @@ __device__ void block_pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* 
   __syncthreads();
 }
 
-// One cluster of kSelCluster CTAs per unit; CTA `rank` owns the positions
-// [rank * ch, (rank + 1) * ch) of [0, n) and keeps their scores in shared
-// memory.  Cluster-wide quantities (the key-norm sum over E, the radix
-// histograms, the compaction offsets) are exchanged through distributed
-// shared memory; every CTA takes the same decisions from the same data.
-// EV_G > 0: the evidence is computed here from the attention kernel's
-// log2-scaled logits [pos][EV_G] and per-head (M, Z) (decode path); EV_G == 0:
-// `evidence` holds f (or, per sequence, the per-KV-head logit sums).
-template <int EV_G>
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelCT)
-    select_cluster_kernel(const SelectArgs a) {
-  namespace cg = cooperative_groups;
-  cg::cluster_group cl = cg::this_cluster();
-  extern __shared__ __align__(16) unsigned char sel_smem[];
-  float* sc = reinterpret_cast<float*>(sel_smem);
-  __shared__ uint32_t hist[kRadixBins];
-  __shared__ uint32_t hist_loc[kRadixBins];  // this CTA's pass-0 histogram
-  // cluster totals, used in rank 0; on the candidate path rows 1-2 hold the
-  // gathered candidate keys
-  __shared__ uint32_t hist_g[kRadixPasses][kRadixBins];
-  // this CTA's keys in the k-th key's top bin (dynamic memory, after the scores)
-  uint32_t* cand = reinterpret_cast<uint32_t*>(sel_smem + select_cand_offset(a.max_len));
-  __shared__ uint32_t cand_n, sh_tau, sh_take, sh_off;
-  __shared__ float shf[33];
-  __shared__ float part_nu;
-  __shared__ uint32_t cnt_gt, cnt_eq;
-  __shared__ uint32_t sh_digit, sh_above;
-  __shared__ uint32_t scan_sh[33];
+// One selecting unit and this CTA's chunk of it.
+struct SelUnit {
+  int b, unit, u;       // sequence; unit; row of the per-position arrays (b * H_kv in the
+                        // per-sequence mode)
+  int n, lo, hi, keff;  // length; E = [lo, hi); selection size
+  int n_sc, ch;         // positions that get a score; chunk length
+  int p0, p1, e0, e1;   // this chunk's positions and its part of E
+  bool per_seq, prior, need_radix;
+};
 
-  const int tid = threadIdx.x;
-  const int rank = int(cl.block_rank());
-  // clusters are launched for the active units only: cluster c serves the
-  // (c / units-per-sequence)-th active sequence
-  const bool per_seq = a.mode == SFI_SELECT_LOGIT_SUM_SEQ;
-  const bool prior = a.mode == SFI_SELECT_FUSED;  // key-norm prior and (1 - lambda) weight
-  const bool one_head = prior && a.g_only >= 0;  // only KV head g_only of each sequence
-  const int ups = per_seq || one_head ? 1 : a.H_kv;  // units per sequence
-  const int c = blockIdx.x / kSelCluster;
-  const int b = active_seq(a.active, c / ups);
-  if (b < 0 || b >= a.B) return;  // uniform over the cluster (cannot happen for a valid grid)
-  const int unit = per_seq ? b : b * a.H_kv + (one_head ? a.g_only : c % ups);
-  const int u = per_seq ? b * a.H_kv : unit;
-  const int n = a.len[b];
-  if (n < 1 || n > a.max_len) {
-    if (tid == 0 && rank == 0) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
-    return;  // uniform over the cluster
+// First position of E in chunk c (where chunk c's list region starts).
+__device__ __forceinline__ int sel_chunk_e0(const SelUnit& s, int c) {
+  return max(s.lo, min(s.n_sc, c * s.ch));
+}
+
+// 0: ok; 1: no such unit (cannot happen for a valid grid); 2: length outside
+// [1, max_len].  The result is the same in every CTA of the unit.
+__device__ __forceinline__ int sel_unit(const SelectArgs& a, int j, int c, int C, SelUnit& s) {
+  s.per_seq = a.mode == SFI_SELECT_LOGIT_SUM_SEQ;
+  s.prior = a.mode == SFI_SELECT_FUSED;            // key-norm prior and (1 - lambda) weight
+  const bool one_head = s.prior && a.g_only >= 0;  // only KV head g_only of each sequence
+  const int ups = s.per_seq || one_head ? 1 : a.H_kv;  // units per sequence
+  s.b = active_seq(a.active, j / ups);
+  if (s.b < 0 || s.b >= a.B) return 1;
+  s.unit = s.per_seq ? s.b : s.b * a.H_kv + (one_head ? a.g_only : j % ups);
+  s.u = s.per_seq ? s.b * a.H_kv : s.unit;
+  s.n = a.len[s.b];
+  if (s.n < 1 || s.n > a.max_len) return 2;
+  s.lo = s.per_seq ? 0 : a.n_sink;
+  s.hi = max(s.lo, s.n - a.window);
+  const int ne = s.hi - s.lo;
+  s.keff = min(a.k, ne);
+  s.n_sc = s.per_seq ? s.hi : s.n;
+  s.ch = ((s.n_sc + C - 1) / C + 3) & ~3;
+  s.p0 = min(s.n_sc, c * s.ch);
+  s.p1 = min(s.n_sc, s.p0 + s.ch);
+  s.e0 = max(s.p0, s.lo);
+  s.e1 = max(s.e0, min(s.p1, s.hi));
+  s.need_radix = s.keff > 0 && s.keff < ne;
+  return 0;
+}
+
+// The three launches are programmatic dependents of the launch before them:
+// each may be scheduled while its predecessor drains, and waits for it before
+// any global access.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch 1 (fused mode): this chunk's sum of key norms over E.
+__global__ void __launch_bounds__(kSelNuT) sel_nu_kernel(const SelectArgs a) {
+  __shared__ float sh[33];
+  pdl_wait();
+  pdl_trigger();
+  SelUnit s;
+  if (sel_unit(a, blockIdx.y, blockIdx.x, gridDim.x, s) != 0) return;
+  const float* kn = a.knorm + size_t(s.u) * a.max_len;
+  float part = 0.f;
+  constexpr int V = 16;  // loads in flight per thread
+  for (int base = s.e0; base < s.e1; base += kSelNuT * V) {
+    float x[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const int i = base + j * kSelNuT + int(threadIdx.x);
+      x[j] = i < s.e1 ? kn[i] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < V; ++j) part += x[j];
   }
-  const int lo = per_seq ? 0 : a.n_sink;
-  const int hi = max(lo, n - a.window);
-  const int ne = hi - lo;
-  const int keff = min(a.k, ne);
-  const int n_sc = per_seq ? hi : n;  // positions that receive a score
-  const int ch = (n_sc + kSelCluster - 1) / kSelCluster;
-  const int p0 = min(n_sc, rank * ch), p1 = min(n_sc, p0 + ch);
-  const bool need_radix = keff > 0 && keff < ne;
-  const float* kn = prior ? a.knorm + size_t(u) * a.max_len : nullptr;
+  const float t = sel_block_sum(part, sh);
+  if (threadIdx.x == 0) a.sel_nu[size_t(s.u) * kSelMaxChunks + blockIdx.x] = t;
+}
 
-  // ---------------------------------------------------------------- evidence
+// Launch 2: scores, order keys and the top-digit histogram.  EV_G > 0: the
+// evidence comes from the attention kernel's log2-scaled logits [pos][EV_G]
+// and per-head (M, Z) (decode path); EV_G == 0: `evidence` holds f (or the
+// per-KV-head logit sums).
+template <int EV_G>
+__global__ void __launch_bounds__(kSelT, 2) sel_score_kernel(const SelectArgs a) {
+  __shared__ uint32_t hist[kRadixBins];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, c = blockIdx.x;
+  SelUnit s;
+  const int r = sel_unit(a, blockIdx.y, c, gridDim.x, s);
+  if (r != 0) {
+    if (r == 2 && c == 0 && tid == 0) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
+    return;  // uniform over the unit
+  }
+  float coef = 0.f;
+  if (s.prior) {
+    // the chunks' key-norm sums in one fixed order: every thread of every CTA
+    // of the unit forms the same value
+    const float* pn = a.sel_nu + size_t(s.u) * kSelMaxChunks;
+    const int lane = tid & 31, C = gridDim.x;
+    float x = (lane < C ? pn[lane] : 0.f) + (lane + 32 < C ? pn[lane + 32] : 0.f);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_down_sync(kFull, x, o);
+    x = __shfl_sync(kFull, x, 0);
+    coef = x > 0.f ? a.lambda / x : 0.f;
+  }
+  if (s.need_radix)
+    for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
+  __syncthreads();
   float M[EV_G > 0 ? EV_G : 1], iz[EV_G > 0 ? EV_G : 1];
   if constexpr (EV_G > 0) {
 #pragma unroll
     for (int hh = 0; hh < EV_G; ++hh) {
-      const size_t qh = size_t(b) * a.H_q + size_t(unit % a.H_kv) * EV_G + hh;
+      const size_t qh = size_t(s.b) * a.H_q + size_t(s.unit % a.H_kv) * EV_G + hh;
       M[hh] = a.stats[qh * 2];
       iz[hh] = 1.0f / a.stats[qh * 2 + 1];
     }
   }
-  // Positions are processed kSelU at a time per thread with every load
-  // issued before any is used, so the loop is bound by bandwidth, not by the
-  // latency of one load after another.
-  float* kns = a.kn_smem ? reinterpret_cast<float*>(sel_smem + select_kn_offset(a.max_len)) : nullptr;
-  float part = 0.f;
-  for (int base = p0; base < p1; base += kSelCT * kSelU) {
-    float lg[kSelU][EV_G > 0 ? EV_G : 1];
-    float ev[kSelU], kv[kSelU];
-#pragma unroll
-    for (int j = 0; j < kSelU; ++j) {
-      const int i = base + j * kSelCT + tid;
-      ev[j] = 0.f;
-      kv[j] = 0.f;
-      if (i < p1) {
-        if constexpr (EV_G > 0) {
-          load_row<EV_G>(a.logits + (size_t(u) * a.max_len + i) * EV_G, lg[j]);
-        } else if (per_seq) {
-          for (int g = 0; g < a.H_kv; ++g) ev[j] += a.evidence[(size_t(b) * a.H_kv + g) * a.max_len + i];
-        } else {
-          ev[j] = a.evidence[size_t(u) * a.max_len + i];
-        }
-        if (prior && i >= lo && i < hi) kv[j] = kn[i];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kSelU; ++j) {
-      const int i = base + j * kSelCT + tid;
-      if (i < p1) {
-        if constexpr (EV_G > 0) ev[j] = evidence_from_logits<EV_G>(lg[j], M, iz);
-        sc[i - p0] = ev[j];
-        if (kns) kns[i - p0] = kv[j];
-        part += kv[j];
-      }
-    }
-  }
-  for (int i = tid; i < kRadixBins; i += kSelCT) {
-    hist[i] = 0;
-    if (rank == 0) {
-      for (int j = 0; j < kRadixPasses; ++j) hist_g[j][i] = 0;
-    }
-  }
-  if (prior) {
-    const float t = sel_block_sum(part, shf);
-    if (tid == 0) part_nu = t;
-  }
-  cl.sync();  // partial norm sums and the zeroed cluster histograms are visible
-  float coef = 0.f;
-  if (prior) {
-    float tot = 0.f;
-    for (int r = 0; r < kSelCluster; ++r) tot += *cl.map_shared_rank(&part_nu, r);
-    coef = tot > 0.f ? a.lambda / tot : 0.f;
-  }
-  // ---------------------------------------------------------------- scores
-  float* srow = a.s ? a.s + size_t(u) * a.max_len : nullptr;
-  const float w_f = prior ? 1.0f - a.lambda : 1.0f;
+  const float* kn = s.prior ? a.knorm + size_t(s.u) * a.max_len : nullptr;
+  float* srow = a.s ? a.s + size_t(s.u) * a.max_len : nullptr;
   // exclusivity: the fused score is written to s as it is; the selection
   // ranks it times exp(-beta * picks of the earlier KV heads)
-  const uint8_t* exrow = prior && a.excl ? a.excl + size_t(b) * a.max_len : nullptr;
-  for (int base = p0; base < p1; base += kSelCT * kSelU) {
-    float kv[kSelU];
-    uint32_t cx[kSelU];
+  const uint8_t* exrow = s.prior && a.excl ? a.excl + size_t(s.b) * a.max_len : nullptr;
+  uint32_t* krow = a.sel_keys + size_t(s.u) * a.max_len;
+  int32_t* out_idx = a.idx + size_t(s.per_seq ? s.b * a.H_kv : s.unit) * a.k;
+  const int n_rows = s.per_seq ? a.H_kv : 1;  // idx rows that receive the set
+  const float w_f = s.prior ? 1.0f - a.lambda : 1.0f;
+  // U positions per thread at a time, every load issued before any is used
+  // (fewer when each position brings G logits, so two CTAs fit an SM)
+  constexpr int U = EV_G >= 8 ? 2 : (EV_G >= 4 ? 4 : kSelU);
+  for (int base = s.p0; base < s.p1; base += kSelT * U) {
+    float lg[U][EV_G > 0 ? EV_G : 1];
+    float ev[U], kv[U];
+    uint32_t cx[U];
 #pragma unroll
-    for (int j = 0; j < kSelU; ++j) {
-      const int i = base + j * kSelCT + tid;
-      const bool e = i < p1 && i >= lo && i < hi;
-      kv[j] = (prior && e) ? (kns ? kns[i - p0] : kn[i]) : 0.f;
-      cx[j] = exrow && e ? exrow[i] : 0u;
+    for (int j = 0; j < U; ++j) {
+      const int i = base + j * kSelT + tid;
+      const bool e = i >= s.lo && i < s.hi;
+      ev[j] = 0.f;
+      kv[j] = 0.f;
+      cx[j] = 0u;
+      if (i < s.p1) {
+        if constexpr (EV_G > 0) {
+          load_row<EV_G>(a.logits + (size_t(s.u) * a.max_len + i) * EV_G, lg[j]);
+        } else if (s.per_seq) {
+          for (int g = 0; g < a.H_kv; ++g)
+            ev[j] += a.evidence[(size_t(s.b) * a.H_kv + g) * a.max_len + i];
+        } else {
+          ev[j] = a.evidence[size_t(s.u) * a.max_len + i];
+        }
+        if (s.prior && e) kv[j] = kn[i];
+        if (exrow && e) cx[j] = exrow[i];
+      }
     }
 #pragma unroll
-    for (int j = 0; j < kSelU; ++j) {
-      const int i = base + j * kSelCT + tid;
-      const bool in = i < p1;
-      float v = 0.f;
+    for (int j = 0; j < U; ++j) {
+      const int i = base + j * kSelT + tid;
+      const bool in = i < s.p1;
+      const bool e = in && i >= s.lo && i < s.hi;
+      uint32_t key = 0u;
       if (in) {
-        v = w_f * sc[i - p0];
-        if (prior && i >= lo && i < hi) v = fmaf(coef, kv[j], v);
+        if constexpr (EV_G > 0) ev[j] = evidence_from_logits<EV_G>(lg[j], M, iz);
+        float v = w_f * ev[j];
+        if (s.prior && e) v = fmaf(coef, kv[j], v);
         if (srow) srow[i] = v;
         v *= excl_factor(cx[j], a.excl_beta);
-        sc[i - p0] = v;
+        key = order_key(v);
+        if (e) {
+          if (s.need_radix) {
+            krow[i] = key;
+          } else {  // keep all of E: position lo + t goes to slot t
+            for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + (i - s.lo)] = i;
+          }
+        }
       }
-      if (need_radix) hist_add(hist, order_key(v) >> kRadixShift0, in && i >= lo && i < hi);
+      if (s.need_radix) hist_add(hist, key >> kRadixShift0, e);
     }
+  }
+  if (c == 0 && tid == 0) {
+    if (s.per_seq) {
+      for (int g = 0; g < a.H_kv; ++g) a.count[s.b * a.H_kv + g] = s.keff;
+    } else {
+      a.count[s.u] = s.keff;
+    }
+  }
+  if (s.need_radix) {
+    __syncthreads();
+    uint32_t* gh = a.sel_hist + size_t(s.u) * kRadixBins;
+    for (int i = tid; i < kRadixBins; i += kSelT)
+      if (hist[i]) atomicAdd(gh + i, hist[i]);
+  }
+}
+
+// Address of entry e (chunks in order, each in position order) of the
+// unit's list, given the chunks' exclusive entry offsets offs[0..C].
+__device__ __forceinline__ size_t sel_entry(const SelUnit& s, const uint32_t* offs, int C,
+                                            uint32_t e, size_t row0) {
+  int lo = 0, hi = C - 1;  // largest c with offs[c] <= e: the chunk holding e
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (offs[mid] <= e) lo = mid;
+    else hi = mid - 1;
+  }
+  return row0 + size_t(sel_chunk_e0(s, lo)) + (e - offs[lo]);
+}
+
+// Launch 3: per chunk, the ordered list of keys at or above the k-th key's
+// top digit; the unit's last chunk CTA to finish completes the selection.
+__global__ void __launch_bounds__(kSelT) sel_list_kernel(const SelectArgs a) {
+  __shared__ uint32_t hist[kRadixBins];
+  __shared__ uint32_t cand[kCandCap];
+  __shared__ uint32_t offs[kSelMaxChunks + 1];
+  __shared__ uint32_t scan_sh[33];
+  __shared__ uint32_t sh_digit, sh_above, sh_last, cand_n;
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, c = blockIdx.x, C = gridDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  SelUnit s;
+  if (sel_unit(a, blockIdx.y, c, C, s) != 0 || !s.need_radix) return;  // uniform over the unit
+  uint32_t* gh = a.sel_hist + size_t(s.u) * kRadixBins;
+  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = __ldcg(gh + i);
+  __syncthreads();
+  block_pick_digit<kRadixBins>(hist, uint32_t(s.keff), &sh_digit, &sh_above, scan_sh);
+  const uint32_t d0 = sh_digit;
+  uint32_t krem = uint32_t(s.keff) - sh_above;
+  const uint32_t n_cand = hist[d0];
+  // ---- this chunk's keys at or above d0, in position order, into its own
+  // region of the unit's list (starting at its first position of E).  Tiles
+  // of kSelT * kRun positions; thread t takes kRun consecutive positions of a
+  // tile, all loaded before any is used; one block scan per tile.
+  const uint32_t* krow = a.sel_keys + size_t(s.u) * a.max_len;
+  const size_t row0 = size_t(s.u) * a.max_len;
+  unsigned long long* lrow = a.sel_list + row0 + s.e0;
+  uint32_t tot = 0;
+  for (int tb = s.e0; tb < s.e1; tb += kSelT * kRun) {
+    const int i0 = tb + tid * kRun;
+    uint32_t key[kRun];
+    uint32_t nm = 0;
+#pragma unroll
+    for (int j = 0; j < kRun; ++j) key[j] = i0 + j < s.e1 ? krow[i0 + j] : 0u;
+#pragma unroll
+    for (int j = 0; j < kRun; ++j) nm += (i0 + j < s.e1 && (key[j] >> kRadixShift0) >= d0) ? 1u : 0u;
+    uint32_t ttot;
+    uint32_t at = tot + block_excl_scan(nm, scan_sh, ttot);
+#pragma unroll
+    for (int j = 0; j < kRun; ++j)
+      if (i0 + j < s.e1 && (key[j] >> kRadixShift0) >= d0)
+        lrow[at++] = (static_cast<unsigned long long>(key[j]) << 32) | uint32_t(i0 + j);
+    tot += ttot;
+  }
+  if (tid == 0) a.sel_cnt[size_t(s.u) * kSelMaxChunks + c] = tot;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh_last = atomicAdd(a.sel_done + s.u, 1u) == uint32_t(C - 1);
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+
+  // ---------------------------------------------------------------- finisher
+  // exclusive entry offsets of the chunks (warp 0, two chunks per lane)
+  if (warp == 0) {
+    const uint32_t* pc = a.sel_cnt + size_t(s.u) * kSelMaxChunks;
+    const uint32_t x0 = lane < C ? __ldcg(pc + lane) : 0u;
+    const uint32_t x1 = lane + 32 < C ? __ldcg(pc + lane + 32) : 0u;
+    uint32_t i0 = x0, i1 = x1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
+      if (lane >= o) i0 += y0, i1 += y1;
+    }
+    const uint32_t t0 = __shfl_sync(kFull, i0, 31);
+    offs[lane] = i0 - x0;
+    offs[lane + 32] = t0 + i1 - x1;
+    if (lane == 31) offs[kSelMaxChunks] = t0 + i1;
+    if (lane == 0) cand_n = 0;
   }
   __syncthreads();
-
-  int32_t* out_idx = a.idx + size_t(per_seq ? b * a.H_kv : unit) * a.k;
-  if (need_radix) {
-    // ------------------------------------------------------------ radix select
-    // Digits of 11, 11 and 10 bits of the order keys of E.  Pass 0's
-    // histogram was built with the scores; its cluster total gives the top
-    // digit d0 of the k-th key.  Few keys share that digit (at the decode
-    // workloads about 2% of E), so when at most kCandCap do, each CTA lists
-    // its keys of bin d0 and rank 0 finishes the two lower digits on the
-    // gathered list alone; otherwise every CTA runs the two passes over all
-    // its keys.  Shared-memory reads go 8 positions per thread (two 16-byte
-    // loads) in tiles aligned to the CTA's first position.
-    uint32_t prefix = 0, krem = uint32_t(keff);
-    const int e0 = max(p0, lo), e1 = min(p1, hi);
-    for (int i = tid; i < kRadixBins; i += kSelCT) {
-      hist_loc[i] = hist[i];
-      if (hist[i]) atomicAdd(cl.map_shared_rank(&hist_g[0][i], 0), hist[i]);
+  const uint32_t NE = offs[C];  // chunks past C count 0, so this is the total
+  // ---- the keys of bin d0, gathered in shared memory when they fit
+  const bool in_smem = n_cand <= uint32_t(kCandCap);
+  if (in_smem) {
+    for (uint32_t tb = 0; tb < NE; tb += kSelT * kRun) {
+      uint32_t key[kRun];
+#pragma unroll
+      for (int j = 0; j < kRun; ++j) {
+        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
+        key[j] = e < NE ? uint32_t(__ldcg(a.sel_list + sel_entry(s, offs, C, e, row0)) >> 32) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < kRun; ++j) {
+        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
+        const bool m = e < NE && (key[j] >> kRadixShift0) == d0;
+        const unsigned bal = __ballot_sync(kFull, m);
+        if (bal) {
+          uint32_t b0 = 0;
+          if (lane == 0) b0 = atomicAdd(&cand_n, uint32_t(__popc(bal)));
+          b0 = __shfl_sync(kFull, b0, 0);
+          const uint32_t at_c = b0 + __popc(bal & lt);
+          if (m && at_c < uint32_t(kCandCap)) cand[at_c] = key[j];
+        }
+      }
     }
-    if (tid == 0) cand_n = 0;
-    cl.sync();
-    for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = *cl.map_shared_rank(&hist_g[0][i], 0);
     __syncthreads();
-    block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
-    const uint32_t d0 = sh_digit;
-    prefix = d0;
+  }
+  const uint32_t n_in = min(cand_n, uint32_t(kCandCap));  // == n_cand
+  // ---- the two lower digits (11 and 10 bits) among the keys of bin d0; with
+  // more than kCandCap of them, the passes read the list itself
+  uint32_t prefix = d0;
+  for (int pass = 1; pass < 3; ++pass) {
+    const int shift = pass == 1 ? kRadixShift1 : 0;
+    const int width = pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1;
+    const uint32_t dmask = (1u << width) - 1u;
+    const int hs = shift + width;
+    for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
+    __syncthreads();
+    const uint32_t n_it = in_smem ? n_in : NE;
+    for (uint32_t tb = 0; tb < n_it; tb += kSelT * kRun) {
+      uint32_t key[kRun];
+#pragma unroll
+      for (int j = 0; j < kRun; ++j) {
+        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
+        key[j] = e >= n_it ? 0u
+                 : in_smem ? cand[e]
+                           : uint32_t(__ldcg(a.sel_list + sel_entry(s, offs, C, e, row0)) >> 32);
+      }
+#pragma unroll
+      for (int j = 0; j < kRun; ++j) {
+        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
+        hist_add(hist, (key[j] >> shift) & dmask, e < n_it && (key[j] >> hs) == prefix);
+      }
+    }
+    __syncthreads();
+    if (width == 11) block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
+    else block_pick_digit<1024>(hist, krem, &sh_digit, &sh_above, scan_sh);
+    prefix = (prefix << width) | sh_digit;
     krem -= sh_above;
-    const uint32_t n_cand = hist[d0];  // keys of E with top digit d0, cluster-wide
-    uint32_t tau, take_eq;
-    if (n_cand <= uint32_t(kCandCap)) {
-      // ---- this CTA's keys of bin d0: into its own list and, at offset
-      // (keys of bin d0 in lower ranks), into rank 0's gathered list (the
-      // rows 1-2 of its total histograms, unused on this path)
-      const int lane = tid & 31;
-      if (tid < 32) {
-        uint32_t v = tid < rank ? *cl.map_shared_rank(&hist_loc[d0], tid) : 0u;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-        if (tid == 0) sh_off = v;
-      }
-      __syncthreads();
-      const uint32_t my_off = sh_off;
-      uint32_t* all_r0 = cl.map_shared_rank(&hist_g[1][0], 0);
-      for (int tb = p0; tb < e1; tb += kSelCT * 8) {
-        const int i0 = tb + tid * 8;
-        float v8[8];
-        load8(sc, i0 - p0, p1 - p0, v8);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + j;
-          const uint32_t key = order_key(v8[j]);
-          const bool m = i >= e0 && i < e1 && (key >> kRadixShift0) == d0;
-          const unsigned bal = __ballot_sync(kFull, m);
-          if (bal) {
-            uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(&cand_n, uint32_t(__popc(bal)));
-            base = __shfl_sync(kFull, base, 0);
-            if (m) {
-              const uint32_t at = base + __popc(bal & ((1u << lane) - 1u));
-              cand[at] = key;
-              all_r0[my_off + at] = key;
-            }
-          }
-        }
-      }
-      cl.sync();  // every CTA's list is complete
-      if (rank == 0) {
-        const uint32_t* all = &hist_g[1][0];  // the n_cand gathered keys
-        for (int pass = 1; pass < kRadixPasses; ++pass) {
-          const int shift = pass == 1 ? kRadixShift1 : 0;
-          const int width = pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1;
-          const uint32_t dmask = (1u << width) - 1u;
-          const int hs = shift + width;
-          for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = 0;
-          __syncthreads();
-          for (uint32_t j0 = 0; j0 < n_cand; j0 += kSelCT) {
-            const uint32_t j = j0 + tid;
-            const uint32_t key = j < n_cand ? all[j] : 0u;
-            hist_add(hist, (key >> shift) & dmask, j < n_cand && (key >> hs) == prefix);
-          }
-          __syncthreads();
-          if (width == 11) block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
-          else block_pick_digit<1024>(hist, krem, &sh_digit, &sh_above, scan_sh);
-          prefix = (prefix << width) | sh_digit;
-          krem -= sh_above;
-        }
-        if (tid == 0) {
-          sh_tau = prefix;
-          sh_take = krem;
-        }
-      }
-      cl.sync();  // tau is known in rank 0; no list is read any more
-      tau = *cl.map_shared_rank(&sh_tau, 0);
-      take_eq = *cl.map_shared_rank(&sh_take, 0);
-    } else {
-      for (int pass = 1; pass < kRadixPasses; ++pass) {
-        const int shift = pass == 1 ? kRadixShift1 : 0;
-        const int width = pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1;
-        const uint32_t dmask = (1u << width) - 1u;
-        const int hs = shift + width;
-        for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = 0;
-        __syncthreads();
-        for (int tb = p0; tb < e1; tb += kSelCT * 8) {
-          const int i0 = tb + tid * 8;
-          float v8[8];
-          load8(sc, i0 - p0, p1 - p0, v8);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int i = i0 + j;
-            const uint32_t key = order_key(v8[j]);
-            const bool m = i >= e0 && i < e1 && (key >> hs) == prefix;
-            hist_add(hist, (key >> shift) & dmask, m);
-          }
-        }
-        __syncthreads();
-        for (int i = tid; i < kRadixBins; i += kSelCT)
-          if (hist[i]) atomicAdd(cl.map_shared_rank(&hist_g[pass][i], 0), hist[i]);
-        cl.sync();
-        for (int i = tid; i < kRadixBins; i += kSelCT) hist[i] = *cl.map_shared_rank(&hist_g[pass][i], 0);
-        __syncthreads();
-        if (width == 11) block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
-        else block_pick_digit<1024>(hist, krem, &sh_digit, &sh_above, scan_sh);
-        prefix = (prefix << width) | sh_digit;
-        krem -= sh_above;
-      }
-      tau = prefix;
-      take_eq = krem;
-    }
-    // ------------------------------------------------------------ compaction
-    // Ascending positions: warp w walks the contiguous segment
-    // [e0 + w * seg, ...) 32 positions per step (lane l takes base + l), so
-    // the order is (rank, warp, step, lane).  A counting walk, one block scan
-    // of the warps' counts and an exchange of the CTAs' totals give every
-    // warp its first output slot.
-    constexpr int NW = kSelCT / 32;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int ne_cta = max(e1 - e0, 0);
-    const int seg = ((ne_cta + NW - 1) / NW + 31) / 32 * 32;
-    const int s0 = min(e1, e0 + warp * seg), s1 = min(e1, s0 + seg);
-    uint32_t wg = 0, wq = 0;
-    for (int base = s0; base < s1; base += 32) {
-      const int i = base + lane;
-      const uint32_t key = i < s1 ? order_key(sc[i - p0]) : 0u;
-      wg += __popc(__ballot_sync(kFull, i < s1 && key > tau));
-      wq += __popc(__ballot_sync(kFull, i < s1 && key == tau));
-    }
-    uint32_t tot;
-    const uint32_t ex = block_excl_scan(lane == 0 ? (wg << 16) | wq : 0u, scan_sh, tot);  // < 2^16 per CTA
-    const uint32_t w_ex = __shfl_sync(kFull, ex, 0);
-    if (tid == 0) {
-      cnt_gt = tot >> 16;
-      cnt_eq = tot & 0xffffu;
-    }
-    cl.sync();
-    uint32_t gb = w_ex >> 16, qb = w_ex & 0xffffu;
-    for (int r = 0; r < rank; ++r) {
-      gb += *cl.map_shared_rank(&cnt_gt, r);
-      qb += *cl.map_shared_rank(&cnt_eq, r);
-    }
-    const unsigned lt = (1u << lane) - 1u;
-    for (int base = s0; base < s1; base += 32) {
-      const int i = base + lane;
-      const uint32_t key = i < s1 ? order_key(sc[i - p0]) : 0u;
-      const unsigned bg = __ballot_sync(kFull, i < s1 && key > tau);
-      const unsigned bq = __ballot_sync(kFull, i < s1 && key == tau);
-      const uint32_t g_at = gb + __popc(bg & lt), q_at = qb + __popc(bq & lt);
-      if ((bg >> lane) & 1u) {
-        out_idx[g_at + min(q_at, take_eq)] = i;
-      } else if (((bq >> lane) & 1u) && q_at < take_eq) {
-        out_idx[g_at + q_at] = i;
-      }
-      gb += __popc(bg);
-      qb += __popc(bq);
-    }
-  } else {
-    // keep all of E (or nothing): position lo + j goes to slot j
-    const int e0 = max(p0, lo), e1 = min(min(p1, hi), lo + keff);
-    for (int i = e0 + tid; i < e1; i += kSelCT) out_idx[i - lo] = i;
   }
-  if (tid == 0 && rank == 0) {
-    if (per_seq) {
-      for (int g = 0; g < a.H_kv; ++g) a.count[b * a.H_kv + g] = keff;
-    } else {
-      a.count[u] = keff;
+  const uint32_t tau = prefix, take_eq = krem;
+  // ---- ordered output: the keys above tau, then the first take_eq keys
+  // equal to it; entry e goes to slot (keys above tau before it) +
+  // min(keys equal to tau before it, take_eq).  Eight consecutive entries per
+  // thread, one block scan per tile of kSelT * 8 entries.
+  int32_t* out_idx = a.idx + size_t(s.per_seq ? s.b * a.H_kv : s.unit) * a.k;
+  const int n_rows = s.per_seq ? a.H_kv : 1;
+  uint32_t g_run = 0, q_run = 0;
+  for (uint32_t tb = 0; tb < NE; tb += kSelT * 8) {
+    const uint32_t ea = tb + uint32_t(tid) * 8;
+    unsigned long long ent[8];
+    uint32_t ng = 0, nq = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool v = ea + j < NE;
+      ent[j] = v ? __ldcg(a.sel_list + sel_entry(s, offs, C, ea + j, row0)) : 0ull;
+      const uint32_t key = uint32_t(ent[j] >> 32);
+      ng += (v && key > tau) ? 1u : 0u;
+      nq += (v && key == tau) ? 1u : 0u;
     }
+    uint32_t ttot;
+    const uint32_t ex = block_excl_scan((ng << 16) | nq, scan_sh, ttot);  // < 2^16 per tile
+    uint32_t gb = g_run + (ex >> 16), qb = q_run + (ex & 0xffffu);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (ea + j < NE) {
+        const uint32_t key = uint32_t(ent[j] >> 32);
+        const int pos = int(uint32_t(ent[j]));
+        // slots stay below keff for the counts above; the bound only guards
+        // the output row against an inconsistent list
+        if (key > tau) {
+          const uint32_t slot = gb + min(qb, take_eq);
+          if (slot < uint32_t(s.keff))
+            for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + slot] = pos;
+          ++gb;
+        } else if (key == tau) {
+          if (qb < take_eq && gb + qb < uint32_t(s.keff))
+            for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + gb + qb] = pos;
+          ++qb;
+        }
+      }
+    }
+    g_run += ttot >> 16;
+    q_run += ttot & 0xffffu;
   }
-  cl.sync();  // every CTA's set is written, and no CTA leaves while others read its memory
-  if (per_seq && a.H_kv > 1) {
-    // every KV head of the sequence reads the same set; CTA `rank` copies its share
-    const int cs = (keff + kSelCluster - 1) / kSelCluster;
-    const int j0 = rank * cs, j1 = min(keff, j0 + cs);
-    for (int g = 1; g < a.H_kv; ++g)
-      for (int j = j0 + tid; j < j1; j += kSelCT) out_idx[size_t(g) * a.k + j] = out_idx[j];
-  }
+  // leave the histogram and the counter at zero for the next launch
+  for (int i = tid; i < kRadixBins; i += kSelT) gh[i] = 0u;
+  if (tid == 0) a.sel_done[s.u] = 0u;
 }
 
 cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st) {
@@ -578,30 +594,46 @@ cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Dynamic shared memory of a launch; the key-norm copy is kept when the CTA's
-// total stays within 227 KB (the static part is about 41 KB).
-size_t select_smem_bytes(int max_len, bool kn_smem) {
-  const size_t base = select_kn_offset(max_len);
-  return kn_smem ? base + size_t((max_len + kSelCluster - 1) / kSelCluster) * sizeof(float) : base;
+// Chunks per unit: about two CTAs per SM over all selecting units, chunks of
+// at least kSelMinChunk positions, at most kSelMaxChunks.
+int select_chunks(int units, int max_len) {
+  const int sms = device_sm_count();
+  int C = (2 * sms + units - 1) / units;
+  C = min(C, kSelMaxChunks);
+  C = min(C, max(1, (max_len + kSelMinChunk - 1) / kSelMinChunk));
+  return max(C, 1);
 }
 
-bool select_kn_fits(int max_len) { return select_smem_bytes(max_len, true) <= size_t(180) * 1024; }
+template <typename K>
+cudaError_t launch_dependent(K kernel, dim3 grid, int threads, cudaStream_t st,
+                             const SelectArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
 template <int EV_G>
-cudaError_t launch_select_t(const SelectArgs& args, cudaStream_t st) {
-  SelectArgs a = args;
-  a.kn_smem = a.mode == SFI_SELECT_FUSED && select_kn_fits(a.max_len) ? 1 : 0;
-  const size_t smem = select_smem_bytes(a.max_len, a.kn_smem != 0);
-  cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel<EV_G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e != cudaSuccess) return e;
+cudaError_t launch_select_t(const SelectArgs& a, cudaStream_t st) {
   int n_active = 0;
   for (int b = 0; b < a.B; ++b) n_active += int((a.active.bits[b >> 5] >> (b & 31)) & 1u);
-  const bool one_unit = a.mode == SFI_SELECT_LOGIT_SUM_SEQ || (a.mode == SFI_SELECT_FUSED && a.g_only >= 0);
+  const bool one_unit =
+      a.mode == SFI_SELECT_LOGIT_SUM_SEQ || (a.mode == SFI_SELECT_FUSED && a.g_only >= 0);
   const int units = n_active * (one_unit ? 1 : a.H_kv);
   if (units == 0) return cudaSuccess;
-  select_cluster_kernel<EV_G><<<units * kSelCluster, kSelCT, smem, st>>>(a);
-  return cudaGetLastError();
+  const dim3 grid(select_chunks(units, a.max_len), units);
+  cudaError_t e = cudaSuccess;
+  if (a.mode == SFI_SELECT_FUSED) e = launch_dependent(sel_nu_kernel, grid, kSelNuT, st, a);
+  if (e == cudaSuccess) e = launch_dependent(sel_score_kernel<EV_G>, grid, kSelT, st, a);
+  if (e == cudaSuccess) e = launch_dependent(sel_list_kernel, grid, kSelT, st, a);
+  return e;
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {

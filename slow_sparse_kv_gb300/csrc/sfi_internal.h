@@ -39,6 +39,10 @@ struct AttnArgs {
   float* out;     // [B][H_q][D]
   float* logits;  // [B*H_kv][max_len][G], log2-scaled logits of slow units (emit)
   float* knorm;   // [B*H_kv][max_len] key norms of slow units (nullable)
+  // optional [B*H_kv]: rows below knorm_valid[u] already have their key norms
+  // in knorm (a cache row never changes); a slow unit computes the rest and
+  // sets it to its length
+  int32_t* knorm_valid;
   float* stats;   // [B*H_q][2]: (max log2-logit, sum of 2^(l - max)) of slow units
   const int32_t* idx;    // [B*H_kv][idx_stride] selected positions (fast units)
   const int32_t* count;  // [B*H_kv]
@@ -47,6 +51,10 @@ struct AttnArgs {
   int32_t window;
   int32_t B, H_q, H_kv, max_len;
   int32_t rpi_slow, rpi_fast;  // rows per work item of slow and of fast units
+  // > 0: no slow unit in the launch and every unit has exactly this many
+  // items (its rows dealt over them; items past a short unit's rows are
+  // empty); the kernel then builds no unit table
+  int32_t fast_items;
   int32_t max_items;
   int32_t emit;    // slow units write logits, stats (and knorm if non-null)
   float qscale;    // log2(e) / sqrt(D)
@@ -71,7 +79,8 @@ struct FpassArgs {
   uint32_t* status;
 };
 
-constexpr int kSelectMaxLen = 327680;  // per-position rows the cluster selector holds in shared memory
+constexpr int kSelectMaxLen = 327680;  // positions per row a selection takes (documented limit)
+constexpr int kSelMaxChunks = 64;      // chunk CTAs per selecting unit, at most
 
 struct SelectArgs {
   const float* evidence;  // f (fused mode) or per-KV-head logit sums (logit-sum mode)
@@ -89,7 +98,13 @@ struct SelectArgs {
   int32_t mode;
   SeqMask active;
   uint32_t* status;
-  int32_t kn_smem;  // set by the launcher: the CTAs keep their key norms in shared memory
+  // selector scratch (workspace), rows indexed like the per-position arrays
+  float* sel_nu;                 // [B*H_kv][kSelMaxChunks] chunk sums of key norms over E
+  uint32_t* sel_cnt;             // [B*H_kv][kSelMaxChunks] list entries per chunk
+  uint32_t* sel_hist;            // [B*H_kv][2048] top-digit histogram, zero between launches
+  uint32_t* sel_done;            // [B*H_kv] chunk CTAs finished, zero between launches
+  uint32_t* sel_keys;            // [B*H_kv][max_len] order keys of the ranked scores
+  unsigned long long* sel_list;  // [B*H_kv][max_len] (key << 32 | position) entries
   // Cross-head exclusivity (fused mode): the ranked score of position i is
   // s_i * exp(-excl_beta * excl[b][i]) when excl is set ([B][max_len] counts).
   const uint8_t* excl;
@@ -112,11 +127,16 @@ int verify_stage_rows();
 
 // Workspace plan: one layout serves every call of a given geometry.
 struct WsPlan {
-  size_t status_off, counters_off, partials_off, logits_off, stats_off, s_off, total;
+  size_t status_off, counters_off, partials_off, logits_off, stats_off, s_off;
+  size_t sel_nu_off, sel_cnt_off, sel_hist_off, sel_done_off, sel_keys_off, sel_list_off;
+  size_t total;
   int32_t max_items;
 };
 
 WsPlan plan_workspace(int B, int H_q, int H_kv, int D, int max_len);
+
+// Point the selector's scratch fields of `a` into workspace `ws` laid out by `p`.
+void attach_select_scratch(SelectArgs& a, char* ws, const WsPlan& p);
 
 // Kernel launchers (return the CUDA error of the launch).
 cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st);

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
   unsigned first_id = 0;
   const bool fetcher = warp == C::NCW && lane == 0;
   if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
-  const bool units_fit = attn_build_units<C::NT>(a, units, n_units, misc);
+  const bool units_fit = attn_build_units<C::NT>(a, units, n_units, misc);  // fast_items is 0
   const int total = units[n_units];
   if (total > a.max_items || !units_fit) {
     if (tid == 0 && blockIdx.x == 0) set_status(a.status, SFI_DEV_ITEMS_OVERFLOW);

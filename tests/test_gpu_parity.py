@@ -338,3 +338,37 @@ def test_select_top_bin_over_candidate_cap(sfi):
         check_selection(sel, s_ref[g], lo, hi, k)
         assert np.array_equal(sel, O.top_k(s_gpu[0, g].astype(np.float64), lo, hi, k))
     assert np.array_equal(idx[0, 1, :k], np.arange(lo, lo + k))
+
+
+def test_fast_only_launch_short_units(sfi):
+    """A launch of fast units only deals each unit's rows over the items of the
+    row bound n_sink + k + window; units with far fewer rows (|E| < k, or E
+    empty) leave some of their items without rows, and those must weigh
+    nothing in the merge.  Lengths 6000, 300 and 40 with k = 1500: 25, 5 and
+    1 stages of rows against a bound of 25."""
+    B, hq, hkv, d, ns, win, k = 3, 32, 8, 128, 4, 64, 1500
+    lens = [6000, 300, 40]
+    wl = W.small(B, hq, hkv, d, "bf16", lens, 23, n_sink=ns, window=win, k=k)
+    dl = DeviceLayer.build(wl)
+    lay = dl.layout(sfi, lens)
+    ws = sfi.alloc_workspace(lay)
+    qd, q64 = dl.queries(0)
+    rng = np.random.default_rng(23)
+    idx = np.zeros((B, hkv, k), np.int32)
+    cnt = np.zeros((B, hkv), np.int32)
+    for b in range(B):
+        lo, hi = O.eligible_range(lens[b], ns, win)
+        ke = max(0, min(k, hi - lo))
+        for g in range(hkv):
+            idx[b, g, :ke] = np.sort(rng.choice(np.arange(lo, hi), size=ke, replace=False)) if ke else []
+            cnt[b, g] = ke
+    out = torch.full((B, hq, d), float("nan"), device="cuda")
+    sfi.sfi_fast_attn(lay, sfi.params(ns, win, k, wl.lam), qd, dl.k, dl.v, torch.from_numpy(idx).cuda(),
+                      torch.from_numpy(cnt).cuda(), out, ws)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws) == 0
+    out = out.cpu().numpy()
+    for b in range(B):
+        exp = O.fast_step(q64[b], dl.K64[b], dl.V64[b], lens[b],
+                          [idx[b, g, :cnt[b, g]].astype(np.int64) for g in range(hkv)], ns, win)
+        assert max_abs(out[b], exp) <= O_TOL["bf16"], (b, max_abs(out[b], exp))
