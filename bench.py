@@ -135,66 +135,138 @@ def attention_bytes(wl: W.Workload, slow_masks: np.ndarray) -> float:
 
 # ---------------------------------------------------------------- CPU oracle leg
 
-def _cpu_unit_worker(args):
-    """Time the fp64 oracle on one (sequence, layer, KV head) unit: slow steps
-    and fast steps at the workload's length, for about `budget_s` seconds."""
-    n, G, d, k, ns, win, lam, budget_s, seed = args
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _unit_server(conn, wl, layer, b, g):
+    """One single-threaded oracle process for one (layer, sequence, KV head)
+    unit of the seeded workload: it generates the unit's stored K and V rows
+    (the bf16 bytes the GPU reads, as exact fp64) and then runs slices of
+    the unit's decode loop on request, timing each step."""
+    for k_ in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k_] = "1"
     import time as _t
     import numpy as _np
     from oracle import sfi_oracle as O
-    rng = _np.random.default_rng(seed)
-    K = rng.standard_normal((1, n + 8, d)).astype(_np.float32).astype(_np.float64)
-    V = rng.standard_normal((1, n + 8, d)).astype(_np.float32).astype(_np.float64)
-    q = rng.standard_normal((G, d))
-    ts, tf = [], []
-    idx = None
-    t_end = _t.perf_counter() + budget_s
-    while not ts or (_t.perf_counter() < t_end and len(ts) < 50):
-        t0 = _t.perf_counter()
-        st = O.slow_step(q, K, V, n, ns, win, k, lam)
-        ts.append(_t.perf_counter() - t0)
-        idx = st["idx"]
-        for j in range(4):
-            t0 = _t.perf_counter()
-            O.fast_step(q, K, V, n + 1 + j, idx, ns, win)
-            tf.append(_t.perf_counter() - t0)
-    return float(_np.mean(ts)), float(_np.mean(tf)), len(ts), len(tf)
-
-
-def cpu_oracle_rate(wl: W.Workload, slow_frac: float, budget_s: float = 2.0, workers=None):
-    """Decode steps/s of the fp64 oracle on the host: every worker process is
-    single-threaded and times (sequence, layer, KV head) units; the job rate is
-    the pool's unit throughput divided by the units of one decode step."""
     sh = wl.shape
-    P = workers or max(1, min(16, os.cpu_count() or 1))
-    n = wl.n0[0]
-    env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
-    for k_ in env_keep:
-        os.environ[k_] = "1"
-    try:
-        ctx = mp.get_context("spawn")
-        with ctx.Pool(P) as pool:
-            args = [(n, sh.group, sh.head_dim, wl.k, wl.n_sink, wl.window, wl.lam, budget_s, 17 + i)
-                    for i in range(P)]
-            t0 = time.perf_counter()
-            res = pool.map(_cpu_unit_worker, args)
-            wall = time.perf_counter() - t0
-    finally:
-        for k_, v_ in env_keep.items():
-            if v_ is None:
-                os.environ.pop(k_, None)
+    G = sh.group
+    K = W.storage_to_f64(wl.kv_storage("k", layer, b, g=g), sh.dtype)[None]
+    V = W.storage_to_f64(wl.kv_storage("v", layer, b, g=g), sh.dtype)[None]
+    slow = O.schedule(wl.boundary_trace(), wl.budget)[:, b]
+    idx = None
+    conn.send("ready")
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            break
+        t0, t1 = msg
+        ts, tf = [], []
+        for t in range(t0, t1):
+            q = W.storage_to_f64(wl.q_storage(layer, t, b), sh.dtype)[g * G:(g + 1) * G]
+            n = wl.n0[b] + t
+            c0 = _t.perf_counter()
+            if slow[t] or idx is None:
+                idx = O.slow_step(q, K, V, n, wl.n_sink, wl.window, wl.k, wl.lam)["idx"]
+                ts.append(_t.perf_counter() - c0)
             else:
-                os.environ[k_] = v_
-    t_slow = float(np.mean([r[0] for r in res]))
-    t_fast = float(np.mean([r[1] for r in res]))
+                O.fast_step(q, K, V, n, idx, wl.n_sink, wl.window)
+                tf.append(_t.perf_counter() - c0)
+        conn.send((ts, tf))
+
+
+class OraclePool:
+    """Persistent single-threaded oracle processes, one per (sequence, KV
+    head) unit of layer 0 (sequences 0, 1, ... in order), at most one per
+    host core."""
+
+    def __init__(self, wl: W.Workload, workers=None):
+        sh = wl.shape
+        units = sh.batch * sh.n_kv_heads
+        self.P = max(1, min(workers or (os.cpu_count() or 1), units))
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for i in range(self.P):
+            a, b_ = ctx.Pipe()
+            pr = ctx.Process(target=_unit_server, args=(b_, wl, 0, i // sh.n_kv_heads, i % sh.n_kv_heads),
+                             daemon=True)
+            pr.start()
+            self.conns.append(a)
+            self.procs.append(pr)
+        for c in self.conns:
+            assert c.recv() == "ready"
+        self.wl = wl
+
+    def run(self, t0: int, t1: int):
+        for c in self.conns:
+            c.send((t0, t1))
+        res = [c.recv() for c in self.conns]
+        ts = [x for r in res for x in r[0]]
+        tf = [x for r in res for x in r[1]]
+        return ts, tf
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except Exception:
+                pass
+        for pr in self.procs:
+            pr.join(timeout=10)
+
+
+def oracle_rates(wl: W.Workload, slow_frac: float, ts, tf, P: int):
+    """Decode steps/s of the job on P cores and on one core, from mean unit
+    step times: one decode step is n_layers x batch x n_kv_heads units, a
+    fraction slow_frac of them slow."""
+    sh = wl.shape
+    t_slow = float(np.mean(ts)) if ts else 0.0
+    t_fast = float(np.mean(tf)) if tf else 0.0
     units_per_step = wl.n_layers * sh.batch * sh.n_kv_heads
     t_step_one_core = units_per_step * (slow_frac * t_slow + (1 - slow_frac) * t_fast)
-    rate = P / t_step_one_core
-    sample = (f"{sum(r[2] for r in res)} slow + {sum(r[3] for r in res)} fast (sequence, layer, "
-              f"KV-head) unit steps at n={n}, G={sh.group}, d={sh.head_dim}, k={wl.k} "
-              f"(random bf16-valued inputs) on {P} single-threaded processes in {wall:.1f} s; "
-              f"scaled by {units_per_step} units per decode step and slow fraction {slow_frac:.4f}")
-    return rate, P, sample, t_slow, t_fast
+    return P / t_step_one_core, 1.0 / t_step_one_core, t_slow, t_fast, units_per_step
+
+
+def cpu_oracle_rate(wl: W.Workload, slow_frac: float, workers=None):
+    """The fp64 oracle on the host cores: one process per (sequence, KV head)
+    unit of layer 0 (as many as there are cores) runs that unit's whole
+    decode loop on the seeded workload; the job rate scales the mean slow and
+    fast unit-step times to every unit of a decode step."""
+    t_start = time.perf_counter()
+    pool = OraclePool(wl, workers)
+    gen_s = time.perf_counter() - t_start
+    try:
+        t0 = time.perf_counter()
+        ts, tf = pool.run(0, wl.n_steps)
+        wall = time.perf_counter() - t0
+    finally:
+        pool.close()
+    rate, rate1, t_slow, t_fast, ups = oracle_rates(wl, slow_frac, ts, tf, pool.P)
+    sh = wl.shape
+    sample = (f"layer 0, sequences 0..{(pool.P - 1) // sh.n_kv_heads}: {pool.P} (sequence, KV head) units "
+              f"of the seeded bf16 workload, each its whole {wl.n_steps}-step decode loop "
+              f"({len(ts)} slow + {len(tf)} fast unit steps at n={wl.n0[0]}..{wl.n0[0] + wl.n_steps - 1}, "
+              f"G={sh.group}, d={sh.head_dim}, k={wl.k}) on {pool.P} single-threaded processes in "
+              f"{wall:.1f} s (+{gen_s:.1f} s generating the inputs); scaled by {ups} units per decode "
+              f"step and slow fraction {slow_frac:.4f}")
+    return rate, pool.P, sample, dict(value_1core=rate1, t_slow_s=t_slow, t_fast_s=t_fast,
+                                      cpu_model=cpu_model(), nproc=os.cpu_count())
 
 
 # ---------------------------------------------------------------- clocks
@@ -584,9 +656,13 @@ def run_ours(args, rank, world, local_rank):
     if clk:
         line["clocks"] = clk
     if rank == 0 and not args.no_cpu_baseline:
-        rate, P, sample, ts, tf = cpu_oracle_rate(wl, slow_frac, budget_s=args.cpu_budget)
+        rate, P, sample, extra = cpu_oracle_rate(wl, slow_frac)
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "decode steps/s", "cores": P,
-                                "kind": "oracle", "sample": sample}
+                                "kind": "oracle", "sample": sample,
+                                "value_1core": round(extra["value_1core"], 7),
+                                "cpu_model": extra["cpu_model"], "host_cores": extra["nproc"],
+                                "unit_step_s": {"slow": round(extra["t_slow_s"], 4),
+                                                "fast": round(extra["t_fast_s"], 5)}}
     return line
 
 
@@ -793,32 +869,190 @@ def run_ragged_sweep(args):
             "contexts": lens, "kv_gb": round(sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9, 2)}
 
 
+def run_config_table(args):
+    """Every workload of the build on one GPU, beside the fp64 oracle on the
+    host cores, for the results table: the decode loops of the 2K fp32
+    layer (cfg0) and the 32K layer (cfg1) through the decode driver, the
+    Vegas verify + selection + draft steps (cfg3), and the oracle's unit-step
+    times.  The 128K decode benchmark (cfg2) is the default bench line; the
+    ragged batch (cfg4) is --ragged-sweep.  One JSON line per workload."""
+    import torch
+    from oracle import sfi_oracle as O
+    peak, _ = measured_peak_gbs()
+    out = []
+    for name, mk in (("cfg0", W.cfg0), ("cfg1", W.cfg1)):
+        wl = mk()
+        R = Cfg2Runner(wl, 0, async_select=False)
+        for _ in range(2):
+            R.decode_pass()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(max(3, args.steps)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            R.decode_pass()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        R.ctx.profile(True)
+        R.decode_pass()
+        torch.cuda.synchronize()
+        a_ms, a_n, s_ms, s_n = R.ctx.profile_read()
+        R.ctx.profile(False)
+        masks = R.slow_masks
+        alg = attention_bytes(wl, masks)
+        sh = wl.shape
+        row = 2 * sh.n_kv_heads * sh.head_dim * sh.esize
+        slow_bytes = wl.n0[0] * row
+        frac = float(masks.mean())
+        rate, P, sample, extra = cpu_oracle_rate(wl, frac)
+        line = {"workload": wl.name, "config": name, "gpu": {
+            "decode_steps_per_s": round(wl.n_steps / (ms / 1e3), 1),
+            "tokens_per_s": round(sh.batch * wl.n_steps / (ms / 1e3), 1),
+            "ms_per_loop": round(ms, 4), "steps_per_loop": wl.n_steps,
+            "slow_steps": int(masks.sum()), "attention_launches": a_n,
+            "attention_ms_per_loop": round(a_ms, 4), "selector_ms_per_loop": round(s_ms, 4),
+            "attention_GB_per_s": round(alg / (a_ms / 1e3) / 1e9, 1),
+            "attention_frac_of_measured_peak": round(alg / (a_ms / 1e3) / 1e9 / peak, 4),
+            "slow_step_bytes": slow_bytes, "loop_bytes": alg},
+            "cpu_oracle": {"decode_steps_per_s": round(rate, 4), "cores": P,
+                           "decode_steps_per_s_1core": round(extra["value_1core"], 5),
+                           "unit_step_s": {"slow": round(extra["t_slow_s"], 4), "fast": round(extra["t_fast_s"], 5)},
+                           "cpu_model": extra["cpu_model"], "sample": sample}}
+        print(json.dumps(line), flush=True)
+        out.append(line)
+        del R
+        torch.cuda.empty_cache()
+    # Vegas (cfg3): verify with Collect-2, per-sequence selection, 4 draft steps
+    import slow_sparse_kv_gb300 as sfi
+    wl = W.cfg3()
+    wl.n_steps = 1
+    R = Cfg2Runner(wl, 0, make_ctx=False)
+    sh = wl.shape
+    B, rows = sh.batch, wl.gamma + 1
+    lens = [n + rows for n in wl.n0]
+    lay = sfi.Layout(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16, R.offsets, wl.cap, lens,
+                     R.max_len, device=R.dev)
+    ws = sfi.verify_workspace(lay, rows)
+    ws2 = sfi.alloc_workspace(lay)
+    q5 = torch.stack([torch.stack([torch.from_numpy(wl.q_storage(0, 0, b, t).view(np.int16)).view(torch.bfloat16)
+                                   for t in range(rows)]) for b in range(B)]).to(R.dev)
+    o5 = torch.empty(B, rows, sh.n_q_heads, sh.head_dim, device=R.dev)
+    lsum = torch.empty(B, sh.n_kv_heads, R.max_len, device=R.dev)
+    idx = torch.empty(B, sh.n_kv_heads, wl.k, dtype=torch.int32, device=R.dev)
+    cnt = torch.empty(B, sh.n_kv_heads, dtype=torch.int32, device=R.dev)
+    prm = sfi.params(0, rows, wl.k, 0.0, mode=sfi.SFI_SELECT_LOGIT_SUM_SEQ)
+    o1 = torch.empty(B, sh.n_q_heads, sh.head_dim, device=R.dev)
+    lays = [sfi.Layout(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, torch.bfloat16, R.offsets, wl.cap,
+                       [n + wl.gamma + j for n in wl.n0], R.max_len, device=R.dev) for j in range(1, wl.gamma + 1)]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=R.dev)
+    parts = {"verify_collect2": [], "select": [], "draft": []}
+    for rep in range(2 + max(3, args.steps)):
+        flush.fill_(rep & 0xFF)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record()
+        sfi.sfi_verify_attn(lay, rows, [0, wl.gamma], q5, R.K[0], R.V[0], o5, lsum, ws)
+        ev[1].record()
+        sfi.sfi_select(lay, prm, lsum, None, idx, cnt, None, ws2)
+        ev[2].record()
+        for j in range(wl.gamma):
+            sfi.sfi_fast_attn(lays[j], sfi.params(0, wl.gamma + 1 + j, wl.k, 0.0), q5[:, 0], R.K[0], R.V[0],
+                              idx, cnt, o1, ws2)
+        ev[3].record()
+        torch.cuda.synchronize()
+        if rep >= 2:
+            parts["verify_collect2"].append(ev[0].elapsed_time(ev[1]))
+            parts["select"].append(ev[1].elapsed_time(ev[2]))
+            parts["draft"].append(ev[2].elapsed_time(ev[3]) / wl.gamma)
+    med = {k: statistics.median(v) for k, v in parts.items()}
+    row = 2 * sh.n_kv_heads * sh.head_dim * 2
+    vbytes = sum(lens) * row
+    dbytes = sum(min(wl.k, n) + wl.gamma + 1 for n in wl.n0) * row
+    it_ms = med["verify_collect2"] + med["select"] + wl.gamma * med["draft"]
+    # oracle, one sequence on one core (the four sequences are independent)
+    K64 = W.storage_to_f64(wl.kv_storage("k", 0, 0), "bf16")
+    V64 = W.storage_to_f64(wl.kv_storage("v", 0, 0), "bf16")
+    qr = np.stack([W.storage_to_f64(wl.q_storage(0, 0, 0, t), "bf16") for t in range(rows)])
+    c0 = time.perf_counter()
+    _, logits = O.verify_attention(qr, K64, V64, wl.n0[0])
+    T = O.vegas_select(O.collected_logit_sum(logits, [0, wl.gamma], wl.n0[0]).sum(0), wl.k)
+    c1 = time.perf_counter()
+    for j in range(1, wl.gamma + 1):
+        O.draft_step(qr[0], K64, V64, wl.n0[0], wl.n0[0] + wl.gamma + j, T)
+    c2 = time.perf_counter()
+    line = {"workload": wl.name, "config": "cfg3", "gpu": {
+        "verify_collect2_ms": round(med["verify_collect2"], 4),
+        "verify_GB_per_s": round(vbytes / med["verify_collect2"] / 1e6, 1),
+        "verify_frac_of_measured_peak": round(vbytes / med["verify_collect2"] / 1e6 / peak, 4),
+        "select_ms": round(med["select"], 4), "draft_step_ms": round(med["draft"], 4),
+        "draft_GB_per_s": round(dbytes / med["draft"] / 1e6, 1),
+        "iterations_per_s": round(1e3 / it_ms, 2), "tokens_per_s": round(B * (wl.gamma + 1) * 1e3 / it_ms, 1),
+        "note": "one iteration = verify (5 rows, Collect-2) + selection + 4 draft steps for the batch of 4; "
+                "tokens = draft + bonus positions verified"},
+        "cpu_oracle": {"sequence_verify_select_s": round(c1 - c0, 3), "sequence_draft_steps_s": round(c2 - c1, 3),
+                       "iterations_per_s_1core": round(1.0 / (B * (c2 - c0)), 5), "cores": 1,
+                       "cpu_model": cpu_model(), "sample": "sequence 0, timed whole; batch of 4 scaled by 4"}}
+    print(json.dumps(line), flush=True)
+    out.append(line)
+    return out
+
+
 def run_reference(args):
     """The fp64 oracle as it stands, timed on the host cores for the same
-    workload, metric and unit (bounded sample per step)."""
+    workload, metric and unit.  One process per (sequence, KV head) unit of
+    layer 0 (one per core) generates its seeded inputs once; each bench step
+    then runs the next 32 decode steps of every unit's loop, and the step's
+    decode-steps/s is extrapolated from its mean slow and fast unit-step
+    times to the whole job (every layer, sequence and KV head)."""
     wl = W.cfg2(n_layers=args.layers, n_steps=args.decode_steps) if args.workload == "cfg2" else W.cfg1()
-    # slow fraction of this workload's schedule (host-only bookkeeping on the seeded trace)
     from oracle import sfi_oracle as O
     slow = O.schedule(wl.boundary_trace(), wl.budget)
     frac = float(slow.mean())
-    rates = []
-    sample = ""
-    P = 1
-    for s in range(args.warmup + args.steps):
-        rate, P, sample, _, _ = cpu_oracle_rate(wl, frac, budget_s=args.cpu_budget)
-        if s >= args.warmup:
-            rates.append(rate)
+    pool = OraclePool(wl)
+    per = 32
+    rates, walls, rate1s = [], [], []
+    sample_steps = [0, 0]
+    last_ts = []
+    try:
+        for s_ in range(args.warmup + args.steps):
+            t0 = (s_ * per) % wl.n_steps  # the loops start again after n_steps (step 0 is slow)
+            t_begin = time.perf_counter()
+            ts, tf = pool.run(t0, min(wl.n_steps, t0 + per))
+            wall = time.perf_counter() - t_begin
+            if s_ >= args.warmup:
+                if not ts:  # a slice without a slow step: take the slow time of the last one that had one
+                    ts = last_ts
+                rate, rate1, _, _, ups = oracle_rates(wl, frac, ts, tf, pool.P)
+                rates.append(rate)
+                rate1s.append(rate1)
+                walls.append(wall)
+                sample_steps[0] += len(ts)
+                sample_steps[1] += len(tf)
+            if ts:
+                last_ts = ts
+    finally:
+        pool.close()
     value = float(np.mean(rates))
     units_per_step = wl.n_layers * wl.shape.batch * wl.shape.n_kv_heads
+    sample = (f"{args.steps} bench steps, each the next {per} decode steps of the loops of {pool.P} "
+              f"(sequence, KV head) units of layer 0 (seeded bf16 workload, one single-threaded process "
+              f"per unit): {sample_steps[0]} slow + {sample_steps[1]} fast unit steps; decode steps/s "
+              f"extrapolated to {units_per_step} units per decode step, slow fraction {frac:.4f}")
     return {
         "impl": "reference",
         "metric": "SFI decode steps/s (slow & fast) and achieved HBM GB/s as % of GB300 peak",
         "value": round(value, 6), "unit": "decode steps/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(walls)), 3),
+        "ms_per_step_unit": f"wall time of one bench step ({per} decode steps of {pool.P} units)",
+        "extrapolated": True,
+        "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": wl.name, "units_per_decode_step": units_per_step},
-        "cpu_baseline": {"value": round(value, 6), "unit": "decode steps/s", "cores": P,
-                         "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": "decode steps/s", "cores": pool.P,
+                         "kind": "oracle", "sample": sample,
+                         "value_1core": round(float(np.mean(rate1s)), 7), "cpu_model": cpu_model(),
+                         "host_cores": os.cpu_count()},
         "e2e": {"value": round(value, 6), "unit": "decode steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -833,7 +1067,6 @@ def main():
     ap.add_argument("--workload", default="cfg2", choices=["cfg2", "cfg1"])
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--decode-steps", type=int, default=256)
-    ap.add_argument("--cpu-budget", type=float, default=1.5, help="seconds per CPU worker")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-log-dir", default=os.environ.get("SFI_CLOCK_LOG_DIR", os.path.join(ROOT, "bench_logs")),
                     help="where the nvidia-smi clock samples of the timed region are written")
@@ -848,6 +1081,8 @@ def main():
     ap.add_argument("--case-context", type=int, default=0,
                     help="context of the --kernel-case layer (default: the 131072 of the decode "
                          "benchmark); the fast step's work does not depend on it")
+    ap.add_argument("--config-table", action="store_true", help="time the 2K fp32 and 32K decode loops "
+                    "and the Vegas verify/select/draft workload beside the oracle (one JSON line each)")
     ap.add_argument("--ragged-sweep", action="store_true", help="time one mixed slow/fast step of "
                     "the 32-sequence ragged batch for k in {1024, 4096, 16384} x window in {128, 256, 512}")
     args = ap.parse_args()
@@ -856,6 +1091,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.ragged_sweep:
         print(json.dumps(run_ragged_sweep(args)), flush=True)
+        return
+    if args.config_table:
+        run_config_table(args)
         return
     if args.kernel_case == "verify":
         print(json.dumps(run_verify_cases(args)), flush=True)

@@ -89,6 +89,8 @@ WsPlan plan_workspace(int B, int H_q, int H_kv, int D, int max_len) {
   off += align256(units * kSelMaxChunks * 4);
   p.sel_hist_off = off;
   off += align256(units * 2048 * 4);
+  p.sel_hist2_off = off;
+  off += align256(units * 2048 * 4);
   p.sel_done_off = off;
   off += align256(units * 4);
   p.sel_keys_off = off;
@@ -103,6 +105,7 @@ void attach_select_scratch(SelectArgs& a, char* ws, const WsPlan& p) {
   a.sel_nu = reinterpret_cast<float*>(ws + p.sel_nu_off);
   a.sel_cnt = reinterpret_cast<uint32_t*>(ws + p.sel_cnt_off);
   a.sel_hist = reinterpret_cast<uint32_t*>(ws + p.sel_hist_off);
+  a.sel_hist2 = reinterpret_cast<uint32_t*>(ws + p.sel_hist2_off);
   a.sel_done = reinterpret_cast<uint32_t*>(ws + p.sel_done_off);
   a.sel_keys = reinterpret_cast<uint32_t*>(ws + p.sel_keys_off);
   a.sel_list = reinterpret_cast<unsigned long long*>(ws + p.sel_list_off);
@@ -578,8 +581,12 @@ sfi_status sfi_verify_attn(const sfi_layout* L, int32_t n_rows, const int32_t* c
   fill_attn_common(va.base, L, q, k, v, out, static_cast<char*>(ws), p);
   for (int b = 0; b < L->batch; ++b) va.base.slow.bits[b >> 5] |= 1u << (b & 31);
   va.base.rpi_slow = va.base.rpi_fast =
+      // A verify stage carries R * G query rows (several times the MMA work
+      // of a decode stage), so a CTA left alone at the end of the launch
+      // cannot stream faster: the split is chosen as for evidence-writing
+      // launches, without a tail speed-up.
       choose_item_split((long long)L->batch * L->n_kv_heads, L->max_len, 0, 0, verify_stage_rows(),
-                        device_sm_count(), false).rpi_a;  // 4-byte logit sums barely lengthen a stage
+                        device_sm_count(), true).rpi_a;
   va.R = n_rows;
   va.ncg = n_collect * G;
   for (int i = 0; i < n_ord; ++i) va.t_of_slot[i] = order[i];

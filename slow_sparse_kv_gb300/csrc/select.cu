@@ -47,7 +47,6 @@ constexpr int kSelU = 8;        // positions in flight per thread
 constexpr int kRadixBins = 2048;
 constexpr int kRadixShift0 = 21;  // digits: bits 31..21, 20..10, 9..0 of the order key
 constexpr int kRadixShift1 = 10;
-constexpr int kCandCap = 8192;  // keys of bin d0 the finisher gathers in shared memory
 constexpr int kSelMinChunk = 2048;  // positions per chunk, at least
 constexpr int kRun = 8;             // consecutive list positions or entries per thread and tile
 
@@ -380,65 +379,74 @@ __global__ void __launch_bounds__(kSelT, 2) sel_score_kernel(const SelectArgs a)
   }
 }
 
-// Address of entry e (chunks in order, each in position order) of the
-// unit's list, given the chunks' exclusive entry offsets offs[0..C].
-__device__ __forceinline__ size_t sel_entry(const SelUnit& s, const uint32_t* offs, int C,
-                                            uint32_t e, size_t row0) {
-  int lo = 0, hi = C - 1;  // largest c with offs[c] <= e: the chunk holding e
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (offs[mid] <= e) lo = mid;
-    else hi = mid - 1;
-  }
-  return row0 + size_t(sel_chunk_e0(s, lo)) + (e - offs[lo]);
-}
-
 // Launch 3: per chunk, the ordered list of keys at or above the k-th key's
-// top digit; the unit's last chunk CTA to finish completes the selection.
+// top digit, and the histogram of the next 11 bits of its keys in that
+// digit's bin; the unit's last chunk CTA to finish completes the selection.
 __global__ void __launch_bounds__(kSelT) sel_list_kernel(const SelectArgs a) {
   __shared__ uint32_t hist[kRadixBins];
-  __shared__ uint32_t cand[kCandCap];
-  __shared__ uint32_t offs[kSelMaxChunks + 1];
+  __shared__ uint32_t cnt_c[kSelMaxChunks + 1];  // finisher: entries per chunk
+  __shared__ uint32_t gt_c[kSelMaxChunks + 1];   // finisher: keys above tau per chunk, then offsets
+  __shared__ uint32_t eq_c[kSelMaxChunks + 1];   // finisher: keys equal to tau per chunk, then offsets
   __shared__ uint32_t scan_sh[33];
-  __shared__ uint32_t sh_digit, sh_above, sh_last, cand_n;
+  __shared__ uint32_t sh_digit, sh_above, sh_last;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, c = blockIdx.x, C = gridDim.x;
   const int lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kSelT / 32;
   const unsigned lt = (1u << lane) - 1u;
   SelUnit s;
   if (sel_unit(a, blockIdx.y, c, C, s) != 0 || !s.need_radix) return;  // uniform over the unit
+  const uint32_t* krow = a.sel_keys + size_t(s.u) * a.max_len;
+  const size_t row0 = size_t(s.u) * a.max_len;
   uint32_t* gh = a.sel_hist + size_t(s.u) * kRadixBins;
+  uint32_t* gh2 = a.sel_hist2 + size_t(s.u) * kRadixBins;
+  // this chunk's keys (thread t: kRun consecutive positions of each tile of
+  // kSelT * kRun) are loaded together with the unit's histogram
+  const int ntile = (s.e1 - s.e0 + kSelT * kRun - 1) / (kSelT * kRun);
+  const bool one_tile = ntile <= 1;
+  uint32_t key[kRun];
+  const int i0 = s.e0 + tid * kRun;
+  if (one_tile) {
+#pragma unroll
+    for (int j = 0; j < kRun; ++j) key[j] = i0 + j < s.e1 ? krow[i0 + j] : 0u;
+  }
   for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = __ldcg(gh + i);
   __syncthreads();
   block_pick_digit<kRadixBins>(hist, uint32_t(s.keff), &sh_digit, &sh_above, scan_sh);
   const uint32_t d0 = sh_digit;
-  uint32_t krem = uint32_t(s.keff) - sh_above;
-  const uint32_t n_cand = hist[d0];
-  // ---- this chunk's keys at or above d0, in position order, into its own
-  // region of the unit's list (starting at its first position of E).  Tiles
-  // of kSelT * kRun positions; thread t takes kRun consecutive positions of a
-  // tile, all loaded before any is used; one block scan per tile.
-  const uint32_t* krow = a.sel_keys + size_t(s.u) * a.max_len;
-  const size_t row0 = size_t(s.u) * a.max_len;
+  const uint32_t krem0 = uint32_t(s.keff) - sh_above;
+  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;  // now: next-digit histogram
+  __syncthreads();
+  // ---- keys at or above d0, in position order, into this chunk's region of
+  // the unit's list (starting at its first position of E); one block scan per
+  // tile; the keys of bin d0 also go into the next-digit histogram
   unsigned long long* lrow = a.sel_list + row0 + s.e0;
   uint32_t tot = 0;
-  for (int tb = s.e0; tb < s.e1; tb += kSelT * kRun) {
-    const int i0 = tb + tid * kRun;
-    uint32_t key[kRun];
+  for (int t = 0; t < ntile; ++t) {
+    const int ib = s.e0 + t * kSelT * kRun + tid * kRun;
+    if (!one_tile) {
+#pragma unroll
+      for (int j = 0; j < kRun; ++j) key[j] = ib + j < s.e1 ? krow[ib + j] : 0u;
+    }
     uint32_t nm = 0;
 #pragma unroll
-    for (int j = 0; j < kRun; ++j) key[j] = i0 + j < s.e1 ? krow[i0 + j] : 0u;
-#pragma unroll
-    for (int j = 0; j < kRun; ++j) nm += (i0 + j < s.e1 && (key[j] >> kRadixShift0) >= d0) ? 1u : 0u;
+    for (int j = 0; j < kRun; ++j) nm += (ib + j < s.e1 && (key[j] >> kRadixShift0) >= d0) ? 1u : 0u;
     uint32_t ttot;
     uint32_t at = tot + block_excl_scan(nm, scan_sh, ttot);
 #pragma unroll
-    for (int j = 0; j < kRun; ++j)
-      if (i0 + j < s.e1 && (key[j] >> kRadixShift0) >= d0)
-        lrow[at++] = (static_cast<unsigned long long>(key[j]) << 32) | uint32_t(i0 + j);
+    for (int j = 0; j < kRun; ++j) {
+      const bool in = ib + j < s.e1;
+      const uint32_t dg = key[j] >> kRadixShift0;
+      if (in && dg >= d0)
+        lrow[at++] = (static_cast<unsigned long long>(key[j]) << 32) | uint32_t(ib + j);
+      hist_add(hist, (key[j] >> kRadixShift1) & (kRadixBins - 1), in && dg == d0);
+    }
     tot += ttot;
   }
+  __syncthreads();
+  for (int i = tid; i < kRadixBins; i += kSelT)
+    if (hist[i]) atomicAdd(gh2 + i, hist[i]);
   if (tid == 0) a.sel_cnt[size_t(s.u) * kSelMaxChunks + c] = tot;
   __threadfence();
   __syncthreads();
@@ -448,131 +456,110 @@ __global__ void __launch_bounds__(kSelT) sel_list_kernel(const SelectArgs a) {
   __threadfence();
 
   // ---------------------------------------------------------------- finisher
-  // exclusive entry offsets of the chunks (warp 0, two chunks per lane)
-  if (warp == 0) {
-    const uint32_t* pc = a.sel_cnt + size_t(s.u) * kSelMaxChunks;
-    const uint32_t x0 = lane < C ? __ldcg(pc + lane) : 0u;
-    const uint32_t x1 = lane + 32 < C ? __ldcg(pc + lane + 32) : 0u;
-    uint32_t i0 = x0, i1 = x1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
-      if (lane >= o) i0 += y0, i1 += y1;
-    }
-    const uint32_t t0 = __shfl_sync(kFull, i0, 31);
-    offs[lane] = i0 - x0;
-    offs[lane + 32] = t0 + i1 - x1;
-    if (lane == 31) offs[kSelMaxChunks] = t0 + i1;
-    if (lane == 0) cand_n = 0;
+  // The second digit d1 comes from the chunks' next-digit histograms; the
+  // last 10 bits from the few keys with prefix (d0, d1).  Every walk over the
+  // lists gives each warp whole chunks (entries of chunk c: kRun per lane in
+  // flight, in position order) -- no search for an entry's chunk.
+  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = __ldcg(gh2 + i);
+  for (int i = tid; i < C; i += kSelT) {
+    cnt_c[i] = __ldcg(a.sel_cnt + size_t(s.u) * kSelMaxChunks + i);
+    gt_c[i] = 0u;
+    eq_c[i] = 0u;
   }
   __syncthreads();
-  const uint32_t NE = offs[C];  // chunks past C count 0, so this is the total
-  // ---- the keys of bin d0, gathered in shared memory when they fit
-  const bool in_smem = n_cand <= uint32_t(kCandCap);
-  if (in_smem) {
-    for (uint32_t tb = 0; tb < NE; tb += kSelT * kRun) {
-      uint32_t key[kRun];
+  block_pick_digit<kRadixBins>(hist, krem0, &sh_digit, &sh_above, scan_sh);
+  const uint32_t p1 = (d0 << (kRadixShift0 - kRadixShift1)) | sh_digit;  // top 22 bits
+  const uint32_t krem1 = krem0 - sh_above;
+  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
+  __syncthreads();
+  auto walk = [&](auto&& body) {
+    for (int cc = warp; cc < C; cc += NW) {
+      const unsigned long long* lc = a.sel_list + row0 + sel_chunk_e0(s, cc);
+      const uint32_t nc = cnt_c[cc];
+      for (uint32_t jb = 0; jb < nc; jb += 32 * kRun) {
+        unsigned long long ent[kRun];
 #pragma unroll
-      for (int j = 0; j < kRun; ++j) {
-        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
-        key[j] = e < NE ? uint32_t(__ldcg(a.sel_list + sel_entry(s, offs, C, e, row0)) >> 32) : 0u;
-      }
-#pragma unroll
-      for (int j = 0; j < kRun; ++j) {
-        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
-        const bool m = e < NE && (key[j] >> kRadixShift0) == d0;
-        const unsigned bal = __ballot_sync(kFull, m);
-        if (bal) {
-          uint32_t b0 = 0;
-          if (lane == 0) b0 = atomicAdd(&cand_n, uint32_t(__popc(bal)));
-          b0 = __shfl_sync(kFull, b0, 0);
-          const uint32_t at_c = b0 + __popc(bal & lt);
-          if (m && at_c < uint32_t(kCandCap)) cand[at_c] = key[j];
+        for (int r = 0; r < kRun; ++r) {
+          const uint32_t jj = jb + uint32_t(r) * 32 + lane;
+          ent[r] = jj < nc ? __ldcg(lc + jj) : 0ull;
         }
+#pragma unroll
+        for (int r = 0; r < kRun; ++r) body(cc, jb + uint32_t(r) * 32 + lane < nc, ent[r]);
       }
     }
-    __syncthreads();
-  }
-  const uint32_t n_in = min(cand_n, uint32_t(kCandCap));  // == n_cand
-  // ---- the two lower digits (11 and 10 bits) among the keys of bin d0; with
-  // more than kCandCap of them, the passes read the list itself
-  uint32_t prefix = d0;
-  for (int pass = 1; pass < 3; ++pass) {
-    const int shift = pass == 1 ? kRadixShift1 : 0;
-    const int width = pass == 1 ? kRadixShift0 - kRadixShift1 : kRadixShift1;
-    const uint32_t dmask = (1u << width) - 1u;
-    const int hs = shift + width;
-    for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
-    __syncthreads();
-    const uint32_t n_it = in_smem ? n_in : NE;
-    for (uint32_t tb = 0; tb < n_it; tb += kSelT * kRun) {
-      uint32_t key[kRun];
-#pragma unroll
-      for (int j = 0; j < kRun; ++j) {
-        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
-        key[j] = e >= n_it ? 0u
-                 : in_smem ? cand[e]
-                           : uint32_t(__ldcg(a.sel_list + sel_entry(s, offs, C, e, row0)) >> 32);
-      }
-#pragma unroll
-      for (int j = 0; j < kRun; ++j) {
-        const uint32_t e = tb + uint32_t(j) * kSelT + tid;
-        hist_add(hist, (key[j] >> shift) & dmask, e < n_it && (key[j] >> hs) == prefix);
-      }
+  };
+  // last 10 bits among the keys with prefix p1
+  walk([&](int, bool v, unsigned long long e) {
+    const uint32_t k = uint32_t(e >> 32);
+    hist_add(hist, k & ((1u << kRadixShift1) - 1u), v && (k >> kRadixShift1) == p1);
+  });
+  __syncthreads();
+  block_pick_digit<1 << kRadixShift1>(hist, krem1, &sh_digit, &sh_above, scan_sh);
+  const uint32_t tau = (p1 << kRadixShift1) | sh_digit;
+  const uint32_t take_eq = krem1 - sh_above;
+  // keys above tau and equal to it, per chunk
+  walk([&](int cc, bool v, unsigned long long e) {
+    const uint32_t k = uint32_t(e >> 32);
+    const uint32_t ng = __popc(__ballot_sync(kFull, v && k > tau));
+    const uint32_t nq = __popc(__ballot_sync(kFull, v && k == tau));
+    if (lane == 0) {  // chunks are walked by one warp each: plain adds
+      gt_c[cc] += ng;
+      eq_c[cc] += nq;
     }
-    __syncthreads();
-    if (width == 11) block_pick_digit<2048>(hist, krem, &sh_digit, &sh_above, scan_sh);
-    else block_pick_digit<1024>(hist, krem, &sh_digit, &sh_above, scan_sh);
-    prefix = (prefix << width) | sh_digit;
-    krem -= sh_above;
+  });
+  __syncthreads();
+  if (warp == 0) {  // exclusive offsets over the chunks (two per lane)
+    const uint32_t g0 = lane < C ? gt_c[lane] : 0u, g1 = lane + 32 < C ? gt_c[lane + 32] : 0u;
+    const uint32_t q0 = lane < C ? eq_c[lane] : 0u, q1 = lane + 32 < C ? eq_c[lane + 32] : 0u;
+    uint32_t ig0 = g0, ig1 = g1, iq0 = q0, iq1 = q1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t a0 = __shfl_up_sync(kFull, ig0, o), a1 = __shfl_up_sync(kFull, ig1, o);
+      const uint32_t b0 = __shfl_up_sync(kFull, iq0, o), b1 = __shfl_up_sync(kFull, iq1, o);
+      if (lane >= o) ig0 += a0, ig1 += a1, iq0 += b0, iq1 += b1;
+    }
+    const uint32_t tg = __shfl_sync(kFull, ig0, 31), tq = __shfl_sync(kFull, iq0, 31);
+    __syncwarp();
+    if (lane < C) gt_c[lane] = ig0 - g0, eq_c[lane] = iq0 - q0;
+    if (lane + 32 < C) gt_c[lane + 32] = tg + ig1 - g1, eq_c[lane + 32] = tq + iq1 - q1;
   }
-  const uint32_t tau = prefix, take_eq = krem;
-  // ---- ordered output: the keys above tau, then the first take_eq keys
-  // equal to it; entry e goes to slot (keys above tau before it) +
-  // min(keys equal to tau before it, take_eq).  Eight consecutive entries per
-  // thread, one block scan per tile of kSelT * 8 entries.
+  __syncthreads();
+  // ordered output: entry goes to slot (keys above tau before it) +
+  // min(keys equal to tau before it, take_eq) -- the keys above tau, then the
+  // lowest-positioned take_eq keys equal to it, all in position order
   int32_t* out_idx = a.idx + size_t(s.per_seq ? s.b * a.H_kv : s.unit) * a.k;
   const int n_rows = s.per_seq ? a.H_kv : 1;
-  uint32_t g_run = 0, q_run = 0;
-  for (uint32_t tb = 0; tb < NE; tb += kSelT * 8) {
-    const uint32_t ea = tb + uint32_t(tid) * 8;
-    unsigned long long ent[8];
-    uint32_t ng = 0, nq = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool v = ea + j < NE;
-      ent[j] = v ? __ldcg(a.sel_list + sel_entry(s, offs, C, ea + j, row0)) : 0ull;
-      const uint32_t key = uint32_t(ent[j] >> 32);
-      ng += (v && key > tau) ? 1u : 0u;
-      nq += (v && key == tau) ? 1u : 0u;
+  int cur = -1;
+  uint32_t gb = 0, qb = 0;
+  walk([&](int cc, bool v, unsigned long long e) {
+    if (cc != cur) {
+      cur = cc;
+      gb = gt_c[cc];
+      qb = eq_c[cc];
     }
-    uint32_t ttot;
-    const uint32_t ex = block_excl_scan((ng << 16) | nq, scan_sh, ttot);  // < 2^16 per tile
-    uint32_t gb = g_run + (ex >> 16), qb = q_run + (ex & 0xffffu);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (ea + j < NE) {
-        const uint32_t key = uint32_t(ent[j] >> 32);
-        const int pos = int(uint32_t(ent[j]));
-        // slots stay below keff for the counts above; the bound only guards
-        // the output row against an inconsistent list
-        if (key > tau) {
-          const uint32_t slot = gb + min(qb, take_eq);
-          if (slot < uint32_t(s.keff))
-            for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + slot] = pos;
-          ++gb;
-        } else if (key == tau) {
-          if (qb < take_eq && gb + qb < uint32_t(s.keff))
-            for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + gb + qb] = pos;
-          ++qb;
-        }
-      }
+    const uint32_t k = uint32_t(e >> 32);
+    const int pos = int(uint32_t(e));
+    const unsigned bg = __ballot_sync(kFull, v && k > tau);
+    const unsigned bq = __ballot_sync(kFull, v && k == tau);
+    const uint32_t g_at = gb + __popc(bg & lt), q_at = qb + __popc(bq & lt);
+    // slots stay below keff for consistent counts; the bound only guards the
+    // output row against an inconsistent list
+    if ((bg >> lane) & 1u) {
+      const uint32_t slot = g_at + min(q_at, take_eq);
+      if (slot < uint32_t(s.keff))
+        for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + slot] = pos;
+    } else if (((bq >> lane) & 1u) && q_at < take_eq && g_at + q_at < uint32_t(s.keff)) {
+      for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + g_at + q_at] = pos;
     }
-    g_run += ttot >> 16;
-    q_run += ttot & 0xffffu;
+    gb += __popc(bg);
+    qb += __popc(bq);
+  });
+  __syncthreads();
+  // leave the histograms and the counter at zero for the next launch
+  for (int i = tid; i < kRadixBins; i += kSelT) {
+    gh[i] = 0u;
+    gh2[i] = 0u;
   }
-  // leave the histogram and the counter at zero for the next launch
-  for (int i = tid; i < kRadixBins; i += kSelT) gh[i] = 0u;
   if (tid == 0) a.sel_done[s.u] = 0u;
 }
 

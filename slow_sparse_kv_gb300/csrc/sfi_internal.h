@@ -102,6 +102,7 @@ struct SelectArgs {
   float* sel_nu;                 // [B*H_kv][kSelMaxChunks] chunk sums of key norms over E
   uint32_t* sel_cnt;             // [B*H_kv][kSelMaxChunks] list entries per chunk
   uint32_t* sel_hist;            // [B*H_kv][2048] top-digit histogram, zero between launches
+  uint32_t* sel_hist2;           // [B*H_kv][2048] next-digit histogram of the k-th key's top bin
   uint32_t* sel_done;            // [B*H_kv] chunk CTAs finished, zero between launches
   uint32_t* sel_keys;            // [B*H_kv][max_len] order keys of the ranked scores
   unsigned long long* sel_list;  // [B*H_kv][max_len] (key << 32 | position) entries
@@ -128,7 +129,8 @@ int verify_stage_rows();
 // Workspace plan: one layout serves every call of a given geometry.
 struct WsPlan {
   size_t status_off, counters_off, partials_off, logits_off, stats_off, s_off;
-  size_t sel_nu_off, sel_cnt_off, sel_hist_off, sel_done_off, sel_keys_off, sel_list_off;
+  size_t sel_nu_off, sel_cnt_off, sel_hist_off, sel_hist2_off, sel_done_off, sel_keys_off,
+      sel_list_off;
   size_t total;
   int32_t max_items;
 };
