@@ -49,6 +49,7 @@ constexpr int kRadixShift0 = 21;  // digits: bits 31..21, 20..10, 9..0 of the or
 constexpr int kRadixShift1 = 10;
 constexpr int kSelMinChunk = 2048;  // positions per chunk, at least
 constexpr int kRun = 8;             // consecutive list positions or entries per thread and tile
+constexpr int kListCap = 12288;     // list entries the finisher stages in shared memory (96 KB)
 
 // The G logits of one position ([pos][G] rows are 4*G-byte aligned).
 template <int G>
@@ -384,7 +385,9 @@ __global__ void __launch_bounds__(kSelT, 2) sel_score_kernel(const SelectArgs a)
 // digit's bin; the unit's last chunk CTA to finish completes the selection.
 __global__ void __launch_bounds__(kSelT) sel_list_kernel(const SelectArgs a) {
   __shared__ uint32_t hist[kRadixBins];
+  extern __shared__ unsigned long long lst[];     // finisher: the unit's list (kListCap entries)
   __shared__ uint32_t cnt_c[kSelMaxChunks + 1];  // finisher: entries per chunk
+  __shared__ uint32_t offs_c[kSelMaxChunks + 1]; // finisher: their exclusive offsets
   __shared__ uint32_t gt_c[kSelMaxChunks + 1];   // finisher: keys above tau per chunk, then offsets
   __shared__ uint32_t eq_c[kSelMaxChunks + 1];   // finisher: keys equal to tau per chunk, then offsets
   __shared__ uint32_t scan_sh[33];
@@ -467,24 +470,76 @@ __global__ void __launch_bounds__(kSelT) sel_list_kernel(const SelectArgs a) {
     eq_c[i] = 0u;
   }
   __syncthreads();
-  block_pick_digit<kRadixBins>(hist, krem0, &sh_digit, &sh_above, scan_sh);
+  if (warp == 0) {  // exclusive entry offsets of the chunks (two per lane)
+    const uint32_t x0 = lane < C ? cnt_c[lane] : 0u, x1 = lane + 32 < C ? cnt_c[lane + 32] : 0u;
+    uint32_t i0 = x0, i1 = x1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
+      if (lane >= o) i0 += y0, i1 += y1;
+    }
+    const uint32_t t0 = __shfl_sync(kFull, i0, 31);
+    offs_c[lane] = i0 - x0;
+    offs_c[lane + 32] = t0 + i1 - x1;
+    if (lane == 31) offs_c[kSelMaxChunks] = t0 + i1;
+  }
+  block_pick_digit<kRadixBins>(hist, krem0, &sh_digit, &sh_above, scan_sh);  // (barriers)
   const uint32_t p1 = (d0 << (kRadixShift0 - kRadixShift1)) | sh_digit;  // top 22 bits
   const uint32_t krem1 = krem0 - sh_above;
+  const uint32_t NE = offs_c[C];  // chunks past C count 0
+  // The unit's list, staged in shared memory when it fits: every thread
+  // loads kRun * 2 entries at once (the entry's chunk from the offsets), so
+  // the walks below read shared memory only.
+  const bool staged = NE <= uint32_t(kListCap);
+  if (staged) {
+    constexpr int V = 2 * kRun;
+    for (uint32_t tb = 0; tb < NE; tb += kSelT * V) {
+      unsigned long long ent[V];
+#pragma unroll
+      for (int r = 0; r < V; ++r) {
+        const uint32_t e = tb + uint32_t(r) * kSelT + tid;
+        ent[r] = 0ull;
+        if (e < NE) {
+          int lo = 0, hi = C - 1;  // chunk holding e: the largest c with offs_c[c] <= e
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (offs_c[mid] <= e) lo = mid;
+            else hi = mid - 1;
+          }
+          ent[r] = __ldcg(a.sel_list + row0 + sel_chunk_e0(s, lo) + (e - offs_c[lo]));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < V; ++r) {
+        const uint32_t e = tb + uint32_t(r) * kSelT + tid;
+        if (e < NE) lst[e] = ent[r];
+      }
+    }
+  }
   for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
   __syncthreads();
+  // each warp takes whole chunks, their entries in position order
   auto walk = [&](auto&& body) {
     for (int cc = warp; cc < C; cc += NW) {
-      const unsigned long long* lc = a.sel_list + row0 + sel_chunk_e0(s, cc);
       const uint32_t nc = cnt_c[cc];
-      for (uint32_t jb = 0; jb < nc; jb += 32 * kRun) {
-        unsigned long long ent[kRun];
-#pragma unroll
-        for (int r = 0; r < kRun; ++r) {
-          const uint32_t jj = jb + uint32_t(r) * 32 + lane;
-          ent[r] = jj < nc ? __ldcg(lc + jj) : 0ull;
+      if (staged) {
+        const unsigned long long* lc = lst + offs_c[cc];
+        for (uint32_t jb = 0; jb < nc; jb += 32) {
+          const uint32_t jj = jb + lane;
+          body(cc, jj < nc, jj < nc ? lc[jj] : 0ull);
         }
+      } else {
+        const unsigned long long* lc = a.sel_list + row0 + sel_chunk_e0(s, cc);
+        for (uint32_t jb = 0; jb < nc; jb += 32 * kRun) {
+          unsigned long long ent[kRun];
 #pragma unroll
-        for (int r = 0; r < kRun; ++r) body(cc, jb + uint32_t(r) * 32 + lane < nc, ent[r]);
+          for (int r = 0; r < kRun; ++r) {
+            const uint32_t jj = jb + uint32_t(r) * 32 + lane;
+            ent[r] = jj < nc ? __ldcg(lc + jj) : 0ull;
+          }
+#pragma unroll
+          for (int r = 0; r < kRun; ++r) body(cc, jb + uint32_t(r) * 32 + lane < nc, ent[r]);
+        }
       }
     }
   };
@@ -593,11 +648,11 @@ int select_chunks(int units, int max_len) {
 
 template <typename K>
 cudaError_t launch_dependent(K kernel, dim3 grid, int threads, cudaStream_t st,
-                             const SelectArgs& a) {
+                             const SelectArgs& a, size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -619,7 +674,11 @@ cudaError_t launch_select_t(const SelectArgs& a, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   if (a.mode == SFI_SELECT_FUSED) e = launch_dependent(sel_nu_kernel, grid, kSelNuT, st, a);
   if (e == cudaSuccess) e = launch_dependent(sel_score_kernel<EV_G>, grid, kSelT, st, a);
-  if (e == cudaSuccess) e = launch_dependent(sel_list_kernel, grid, kSelT, st, a);
+  if (e == cudaSuccess) {
+    const size_t smem = size_t(kListCap) * sizeof(unsigned long long);
+    e = cudaFuncSetAttribute(sel_list_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e == cudaSuccess) e = launch_dependent(sel_list_kernel, grid, kSelT, st, a, smem);
+  }
   return e;
 }
 
