@@ -581,8 +581,9 @@ sfi_status sfi_verify_attn(const sfi_layout* L, int32_t n_rows, const int32_t* c
   fill_attn_common(va.base, L, q, k, v, out, static_cast<char*>(ws), p);
   for (int b = 0; b < L->batch; ++b) va.base.slow.bits[b >> 5] |= 1u << (b & 31);
   va.base.rpi_slow = va.base.rpi_fast =
-      // (measured: finer items without the tail speed-up -- 19 per unit at
-      // batch 4 x 65541 rows instead of 8 -- made the launch 20% slower)
+      // (measured: finer items -- 19 per unit at batch 4 x 65541 rows, 4 per
+      // CTA, instead of 8 -- were 25% slower: a split verify item is merged
+      // from R * G partial rows, which costs more than the idle tail saved)
       choose_item_split((long long)L->batch * L->n_kv_heads, L->max_len, 0, 0, verify_stage_rows(),
                         device_sm_count(), false).rpi_a;
   va.R = n_rows;

@@ -51,6 +51,7 @@ struct VerifyCfg {
   static constexpr int STATE = (D / 16) * kVerifyMaxTiles * 4 + kVerifyMaxTiles * 4;
   static constexpr size_t RED_B = size_t(4) * 32 * STATE * 4;  // four warps' states
   static_assert(size_t(32) * (D + 2) * 4 <= RED_B, "the final [column][D + 2] rows fit the merge buffer");
+  static_assert((size_t(kItemSlotsPerUnit) * 32 + 64) * 4 <= RED_B, "item scales fit the merge buffer");
   static constexpr int NS_FIT =
       int((227 * 1024 - 2048 - RED_B - size_t(8 * kVerifyMaxTiles) * (D * 2 + 16) -
            (size_t(kMaxUnits) + 1 + kRankWords) * 4) / (2 * size_t(SR) * ROWB));
@@ -83,6 +84,9 @@ struct VState {
   float m[NTT][2], z[NTT][2];
 };
 
+// A warp's state in shared memory: element i of lane l at o[i * 32 + l]
+// (consecutive lanes in consecutive banks).  `o` points at the warp's block
+// plus the lane.
 // Combine `o` (the part of the item later in the fixed order) into `s`.
 template <int D, int NTT>
 __device__ __forceinline__ void vstate_merge(VState<D, NTT>& s, const float* o) {
@@ -91,15 +95,15 @@ __device__ __forceinline__ void vstate_merge(VState<D, NTT>& s, const float* o) 
   for (int j = 0; j < NTT; ++j)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const float mo = o[DT * NTT * 4 + (j * 2 + h)];
-      const float zo = o[DT * NTT * 4 + 2 * NTT + (j * 2 + h)];
+      const float mo = o[(DT * NTT * 4 + (j * 2 + h)) * 32];
+      const float zo = o[(DT * NTT * 4 + 2 * NTT + (j * 2 + h)) * 32];
       const float M = fmaxf(s.m[j][h], mo);
       const float sa = s.m[j][h] == -INFINITY ? 0.f : exp2f(s.m[j][h] - M);
       const float sb = mo == -INFINITY ? 0.f : exp2f(mo - M);
 #pragma unroll
       for (int dt = 0; dt < DT; ++dt) {
-        s.acc[dt][j][h] = fmaf(o[(dt * NTT + j) * 4 + h], sb, s.acc[dt][j][h] * sa);
-        s.acc[dt][j][2 + h] = fmaf(o[(dt * NTT + j) * 4 + 2 + h], sb, s.acc[dt][j][2 + h] * sa);
+        s.acc[dt][j][h] = fmaf(o[((dt * NTT + j) * 4 + h) * 32], sb, s.acc[dt][j][h] * sa);
+        s.acc[dt][j][2 + h] = fmaf(o[((dt * NTT + j) * 4 + 2 + h) * 32], sb, s.acc[dt][j][2 + h] * sa);
       }
       s.z[j][h] = fmaf(zo, sb, s.z[j][h] * sa);
       s.m[j][h] = M;
@@ -114,13 +118,13 @@ __device__ __forceinline__ void vstate_store(const VState<D, NTT>& s, float* o) 
 #pragma unroll
     for (int j = 0; j < NTT; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[(dt * NTT + j) * 4 + e] = s.acc[dt][j][e];
+      for (int e = 0; e < 4; ++e) o[((dt * NTT + j) * 4 + e) * 32] = s.acc[dt][j][e];
 #pragma unroll
   for (int j = 0; j < NTT; ++j)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      o[DT * NTT * 4 + (j * 2 + h)] = s.m[j][h];
-      o[DT * NTT * 4 + 2 * NTT + (j * 2 + h)] = s.z[j][h];
+      o[(DT * NTT * 4 + (j * 2 + h)) * 32] = s.m[j][h];
+      o[(DT * NTT * 4 + 2 * NTT + (j * 2 + h)) * 32] = s.z[j][h];
     }
 }
 
@@ -395,17 +399,17 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
     // ---- merge the eight warp states: the other group into the first, then
     // slots 2, 3 into 0, 1, then slot 1 into slot 0
     named_bar_sync(1, nct);
-    if (wpar != first) vstate_store<D, NTT>(st, red + (wslot * 32 + lane) * S);
+    if (wpar != first) vstate_store<D, NTT>(st, red + wslot * 32 * S + lane);
     named_bar_sync(1, nct);
-    if (wpar == first) vstate_merge<D, NTT>(st, red + (wslot * 32 + lane) * S);
+    if (wpar == first) vstate_merge<D, NTT>(st, red + wslot * 32 * S + lane);
     named_bar_sync(1, nct);
-    if (wpar == first && wslot >= 2) vstate_store<D, NTT>(st, red + ((wslot - 2) * 32 + lane) * S);
+    if (wpar == first && wslot >= 2) vstate_store<D, NTT>(st, red + (wslot - 2) * 32 * S + lane);
     named_bar_sync(1, nct);
-    if (wpar == first && wslot < 2) vstate_merge<D, NTT>(st, red + (wslot * 32 + lane) * S);
+    if (wpar == first && wslot < 2) vstate_merge<D, NTT>(st, red + wslot * 32 * S + lane);
     named_bar_sync(1, nct);
-    if (wpar == first && wslot == 1) vstate_store<D, NTT>(st, red + lane * S);
+    if (wpar == first && wslot == 1) vstate_store<D, NTT>(st, red + lane);
     named_bar_sync(1, nct);
-    if (wpar == first && wslot == 0) vstate_merge<D, NTT>(st, red + lane * S);
+    if (wpar == first && wslot == 0) vstate_merge<D, NTT>(st, red + lane);
     named_bar_sync(1, nct);
     // ---- the item's rows [column][M, Z, O] in shared memory, then out
     if (wpar == first && wslot == 0) {
@@ -455,24 +459,58 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
       named_bar_sync(1, nct);
       if (misc[kMiscLast]) {
         __threadfence();
+        // the unit's items, merged by this CTA: per column (one warp each)
+        // the maximum M over the items and each item's scale 2^(m_i - M)
+        // once, in shared memory; then every output element sums its items'
+        // partial rows with the loads in flight.  Fixed order throughout.
+        const int n = I.n_items;  // <= kItemSlotsPerUnit = 64
+        const size_t pstride = size_t(QR) * (D + 2);
+        const float* pbase = a.partials + size_t(I.first) * pstride;
+        float* sc = red;                              // [n][QR]
+        float* mz = red + kItemSlotsPerUnit * 32;     // [QR][2]: M, Z
+        for (int c = warp; c < QR; c += C::NCW) {
+          float m[2], zz[2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int i = lane + 32 * r;
+            m[r] = i < n ? __ldcg(pbase + i * pstride + c * (D + 2)) : -INFINITY;
+            zz[r] = i < n ? __ldcg(pbase + i * pstride + c * (D + 2) + 1) : 0.f;
+          }
+          float M = fmaxf(m[0], m[1]);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+          float Z = 0.f;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int i = lane + 32 * r;
+            const float f = i < n && m[r] != -INFINITY ? exp2f(m[r] - M) : 0.f;
+            if (i < n) sc[i * 32 + c] = f;
+            Z = fmaf(zz[r], f, Z);
+          }
+#pragma unroll
+          for (int o = 16; o; o >>= 1) Z += __shfl_xor_sync(kFull, Z, o);
+          if (lane == 0) {
+            mz[2 * c] = M;
+            mz[2 * c + 1] = Z;
+          }
+        }
+        named_bar_sync(1, nct);
         for (int j = tid; j < QR * D; j += nct) {
           const int qr = j / D, dim = j % D;
-          const float* pbase = a.partials + (size_t(I.first) * QR + qr) * (D + 2);
-          const size_t pstride = size_t(QR) * (D + 2);
-          float M = -INFINITY;
-          for (int i = 0; i < I.n_items; ++i) M = fmaxf(M, __ldcg(pbase + i * pstride));
-          float A = 0.f, Z = 0.f;
-#pragma unroll 4
-          for (int i = 0; i < I.n_items; ++i) {
-            const float* p = pbase + i * pstride;
-            const float pm = __ldcg(p);
-            const float sc = pm == -INFINITY ? 0.f : exp2f(pm - M);
-            Z = fmaf(__ldcg(p + 1), sc, Z);
-            A = fmaf(__ldcg(p + 2 + dim), sc, A);
+          const float* pa = pbase + qr * (D + 2) + 2 + dim;
+          float A = 0.f;
+          int i = 0;
+          for (; i + 8 <= n; i += 8) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = __ldcg(pa + (i + q) * pstride);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) A = fmaf(v[q], sc[(i + q) * 32 + qr], A);
           }
+          for (; i < n; ++i) A = fmaf(__ldcg(pa + i * pstride), sc[i * 32 + qr], A);
           const int tr = va.t_of_slot[qr / G], h = qr % G;
           const size_t oh = (size_t(I.b) * va.R + tr) * a.H_q + size_t(I.g) * G + h;
-          a.out[oh * D + dim] = A / Z;
+          a.out[oh * D + dim] = A / mz[2 * qr + 1];
         }
         if (tid == 0) a.counters[I.u] = 0;
       }
