@@ -243,25 +243,29 @@ def oracle_rates(wl: W.Workload, slow_frac: float, ts, tf, P: int):
     return P / t_step_one_core, 1.0 / t_step_one_core, t_slow, t_fast, units_per_step
 
 
-def cpu_oracle_rate(wl: W.Workload, slow_frac: float, workers=None):
+def cpu_oracle_rate(wl: W.Workload, slow_frac: float, workers=None, n_steps=None):
     """The fp64 oracle on the host cores: one process per (sequence, KV head)
-    unit of layer 0 (as many as there are cores) runs that unit's whole
-    decode loop on the seeded workload; the job rate scales the mean slow and
-    fast unit-step times to every unit of a decode step."""
+    unit of layer 0 (as many as there are cores) runs the first n_steps
+    decode steps of that unit's loop (all of them by default) on the seeded
+    workload; the job rate scales the mean slow and fast unit-step times to
+    every unit of a decode step."""
+    n_steps = min(n_steps or wl.n_steps, wl.n_steps)
     t_start = time.perf_counter()
     pool = OraclePool(wl, workers)
     gen_s = time.perf_counter() - t_start
     try:
         t0 = time.perf_counter()
-        ts, tf = pool.run(0, wl.n_steps)
+        ts, tf = pool.run(0, n_steps)
         wall = time.perf_counter() - t0
     finally:
         pool.close()
     rate, rate1, t_slow, t_fast, ups = oracle_rates(wl, slow_frac, ts, tf, pool.P)
     sh = wl.shape
+    loop = (f"its whole {wl.n_steps}-step decode loop" if n_steps == wl.n_steps
+            else f"the first {n_steps} steps of its {wl.n_steps}-step decode loop")
     sample = (f"layer 0, sequences 0..{(pool.P - 1) // sh.n_kv_heads}: {pool.P} (sequence, KV head) units "
-              f"of the seeded bf16 workload, each its whole {wl.n_steps}-step decode loop "
-              f"({len(ts)} slow + {len(tf)} fast unit steps at n={wl.n0[0]}..{wl.n0[0] + wl.n_steps - 1}, "
+              f"of the seeded bf16 workload, each {loop} "
+              f"({len(ts)} slow + {len(tf)} fast unit steps at n={wl.n0[0]}..{wl.n0[0] + n_steps - 1}, "
               f"G={sh.group}, d={sh.head_dim}, k={wl.k}) on {pool.P} single-threaded processes in "
               f"{wall:.1f} s (+{gen_s:.1f} s generating the inputs); scaled by {ups} units per decode "
               f"step and slow fraction {slow_frac:.4f}")
@@ -461,7 +465,7 @@ def run_ours(args, rank, world, local_rank):
         wl.seed = rank_seed(wl.seed, rank)
     t_setup = time.perf_counter()
     refine = parse_refine(args.refine)
-    R = Cfg2Runner(wl, local_rank, async_select=not args.sync_select, refine=refine)
+    R = Cfg2Runner(wl, local_rank, async_select=args.async_select, refine=refine)
     setup_s = time.perf_counter() - t_setup
     sfi = R.sfi
     sh = wl.shape
@@ -620,7 +624,7 @@ def run_ours(args, rank, world, local_rank):
             "l2": "inputs larger than L2 (%.1f GB of KV per GPU)" % (
                 sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9),
             "parallelism": f"dp{world} (independent sequences per GPU)",
-            "selector": "in line" if args.sync_select else "overlapped with the next layer",
+            "selector": "overlapped with the next layer" if args.async_select else "in line",
             **({"refine": {"nms_radius": refine[0], "nms_sigma": refine[1], "excl_beta": refine[2]}}
                if refine else {}),
         },
@@ -656,7 +660,8 @@ def run_ours(args, rank, world, local_rank):
     if clk:
         line["clocks"] = clk
     if rank == 0 and not args.no_cpu_baseline:
-        rate, P, sample, extra = cpu_oracle_rate(wl, slow_frac)
+        rate, P, sample, extra = cpu_oracle_rate(wl, slow_frac,
+                                                 n_steps=None if args.cpu_full_loop else 32)
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "decode steps/s", "cores": P,
                                 "kind": "oracle", "sample": sample,
                                 "value_1core": round(extra["value_1core"], 7),
@@ -1010,7 +1015,7 @@ def run_reference(args):
     slow = O.schedule(wl.boundary_trace(), wl.budget)
     frac = float(slow.mean())
     pool = OraclePool(wl)
-    per = 32
+    per = 8
     rates, walls, rate1s = [], [], []
     sample_steps = [0, 0]
     last_ts = []
@@ -1068,11 +1073,14 @@ def main():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-full-loop", action="store_true", help="time the oracle over each unit's "
+                    "whole decode loop (default: its first 32 steps, to keep the run short)")
     ap.add_argument("--clock-log-dir", default=os.environ.get("SFI_CLOCK_LOG_DIR", os.path.join(ROOT, "bench_logs")),
                     help="where the nvidia-smi clock samples of the timed region are written")
-    ap.add_argument("--sync-select", action="store_true",
-                    help="run each layer's selector on the decode stream instead of overlapping it "
-                         "with the next layer's attention")
+    ap.add_argument("--async-select", action="store_true",
+                    help="overlap each layer's selector with the next layer's attention on a side "
+                         "stream (default: the selector runs in line on the decode stream, which "
+                         "measures faster: the persistent attention launch wants every SM)")
     ap.add_argument("--kernel-case", default="", help="comma list of dense,slow,select,fast,fast_contig,mixed (or 'verify' alone): time "
                     "each kernel alone on one 128K layer instead of the decode benchmark")
     ap.add_argument("--refine", default="", help="rho,sigma,beta: decode with the Soft-NMS / "

@@ -46,9 +46,8 @@
  *    past n_b are left untouched.
  *  - Capacity limits (SFI_ERR_CAPACITY beyond them): batch <= 1024;
  *    batch * n_kv_heads <= 4096; for every call that selects (sfi_select,
- *    sfi_select_refined, a decode context) max_len <= 327680, the positions
- *    one selector cluster holds in shared memory.  Further per-call limits
- *    are stated with the call.
+ *    sfi_select_refined, a decode context) max_len <= 327680 positions per
+ *    row.  Further per-call limits are stated with the call.
  */
 #ifndef SFI_H_
 #define SFI_H_

@@ -86,17 +86,15 @@ WsPlan plan_workspace(int B, int H_q, int H_kv, int D, int max_len) {
   p.sel_nu_off = off;
   off += align256(units * kSelMaxChunks * 4);
   p.sel_cnt_off = off;
-  off += align256(units * kSelMaxChunks * 4);
+  off += align256(units * kSelMaxChunks * 2 * 4);
   p.sel_hist_off = off;
-  off += align256(units * 2048 * 4);
-  p.sel_hist2_off = off;
-  off += align256(units * 2048 * 4);
-  p.sel_done_off = off;
-  off += align256(units * 4);
+  off += align256(units * kSelHistWords * 4);
+  p.sel_ctr_off = off;
+  off += align256(units * 4 * 4);
   p.sel_keys_off = off;
   off += align256(units * size_t(max_len) * 4);
-  p.sel_list_off = off;
-  off += align256(units * size_t(max_len) * 8);
+  p.sel_cand_off = off;
+  off += align256(std::min(units, size_t(kSelCandRows)) * size_t(max_len) * 8);
   p.total = off;
   return p;
 }
@@ -105,10 +103,9 @@ void attach_select_scratch(SelectArgs& a, char* ws, const WsPlan& p) {
   a.sel_nu = reinterpret_cast<float*>(ws + p.sel_nu_off);
   a.sel_cnt = reinterpret_cast<uint32_t*>(ws + p.sel_cnt_off);
   a.sel_hist = reinterpret_cast<uint32_t*>(ws + p.sel_hist_off);
-  a.sel_hist2 = reinterpret_cast<uint32_t*>(ws + p.sel_hist2_off);
-  a.sel_done = reinterpret_cast<uint32_t*>(ws + p.sel_done_off);
+  a.sel_ctr = reinterpret_cast<uint32_t*>(ws + p.sel_ctr_off);
   a.sel_keys = reinterpret_cast<uint32_t*>(ws + p.sel_keys_off);
-  a.sel_list = reinterpret_cast<unsigned long long*>(ws + p.sel_list_off);
+  a.sel_cand = reinterpret_cast<unsigned long long*>(ws + p.sel_cand_off);
 }
 
 sfi_status check_layout(const sfi_layout* L) {

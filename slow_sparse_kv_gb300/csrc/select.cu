@@ -14,42 +14,32 @@
 //
 // Selector.  Each selecting unit -- a (sequence, KV head), or a sequence in
 // the per-sequence logit-sum mode -- is cut into C chunks of consecutive
-// positions, and C is chosen so that all units together give about two CTAs
-// per SM: every SM works on the few units of a decode step.  No CTA ever
-// waits for another; three launches, each a programmatic dependent of the
-// one before it, pass their results through the workspace:
-//  1. (fused mode) each chunk sums its key norms over E;
-//  2. each chunk forms the scores (f from the logits on the decode path),
-//     writes s when asked, the order key of every position of E and adds
-//     its histogram of the keys' top 11 bits to the unit's (integer atomics);
-//  3. each chunk reads the unit's histogram, which fixes the top digit d0 of
-//     the k-th largest key, and writes its keys at or above d0 -- as
-//     (key, position), in position order -- to its own region of a list.  The
-//     last chunk CTA of the unit to finish (an atomic counter) finds the two
-//     lower digits among the keys of bin d0 (few: about 2% of E at the decode
-//     workloads) and writes the keys above the k-th, then the lowest-
-//     positioned keys equal to it, in ascending position order, so ties go to
-//     the lower position exactly as the definition says.  It leaves the
-//     histogram and the counter at zero for the next launch.
-// All sums run in a fixed order, so the selection does not depend on the
-// schedule.
+// positions, one CTA each, in one launch.  C is as large as keeps every CTA
+// of the launch resident at once, so that all SMs work on the few units of a
+// decode step; the C CTAs of a unit exchange the key-norm sum, three radix
+// histograms of the order keys (11 + 11 + 10 bits, integer atomics) and
+// their output counts through the workspace, and meet at up to five barriers
+// on a counter of the unit.  The keys stay in the CTA (shared memory) when
+// they fit.  Ties at the k-th key go to the lower positions exactly as the
+// definition says, and every sum runs in a fixed order, so the selection
+// does not depend on the schedule.
 #include <math.h>
 
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
-#include "warp_hist.cuh"
 
 namespace sfi {
 
 constexpr int kFpassThreads = 256;
-constexpr int kSelT = 512;      // threads of a score or list CTA
-constexpr int kSelNuT = 256;    // threads of a key-norm sum CTA
+constexpr int kSelT = 512;      // threads of a selector CTA
 constexpr int kSelU = 8;        // positions in flight per thread
 constexpr int kRadixBins = 2048;
 constexpr int kRadixShift0 = 21;  // digits: bits 31..21, 20..10, 9..0 of the order key
 constexpr int kRadixShift1 = 10;
-constexpr int kSelMinChunk = 2048;  // positions per chunk, at least
-constexpr int kRun = 8;             // consecutive list positions or entries per thread and tile
-constexpr int kListCap = 12288;     // list entries the finisher stages in shared memory (96 KB)
+constexpr int kSelMinChunk = 2048;     // positions per chunk, at least
+constexpr int kSelSmemMax = 100 << 10;  // dynamic shared memory of a selector CTA, at most
 
 // The G logits of one position ([pos][G] rows are 4*G-byte aligned).
 template <int G>
@@ -125,25 +115,26 @@ __device__ float sel_block_sum(float v, float* sh) {
   return r;
 }
 
-// Exclusive block scan of one packed (gt << 16 | eq) count per thread; also
-// returns the block total.  Two barriers.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t& total) {
+// Exclusive block scan of one value per thread (a packed pair of counts);
+// also returns the block total.  Two barriers.
+template <typename T>
+__device__ __forceinline__ T block_excl_scan(T v, T* sh, T& total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  uint32_t incl = v;
+  T incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    const T y = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) sh[w] = incl;
   __syncthreads();
   if (w == 0) {
     const int nw = blockDim.x >> 5;
-    uint32_t x = lane < nw ? sh[lane] : 0u;
-    uint32_t xi = x;
+    T x = lane < nw ? sh[lane] : T(0);
+    T xi = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, xi, o);
+      const T y = __shfl_up_sync(kFull, xi, o);
       if (lane >= o) xi += y;
     }
     if (lane < nw) sh[lane] = xi - x;
@@ -151,7 +142,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, ui
   }
   __syncthreads();
   total = sh[32];
-  const uint32_t r = sh[w] + incl - v;
+  const T r = sh[w] + incl - v;
   __syncthreads();
   return r;
 }
@@ -233,69 +224,200 @@ __device__ __forceinline__ int sel_unit(const SelectArgs& a, int j, int c, int C
   return 0;
 }
 
-// The three launches are programmatic dependents of the launch before them:
-// each may be scheduled while its predecessor drains, and waits for it before
-// any global access.
+// The launch is a programmatic dependent of the launch before it: it may be
+// scheduled while its predecessor drains, and waits for it before any global
+// access.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Launch 1 (fused mode): this chunk's sum of key norms over E.
-__global__ void __launch_bounds__(kSelNuT) sel_nu_kernel(const SelectArgs a) {
-  __shared__ float sh[33];
-  pdl_wait();
-  pdl_trigger();
-  SelUnit s;
-  if (sel_unit(a, blockIdx.y, blockIdx.x, gridDim.x, s) != 0) return;
-  const float* kn = a.knorm + size_t(s.u) * a.max_len;
-  float part = 0.f;
-  constexpr int V = 16;  // loads in flight per thread
-  for (int base = s.e0; base < s.e1; base += kSelNuT * V) {
-    float x[V];
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const int i = base + j * kSelNuT + int(threadIdx.x);
-      x[j] = i < s.e1 ? kn[i] : 0.f;
-    }
-#pragma unroll
-    for (int j = 0; j < V; ++j) part += x[j];
-  }
-  const float t = sel_block_sum(part, sh);
-  if (threadIdx.x == 0) a.sel_nu[size_t(s.u) * kSelMaxChunks + blockIdx.x] = t;
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// Launch 2: scores, order keys and the top-digit histogram.  EV_G > 0: the
-// evidence comes from the attention kernel's log2-scaled logits [pos][EV_G]
-// and per-head (M, Z) (decode path); EV_G == 0: `evidence` holds f (or the
-// per-KV-head logit sums).
+// Barrier of the C chunk CTAs of one unit on the unit's counter, in two
+// halves so that independent work can run between them.  The counter rests
+// with its low 31 bits at zero: chunk 0 adds 2^31 - (C - 1) and every other
+// chunk 1, so bit 31 flips exactly when the last CTA arrives and the low bits
+// are back at zero -- no reset, whatever C the next launch has.  Arrive:
+// after the block's writes, one release add; thread 0 keeps the value it
+// replaced.  Wait: until bit 31 differs from that value's.  Every CTA
+// arrives at every barrier once, also after one of its waits gave up; a
+// wait gives up after `limit` SM clocks and sets SFI_DEV_WAIT_TIMEOUT, and
+// returns false from then on (the CTA finishes without waiting).
+__device__ __forceinline__ uint32_t unit_arrive(uint32_t* ctr, int c, int C) {
+  __syncthreads();
+  uint32_t old = 0;
+  if (threadIdx.x == 0) {
+    const uint32_t add = c == 0 ? 0x80000000u - uint32_t(C - 1) : 1u;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(old) : "l"(ctr), "r"(add) : "memory");
+  }
+  return old;
+}
+__device__ __forceinline__ bool unit_wait(const uint32_t* ctr, uint32_t old, bool ok, long long limit,
+                                          uint32_t* status, int* sh_ok) {
+  if (threadIdx.x == 0) {
+    if (ok && ((ld_acquire_u32(ctr) ^ old) & 0x80000000u) == 0) {
+      const long long t0 = clock64();
+      while (((ld_acquire_u32(ctr) ^ old) & 0x80000000u) == 0) {
+        if (clock64() - t0 > limit) {
+          ok = false;
+          set_status(status, SFI_DEV_WAIT_TIMEOUT);
+          break;
+        }
+      }
+    }
+    *sh_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *sh_ok != 0;
+}
+
+// Shared-memory histogram count (native shared atomics resolve equal bins
+// within a warp faster than any software aggregation).
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
+  if (active) atomicAdd(hist + bin, 1u);
+}
+
+// Sum of one count per thread over the block.  Two barriers.
+__device__ __forceinline__ uint32_t block_count(uint32_t v, uint32_t* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_down_sync(kFull, v, o);
+  if (lane == 0) sh[w] = v;
+  __syncthreads();
+  uint32_t t = 0;
+  for (int i = 0; i < int(blockDim.x >> 5); ++i) t += sh[i];
+  __syncthreads();
+  return t;
+}
+
+// The selector, one launch.  Block (c, j): chunk c of selecting unit j.
+//  pass 1  (fused mode) the chunk's key norms over E and their sum, published
+//          at barrier 1, whose wait comes after the evidence loads; the
+//          chunk's evidence (f from the logits and (M, Z) on the decode path);
+//  pass 2  the ranked scores, s when asked, the order keys (in shared memory
+//          when the chunk fits, else in the workspace) and their top-11-bit
+//          histogram; barrier 2 completes the unit's histogram, which fixes
+//          the top digit d0 of the k-th largest key;
+//  digits  each chunk writes its keys of bin d0 -- few -- as (key, position)
+//          to its own region of the unit's candidate list and publishes its
+//          count of keys above bin d0 (barrier 3); every CTA then gathers the
+//          candidates and finds the two lower digits among them -- tau, the
+//          k-th key, and take_eq, the keys equal to tau that are kept -- and
+//          the lower chunks' counts of kept keys.  When bin d0 holds more
+//          than kSelCandCap keys, two histogram rounds over all keys
+//          (barriers 3 and 4) and a count exchange (barrier 5) do the same;
+//  output  every kept position goes to slot (keys above tau before it) +
+//          min(keys equal to tau before it, take_eq): the keys above tau,
+//          then the lowest-positioned take_eq keys equal to it, ascending.
+// With C == 1 a CTA holds its whole unit and waits for no other.  Each
+// global histogram is zeroed, a slice per chunk, after the barrier that
+// follows its last read.
 template <int EV_G>
-__global__ void __launch_bounds__(kSelT, 2) sel_score_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
+  extern __shared__ __align__(16) uint32_t sel_smem[];
   __shared__ uint32_t hist[kRadixBins];
+  __shared__ uint32_t scan_sh[33];
+  __shared__ unsigned long long scan64[33];
+  __shared__ float shf[33];
+  __shared__ uint32_t c_off[kSelMaxChunks + 1];  // candidate offsets of the chunks
+  __shared__ uint32_t sh_digit, sh_above, sh_gb, sh_qb, sh_nc;
+  __shared__ int sh_ok;
   pdl_wait();
   pdl_trigger();
-  const int tid = threadIdx.x, c = blockIdx.x;
+  const int tid = threadIdx.x, c = blockIdx.x, C = gridDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kSelT / 32;
+  const unsigned lt = (1u << lane) - 1u;
   SelUnit s;
-  const int r = sel_unit(a, blockIdx.y, c, gridDim.x, s);
-  if (r != 0) {
-    if (r == 2 && c == 0 && tid == 0) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
-    return;  // uniform over the unit
+  const int rs = sel_unit(a, blockIdx.y, c, C, s);
+  if (rs != 0) {
+    if (rs == 2 && c == 0 && tid == 0) set_status(a.status, SFI_DEV_LEN_OVER_CAP);
+    return;  // uniform over the unit: no barrier of it is reached
   }
-  float coef = 0.f;
-  if (s.prior) {
-    // the chunks' key-norm sums in one fixed order: every thread of every CTA
-    // of the unit forms the same value
-    const float* pn = a.sel_nu + size_t(s.u) * kSelMaxChunks;
-    const int lane = tid & 31, C = gridDim.x;
-    float x = (lane < C ? pn[lane] : 0.f) + (lane + 32 < C ? pn[lane + 32] : 0.f);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) x += __shfl_down_sync(kFull, x, o);
-    x = __shfl_sync(kFull, x, 0);
-    coef = x > 0.f ? a.lambda / x : 0.f;
-  }
+  const bool multi = C > 1;
+  uint32_t* ctr = a.sel_ctr + size_t(s.u) * 4;
+  uint32_t* gh = a.sel_hist + size_t(s.u) * kSelHistWords;
+  uint32_t* cnt = a.sel_cnt + size_t(s.u) * kSelMaxChunks * 2;
+  // shared memory: [keys | key norms, later the candidates] when the chunk
+  // fits, else [candidates] with the keys in the workspace
+  uint32_t* keys = a.keys_smem ? sel_smem : a.sel_keys + size_t(s.u) * a.max_len + s.p0;
+  float* nu_s = a.keys_smem ? reinterpret_cast<float*>(sel_smem + a.smem_split) : nullptr;
+  unsigned long long* cands = reinterpret_cast<unsigned long long*>(sel_smem + a.smem_split);
+  bool ok = true;
+  auto barrier = [&]() {
+    const uint32_t old = unit_arrive(ctr, c, C);
+    ok = unit_wait(ctr, old, ok, a.wait_cycles, a.status, &sh_ok);
+  };
+  // this chunk's slice of global histogram r back to zero (no CTA reads it
+  // any more)
+  auto zero_slice = [&](int r) {
+    const int b0 = c * kRadixBins / C, b1 = (c + 1) * kRadixBins / C;
+    for (int i = b0 + tid; i < b1; i += kSelT) gh[r * kRadixBins + i] = 0u;
+  };
   if (s.need_radix)
     for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
   __syncthreads();
+
+  const int lo = s.lo, hi = s.hi;
+  const float* kn = s.prior ? a.knorm + size_t(s.u) * a.max_len : nullptr;
+  float* srow = a.s ? a.s + size_t(s.u) * a.max_len : nullptr;
+  // exclusivity: the fused score is written to s as it is; the selection
+  // ranks it times exp(-beta * picks of the earlier KV heads)
+  const uint8_t* exrow = s.prior && a.excl ? a.excl + size_t(s.b) * a.max_len : nullptr;
+  int32_t* out_idx = a.idx + size_t(s.per_seq ? s.b * a.H_kv : s.unit) * a.k;
+  const int n_rows = s.per_seq ? a.H_kv : 1;  // idx rows that receive the set
+  const float w_f = s.prior ? 1.0f - a.lambda : 1.0f;
+  // score of position i from its evidence; key, s, histogram, and the whole
+  // of E when it is all kept (position lo + t goes to slot t)
+  auto emit = [&](int i, bool in, float ev, float kv, uint32_t cx, float coef) {
+    const bool e = in && i >= lo && i < hi;
+    if (!in) return;
+    float v = w_f * ev;
+    if (s.prior && e) v = fmaf(coef, kv, v);
+    if (srow) srow[i] = v;
+    v *= excl_factor(cx, a.excl_beta);
+    const uint32_t key = order_key(v);
+    keys[i - s.p0] = key;
+    if (e) {
+      if (s.need_radix) hist_add(hist, key >> kRadixShift0, true);
+      else
+        for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + (i - lo)] = i;
+    }
+  };
+
+  // ---- pass 1
+  float coef = 0.f;
+  uint32_t bar1_old = 0;
+  if (s.prior) {
+    float part = 0.f;
+    for (int base = s.e0; base < s.e1; base += kSelT * kSelU) {
+      float x[kSelU];
+#pragma unroll
+      for (int j = 0; j < kSelU; ++j) {
+        const int i = base + j * kSelT + tid;
+        x[j] = i < s.e1 ? kn[i] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kSelU; ++j) {
+        const int i = base + j * kSelT + tid;
+        part += x[j];
+        if (nu_s && i < s.e1) nu_s[i - s.p0] = x[j];
+      }
+    }
+    const float t = sel_block_sum(part, shf);
+    if (multi) {
+      if (tid == 0) a.sel_nu[size_t(s.u) * kSelMaxChunks + c] = t;
+      bar1_old = unit_arrive(ctr, c, C);  // barrier 1: waited for after the evidence loads
+    } else {
+      coef = t > 0.f ? a.lambda / t : 0.f;
+    }
+  }
   float M[EV_G > 0 ? EV_G : 1], iz[EV_G > 0 ? EV_G : 1];
   if constexpr (EV_G > 0) {
 #pragma unroll
@@ -305,29 +427,16 @@ __global__ void __launch_bounds__(kSelT, 2) sel_score_kernel(const SelectArgs a)
       iz[hh] = 1.0f / a.stats[qh * 2 + 1];
     }
   }
-  const float* kn = s.prior ? a.knorm + size_t(s.u) * a.max_len : nullptr;
-  float* srow = a.s ? a.s + size_t(s.u) * a.max_len : nullptr;
-  // exclusivity: the fused score is written to s as it is; the selection
-  // ranks it times exp(-beta * picks of the earlier KV heads)
-  const uint8_t* exrow = s.prior && a.excl ? a.excl + size_t(s.b) * a.max_len : nullptr;
-  uint32_t* krow = a.sel_keys + size_t(s.u) * a.max_len;
-  int32_t* out_idx = a.idx + size_t(s.per_seq ? s.b * a.H_kv : s.unit) * a.k;
-  const int n_rows = s.per_seq ? a.H_kv : 1;  // idx rows that receive the set
-  const float w_f = s.prior ? 1.0f - a.lambda : 1.0f;
   // U positions per thread at a time, every load issued before any is used
   // (fewer when each position brings G logits, so two CTAs fit an SM)
   constexpr int U = EV_G >= 8 ? 2 : (EV_G >= 4 ? 4 : kSelU);
   for (int base = s.p0; base < s.p1; base += kSelT * U) {
     float lg[U][EV_G > 0 ? EV_G : 1];
-    float ev[U], kv[U];
-    uint32_t cx[U];
+    float ev[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const int i = base + j * kSelT + tid;
-      const bool e = i >= s.lo && i < s.hi;
       ev[j] = 0.f;
-      kv[j] = 0.f;
-      cx[j] = 0u;
       if (i < s.p1) {
         if constexpr (EV_G > 0) {
           load_row<EV_G>(a.logits + (size_t(s.u) * a.max_len + i) * EV_G, lg[j]);
@@ -337,32 +446,54 @@ __global__ void __launch_bounds__(kSelT, 2) sel_score_kernel(const SelectArgs a)
         } else {
           ev[j] = a.evidence[size_t(s.u) * a.max_len + i];
         }
-        if (s.prior && e) kv[j] = kn[i];
-        if (exrow && e) cx[j] = exrow[i];
       }
     }
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const int i = base + j * kSelT + tid;
       const bool in = i < s.p1;
-      const bool e = in && i >= s.lo && i < s.hi;
-      uint32_t key = 0u;
       if (in) {
         if constexpr (EV_G > 0) ev[j] = evidence_from_logits<EV_G>(lg[j], M, iz);
-        float v = w_f * ev[j];
-        if (s.prior && e) v = fmaf(coef, kv[j], v);
-        if (srow) srow[i] = v;
-        v *= excl_factor(cx[j], a.excl_beta);
-        key = order_key(v);
-        if (e) {
-          if (s.need_radix) {
-            krow[i] = key;
-          } else {  // keep all of E: position lo + t goes to slot t
-            for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + (i - s.lo)] = i;
-          }
-        }
       }
-      if (s.need_radix) hist_add(hist, key >> kRadixShift0, e);
+      if (s.prior) {
+        if (in) keys[i - s.p0] = __float_as_uint(ev[j]);  // the key once the prior is known
+      } else {
+        emit(i, in, ev[j], 0.f, 0u, 0.f);
+      }
+    }
+  }
+
+  // ---- pass 2 (fused mode): the prior needs the unit's key-norm sum
+  if (s.prior) {
+    if (multi) {
+      ok = unit_wait(ctr, bar1_old, ok, a.wait_cycles, a.status, &sh_ok);
+      // the chunks' sums in one fixed order: every CTA of the unit forms the
+      // same value
+      const float* pn = a.sel_nu + size_t(s.u) * kSelMaxChunks;
+      float x = (lane < C ? __ldcg(pn + lane) : 0.f) + (lane + 32 < C ? __ldcg(pn + lane + 32) : 0.f);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) x += __shfl_down_sync(kFull, x, o);
+      x = __shfl_sync(kFull, x, 0);
+      coef = x > 0.f ? a.lambda / x : 0.f;
+    } else {
+      __syncthreads();  // the key norms kept in shared memory
+    }
+    for (int base = s.p0; base < s.p1; base += kSelT * kSelU) {
+      float kv[kSelU];
+      uint32_t cx[kSelU];
+#pragma unroll
+      for (int j = 0; j < kSelU; ++j) {
+        const int i = base + j * kSelT + tid;
+        const bool e = i < s.p1 && i >= lo && i < hi;
+        kv[j] = e ? (nu_s ? nu_s[i - s.p0] : kn[i]) : 0.f;
+        cx[j] = exrow && e ? exrow[i] : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < kSelU; ++j) {
+        const int i = base + j * kSelT + tid;
+        const bool in = i < s.p1;
+        emit(i, in, in ? __uint_as_float(keys[i - s.p0]) : 0.f, kv[j], cx[j], coef);
+      }
     }
   }
   if (c == 0 && tid == 0) {
@@ -372,233 +503,221 @@ __global__ void __launch_bounds__(kSelT, 2) sel_score_kernel(const SelectArgs a)
       a.count[s.u] = s.keff;
     }
   }
-  if (s.need_radix) {
+  if (!s.need_radix) return;
+
+  const int e0 = s.e0 - s.p0, e1 = s.e1 - s.p0;  // this chunk's part of E, in keys[]
+  // ---- top digit
+  if (multi) {
     __syncthreads();
-    uint32_t* gh = a.sel_hist + size_t(s.u) * kRadixBins;
     for (int i = tid; i < kRadixBins; i += kSelT)
       if (hist[i]) atomicAdd(gh + i, hist[i]);
+    barrier();  // 2
+    for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = __ldcg(gh + i);
   }
-}
-
-// Launch 3: per chunk, the ordered list of keys at or above the k-th key's
-// top digit, and the histogram of the next 11 bits of its keys in that
-// digit's bin; the unit's last chunk CTA to finish completes the selection.
-__global__ void __launch_bounds__(kSelT) sel_list_kernel(const SelectArgs a) {
-  __shared__ uint32_t hist[kRadixBins];
-  extern __shared__ unsigned long long lst[];     // finisher: the unit's list (kListCap entries)
-  __shared__ uint32_t cnt_c[kSelMaxChunks + 1];  // finisher: entries per chunk
-  __shared__ uint32_t offs_c[kSelMaxChunks + 1]; // finisher: their exclusive offsets
-  __shared__ uint32_t gt_c[kSelMaxChunks + 1];   // finisher: keys above tau per chunk, then offsets
-  __shared__ uint32_t eq_c[kSelMaxChunks + 1];   // finisher: keys equal to tau per chunk, then offsets
-  __shared__ uint32_t scan_sh[33];
-  __shared__ uint32_t sh_digit, sh_above, sh_last;
-  pdl_wait();
-  pdl_trigger();
-  const int tid = threadIdx.x, c = blockIdx.x, C = gridDim.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  constexpr int NW = kSelT / 32;
-  const unsigned lt = (1u << lane) - 1u;
-  SelUnit s;
-  if (sel_unit(a, blockIdx.y, c, C, s) != 0 || !s.need_radix) return;  // uniform over the unit
-  const uint32_t* krow = a.sel_keys + size_t(s.u) * a.max_len;
-  const size_t row0 = size_t(s.u) * a.max_len;
-  uint32_t* gh = a.sel_hist + size_t(s.u) * kRadixBins;
-  uint32_t* gh2 = a.sel_hist2 + size_t(s.u) * kRadixBins;
-  // this chunk's keys (thread t: kRun consecutive positions of each tile of
-  // kSelT * kRun) are loaded together with the unit's histogram
-  const int ntile = (s.e1 - s.e0 + kSelT * kRun - 1) / (kSelT * kRun);
-  const bool one_tile = ntile <= 1;
-  uint32_t key[kRun];
-  const int i0 = s.e0 + tid * kRun;
-  if (one_tile) {
-#pragma unroll
-    for (int j = 0; j < kRun; ++j) key[j] = i0 + j < s.e1 ? krow[i0 + j] : 0u;
-  }
-  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = __ldcg(gh + i);
   __syncthreads();
   block_pick_digit<kRadixBins>(hist, uint32_t(s.keff), &sh_digit, &sh_above, scan_sh);
   const uint32_t d0 = sh_digit;
-  const uint32_t krem0 = uint32_t(s.keff) - sh_above;
-  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;  // now: next-digit histogram
-  __syncthreads();
-  // ---- keys at or above d0, in position order, into this chunk's region of
-  // the unit's list (starting at its first position of E); one block scan per
-  // tile; the keys of bin d0 also go into the next-digit histogram
-  unsigned long long* lrow = a.sel_list + row0 + s.e0;
-  uint32_t tot = 0;
-  for (int t = 0; t < ntile; ++t) {
-    const int ib = s.e0 + t * kSelT * kRun + tid * kRun;
-    if (!one_tile) {
-#pragma unroll
-      for (int j = 0; j < kRun; ++j) key[j] = ib + j < s.e1 ? krow[ib + j] : 0u;
+  uint32_t krem = uint32_t(s.keff) - sh_above;
+  const bool by_cands = multi && hist[d0] <= uint32_t(kSelCandCap);  // uniform over the unit
+  uint32_t tau, take_eq;
+  if (by_cands) {
+    // ---- this chunk's keys of bin d0 to its region of the candidate list
+    // (starting at its first position of E), and its count of keys above
+    unsigned long long* row = a.sel_cand + size_t(blockIdx.y) * a.max_len;
+    if (tid == 0) sh_nc = 0;
+    __syncthreads();
+    uint32_t above = 0;
+    for (int b0 = e0; b0 < e1; b0 += kSelT) {
+      const int i = b0 + tid;
+      const uint32_t key = i < e1 ? keys[i] : 0u;
+      const uint32_t dg = key >> kRadixShift0;
+      above += (i < e1 && dg > d0) ? 1u : 0u;
+      const unsigned m = __ballot_sync(kFull, i < e1 && dg == d0);
+      // slots in the chunk's region in any order: only counts and
+      // histograms are taken over the candidates
+      uint32_t at = 0;
+      if (lane == 0 && m) at = atomicAdd(&sh_nc, uint32_t(__popc(m)));
+      at = __shfl_sync(kFull, at, 0) + __popc(m & lt);
+      if ((m >> lane) & 1u) row[s.e0 + at] = (static_cast<unsigned long long>(key) << 32) | uint32_t(s.p0 + i);
     }
-    uint32_t nm = 0;
-#pragma unroll
-    for (int j = 0; j < kRun; ++j) nm += (ib + j < s.e1 && (key[j] >> kRadixShift0) >= d0) ? 1u : 0u;
-    uint32_t ttot;
-    uint32_t at = tot + block_excl_scan(nm, scan_sh, ttot);
-#pragma unroll
-    for (int j = 0; j < kRun; ++j) {
-      const bool in = ib + j < s.e1;
-      const uint32_t dg = key[j] >> kRadixShift0;
-      if (in && dg >= d0)
-        lrow[at++] = (static_cast<unsigned long long>(key[j]) << 32) | uint32_t(ib + j);
-      hist_add(hist, (key[j] >> kRadixShift1) & (kRadixBins - 1), in && dg == d0);
+    above = block_count(above, scan_sh);
+    if (tid == 0) {
+      cnt[2 * c] = above;
+      cnt[2 * c + 1] = sh_nc;
     }
-    tot += ttot;
+    barrier();  // 3
+    zero_slice(0);
+    // ---- every CTA: the chunks' counts, then the candidates in chunk order
+    if (warp == 0) {
+      const uint32_t n0 = lane < C ? __ldcg(cnt + 2 * lane + 1) : 0u;
+      const uint32_t n1 = lane + 32 < C ? __ldcg(cnt + 2 * (lane + 32) + 1) : 0u;
+      uint32_t g = 0;
+      for (int cc = lane; cc < c; cc += 32) g += __ldcg(cnt + 2 * cc);
+      uint32_t i0 = n0, i1 = n1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
+        if (lane >= o) i0 += y0, i1 += y1;
+      }
+      const uint32_t t0 = __shfl_sync(kFull, i0, 31);
+      c_off[lane] = i0 - n0;
+      c_off[lane + 32] = t0 + i1 - n1;
+      if (lane == 31) c_off[kSelMaxChunks] = t0 + i1;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) g += __shfl_down_sync(kFull, g, o);
+      if (lane == 0) sh_gb = g;  // keys above bin d0 in the lower chunks
+    }
+    for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
+    __syncthreads();
+    const uint32_t nc = min(c_off[kSelMaxChunks], uint32_t(kSelCandCap));
+    for (int cc = warp; cc < C; cc += NW) {  // each warp whole chunks, 8 loads in flight per lane
+      const uint32_t o0 = c_off[cc], n = min(c_off[cc + 1], nc) - min(o0, nc);
+      const unsigned long long* src = row + sel_chunk_e0(s, cc);
+      for (uint32_t jb = 0; jb < n; jb += 32 * 8) {
+        unsigned long long ent[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t jj = jb + uint32_t(r) * 32 + lane;
+          ent[r] = jj < n ? __ldcg(src + jj) : 0ull;
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t jj = jb + uint32_t(r) * 32 + lane;
+          if (jj < n) cands[o0 + jj] = ent[r];
+        }
+      }
+    }
+    __syncthreads();
+    // ---- the two lower digits among the candidates
+    for (uint32_t e = tid; e < nc; e += kSelT)
+      hist_add(hist, (uint32_t(cands[e] >> 32) >> kRadixShift1) & (kRadixBins - 1), true);
+    __syncthreads();
+    block_pick_digit<kRadixBins>(hist, krem, &sh_digit, &sh_above, scan_sh);
+    const uint32_t p1 = (d0 << (kRadixShift0 - kRadixShift1)) | sh_digit;  // top 22 bits
+    krem -= sh_above;
+    for (int i = tid; i < (1 << kRadixShift1); i += kSelT) hist[i] = 0;
+    __syncthreads();
+    for (uint32_t e = tid; e < nc; e += kSelT) {
+      const uint32_t key = uint32_t(cands[e] >> 32);
+      hist_add(hist, key & ((1u << kRadixShift1) - 1u), (key >> kRadixShift1) == p1);
+    }
+    __syncthreads();
+    block_pick_digit<1 << kRadixShift1>(hist, krem, &sh_digit, &sh_above, scan_sh);
+    tau = (p1 << kRadixShift1) | sh_digit;
+    take_eq = krem - sh_above;
+    // candidates of the lower chunks above / equal to tau
+    uint32_t g = 0, q = 0;
+    const uint32_t nlow = min(c_off[c], nc);
+    for (uint32_t e = tid; e < nlow; e += kSelT) {
+      const uint32_t key = uint32_t(cands[e] >> 32);
+      g += key > tau ? 1u : 0u;
+      q += key == tau ? 1u : 0u;
+    }
+    g = block_count(g, scan_sh);
+    q = block_count(q, scan_sh);
+    if (tid == 0) {
+      sh_gb += g;
+      sh_qb = q;
+    }
+  } else {
+    // ---- the two lower digits by histogram rounds over all keys: each
+    // round histograms the next digit of the keys that share the prefix so
+    // far, takes the unit's total and picks the digit holding the krem-th key
+    uint32_t prefix = d0;
+    for (int round = 1; round < 3; ++round) {
+      const int width = round == 2 ? kRadixShift1 : kRadixShift0 - kRadixShift1;  // 11, 10
+      const int shift = round == 1 ? kRadixShift1 : 0;
+      const int hs = shift + width;
+      __syncthreads();  // the last histogram has been read
+      for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
+      __syncthreads();
+      for (int b0 = e0; b0 < e1; b0 += kSelT * kSelU) {
+        uint32_t kk[kSelU];
+#pragma unroll
+        for (int j = 0; j < kSelU; ++j) {
+          const int i = b0 + j * kSelT + tid;
+          kk[j] = i < e1 ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < kSelU; ++j) {
+          const int i = b0 + j * kSelT + tid;
+          hist_add(hist, (kk[j] >> shift) & ((1u << width) - 1u), i < e1 && (kk[j] >> hs) == prefix);
+        }
+      }
+      if (multi) {
+        __syncthreads();
+        uint32_t* gr = gh + round * kRadixBins;
+        for (int i = tid; i < (1 << width); i += kSelT)
+          if (hist[i]) atomicAdd(gr + i, hist[i]);
+        barrier();  // 3, 4
+        zero_slice(round - 1);
+        for (int i = tid; i < (1 << width); i += kSelT) hist[i] = __ldcg(gr + i);
+      }
+      __syncthreads();
+      if (round == 1) block_pick_digit<kRadixBins>(hist, krem, &sh_digit, &sh_above, scan_sh);
+      else block_pick_digit<1 << kRadixShift1>(hist, krem, &sh_digit, &sh_above, scan_sh);
+      prefix = (prefix << width) | sh_digit;
+      krem -= sh_above;
+    }
+    tau = prefix;
+    take_eq = krem;
   }
-  __syncthreads();
-  for (int i = tid; i < kRadixBins; i += kSelT)
-    if (hist[i]) atomicAdd(gh2 + i, hist[i]);
-  if (tid == 0) a.sel_cnt[size_t(s.u) * kSelMaxChunks + c] = tot;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh_last = atomicAdd(a.sel_done + s.u, 1u) == uint32_t(C - 1);
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
 
-  // ---------------------------------------------------------------- finisher
-  // The second digit d1 comes from the chunks' next-digit histograms; the
-  // last 10 bits from the few keys with prefix (d0, d1).  Every walk over the
-  // lists gives each warp whole chunks (entries of chunk c: kRun per lane in
-  // flight, in position order) -- no search for an entry's chunk.
-  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = __ldcg(gh2 + i);
-  for (int i = tid; i < C; i += kSelT) {
-    cnt_c[i] = __ldcg(a.sel_cnt + size_t(s.u) * kSelMaxChunks + i);
-    gt_c[i] = 0u;
-    eq_c[i] = 0u;
+  // ---- ordered output: each warp walks one contiguous segment of the
+  // chunk's part of E (lane l at base + l); a counting walk, one block scan
+  // and the lower chunks' totals give every warp its first slot
+  const int len = max(e1 - e0, 0);
+  const int seg = ((len + NW - 1) / NW + 31) / 32 * 32;
+  const int s0 = min(e1, e0 + warp * seg), s1 = min(e1, s0 + seg);
+  uint32_t wg = 0, wq = 0;
+  for (int base = s0; base < s1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < s1 ? keys[i] : 0u;
+    wg += __popc(__ballot_sync(kFull, i < s1 && key > tau));
+    wq += __popc(__ballot_sync(kFull, i < s1 && key == tau));
   }
-  __syncthreads();
-  if (warp == 0) {  // exclusive entry offsets of the chunks (two per lane)
-    const uint32_t x0 = lane < C ? cnt_c[lane] : 0u, x1 = lane + 32 < C ? cnt_c[lane + 32] : 0u;
-    uint32_t i0 = x0, i1 = x1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
-      if (lane >= o) i0 += y0, i1 += y1;
+  unsigned long long tot;
+  const unsigned long long ex = block_excl_scan<unsigned long long>(
+      lane == 0 ? (static_cast<unsigned long long>(wg) << 32) | wq : 0ull, scan64, tot);
+  const unsigned long long w_ex = __shfl_sync(kFull, ex, 0);
+  if (multi && !by_cands) {
+    if (tid == 0) {
+      cnt[2 * c] = uint32_t(tot >> 32);
+      cnt[2 * c + 1] = uint32_t(tot);
     }
-    const uint32_t t0 = __shfl_sync(kFull, i0, 31);
-    offs_c[lane] = i0 - x0;
-    offs_c[lane + 32] = t0 + i1 - x1;
-    if (lane == 31) offs_c[kSelMaxChunks] = t0 + i1;
-  }
-  block_pick_digit<kRadixBins>(hist, krem0, &sh_digit, &sh_above, scan_sh);  // (barriers)
-  const uint32_t p1 = (d0 << (kRadixShift0 - kRadixShift1)) | sh_digit;  // top 22 bits
-  const uint32_t krem1 = krem0 - sh_above;
-  const uint32_t NE = offs_c[C];  // chunks past C count 0
-  // The unit's list, staged in shared memory when it fits: every thread
-  // loads kRun * 2 entries at once (the entry's chunk from the offsets), so
-  // the walks below read shared memory only.
-  const bool staged = NE <= uint32_t(kListCap);
-  if (staged) {
-    constexpr int V = 2 * kRun;
-    for (uint32_t tb = 0; tb < NE; tb += kSelT * V) {
-      unsigned long long ent[V];
-#pragma unroll
-      for (int r = 0; r < V; ++r) {
-        const uint32_t e = tb + uint32_t(r) * kSelT + tid;
-        ent[r] = 0ull;
-        if (e < NE) {
-          int lo = 0, hi = C - 1;  // chunk holding e: the largest c with offs_c[c] <= e
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (offs_c[mid] <= e) lo = mid;
-            else hi = mid - 1;
-          }
-          ent[r] = __ldcg(a.sel_list + row0 + sel_chunk_e0(s, lo) + (e - offs_c[lo]));
-        }
+    barrier();  // 5
+    zero_slice(2);
+    if (warp == 0) {  // totals of the lower chunks
+      uint32_t g = 0, q = 0;
+      for (int cc = lane; cc < c; cc += 32) {
+        g += __ldcg(cnt + 2 * cc);
+        q += __ldcg(cnt + 2 * cc + 1);
       }
 #pragma unroll
-      for (int r = 0; r < V; ++r) {
-        const uint32_t e = tb + uint32_t(r) * kSelT + tid;
-        if (e < NE) lst[e] = ent[r];
+      for (int o = 16; o; o >>= 1) {
+        g += __shfl_down_sync(kFull, g, o);
+        q += __shfl_down_sync(kFull, q, o);
+      }
+      if (lane == 0) {
+        sh_gb = g;
+        sh_qb = q;
       }
     }
-  }
-  for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
-  __syncthreads();
-  // each warp takes whole chunks, their entries in position order
-  auto walk = [&](auto&& body) {
-    for (int cc = warp; cc < C; cc += NW) {
-      const uint32_t nc = cnt_c[cc];
-      if (staged) {
-        const unsigned long long* lc = lst + offs_c[cc];
-        for (uint32_t jb = 0; jb < nc; jb += 32) {
-          const uint32_t jj = jb + lane;
-          body(cc, jj < nc, jj < nc ? lc[jj] : 0ull);
-        }
-      } else {
-        const unsigned long long* lc = a.sel_list + row0 + sel_chunk_e0(s, cc);
-        for (uint32_t jb = 0; jb < nc; jb += 32 * kRun) {
-          unsigned long long ent[kRun];
-#pragma unroll
-          for (int r = 0; r < kRun; ++r) {
-            const uint32_t jj = jb + uint32_t(r) * 32 + lane;
-            ent[r] = jj < nc ? __ldcg(lc + jj) : 0ull;
-          }
-#pragma unroll
-          for (int r = 0; r < kRun; ++r) body(cc, jb + uint32_t(r) * 32 + lane < nc, ent[r]);
-        }
-      }
-    }
-  };
-  // last 10 bits among the keys with prefix p1
-  walk([&](int, bool v, unsigned long long e) {
-    const uint32_t k = uint32_t(e >> 32);
-    hist_add(hist, k & ((1u << kRadixShift1) - 1u), v && (k >> kRadixShift1) == p1);
-  });
-  __syncthreads();
-  block_pick_digit<1 << kRadixShift1>(hist, krem1, &sh_digit, &sh_above, scan_sh);
-  const uint32_t tau = (p1 << kRadixShift1) | sh_digit;
-  const uint32_t take_eq = krem1 - sh_above;
-  // keys above tau and equal to it, per chunk
-  walk([&](int cc, bool v, unsigned long long e) {
-    const uint32_t k = uint32_t(e >> 32);
-    const uint32_t ng = __popc(__ballot_sync(kFull, v && k > tau));
-    const uint32_t nq = __popc(__ballot_sync(kFull, v && k == tau));
-    if (lane == 0) {  // chunks are walked by one warp each: plain adds
-      gt_c[cc] += ng;
-      eq_c[cc] += nq;
-    }
-  });
-  __syncthreads();
-  if (warp == 0) {  // exclusive offsets over the chunks (two per lane)
-    const uint32_t g0 = lane < C ? gt_c[lane] : 0u, g1 = lane + 32 < C ? gt_c[lane + 32] : 0u;
-    const uint32_t q0 = lane < C ? eq_c[lane] : 0u, q1 = lane + 32 < C ? eq_c[lane + 32] : 0u;
-    uint32_t ig0 = g0, ig1 = g1, iq0 = q0, iq1 = q1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t a0 = __shfl_up_sync(kFull, ig0, o), a1 = __shfl_up_sync(kFull, ig1, o);
-      const uint32_t b0 = __shfl_up_sync(kFull, iq0, o), b1 = __shfl_up_sync(kFull, iq1, o);
-      if (lane >= o) ig0 += a0, ig1 += a1, iq0 += b0, iq1 += b1;
-    }
-    const uint32_t tg = __shfl_sync(kFull, ig0, 31), tq = __shfl_sync(kFull, iq0, 31);
-    __syncwarp();
-    if (lane < C) gt_c[lane] = ig0 - g0, eq_c[lane] = iq0 - q0;
-    if (lane + 32 < C) gt_c[lane + 32] = tg + ig1 - g1, eq_c[lane + 32] = tq + iq1 - q1;
+  } else if (!multi && tid == 0) {
+    sh_gb = 0;
+    sh_qb = 0;
   }
   __syncthreads();
-  // ordered output: entry goes to slot (keys above tau before it) +
-  // min(keys equal to tau before it, take_eq) -- the keys above tau, then the
-  // lowest-positioned take_eq keys equal to it, all in position order
-  int32_t* out_idx = a.idx + size_t(s.per_seq ? s.b * a.H_kv : s.unit) * a.k;
-  const int n_rows = s.per_seq ? a.H_kv : 1;
-  int cur = -1;
-  uint32_t gb = 0, qb = 0;
-  walk([&](int cc, bool v, unsigned long long e) {
-    if (cc != cur) {
-      cur = cc;
-      gb = gt_c[cc];
-      qb = eq_c[cc];
-    }
-    const uint32_t k = uint32_t(e >> 32);
-    const int pos = int(uint32_t(e));
-    const unsigned bg = __ballot_sync(kFull, v && k > tau);
-    const unsigned bq = __ballot_sync(kFull, v && k == tau);
+  uint32_t gb = sh_gb + uint32_t(w_ex >> 32), qb = sh_qb + uint32_t(w_ex);
+  for (int base = s0; base < s1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < s1 ? keys[i] : 0u;
+    const unsigned bg = __ballot_sync(kFull, i < s1 && key > tau);
+    const unsigned bq = __ballot_sync(kFull, i < s1 && key == tau);
     const uint32_t g_at = gb + __popc(bg & lt), q_at = qb + __popc(bq & lt);
-    // slots stay below keff for consistent counts; the bound only guards the
-    // output row against an inconsistent list
+    const int pos = s.p0 + i;
+    // slots stay below keff for consistent counts; the bound only guards
+    // the output row against inconsistent counts (a wait that gave up)
     if ((bg >> lane) & 1u) {
       const uint32_t slot = g_at + min(q_at, take_eq);
       if (slot < uint32_t(s.keff))
@@ -608,14 +727,7 @@ __global__ void __launch_bounds__(kSelT) sel_list_kernel(const SelectArgs a) {
     }
     gb += __popc(bg);
     qb += __popc(bq);
-  });
-  __syncthreads();
-  // leave the histograms and the counter at zero for the next launch
-  for (int i = tid; i < kRadixBins; i += kSelT) {
-    gh[i] = 0u;
-    gh2[i] = 0u;
   }
-  if (tid == 0) a.sel_done[s.u] = 0u;
 }
 
 cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st) {
@@ -636,19 +748,9 @@ cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Chunks per unit: about two CTAs per SM over all selecting units, chunks of
-// at least kSelMinChunk positions, at most kSelMaxChunks.
-int select_chunks(int units, int max_len) {
-  const int sms = device_sm_count();
-  int C = (2 * sms + units - 1) / units;
-  C = min(C, kSelMaxChunks);
-  C = min(C, max(1, (max_len + kSelMinChunk - 1) / kSelMinChunk));
-  return max(C, 1);
-}
-
 template <typename K>
 cudaError_t launch_dependent(K kernel, dim3 grid, int threads, cudaStream_t st,
-                             const SelectArgs& a, size_t smem = 0) {
+                             const SelectArgs& a, size_t smem) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
@@ -662,24 +764,52 @@ cudaError_t launch_dependent(K kernel, dim3 grid, int threads, cudaStream_t st,
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// Selector CTAs resident per SM with the largest key buffer (per device).
 template <int EV_G>
-cudaError_t launch_select_t(const SelectArgs& a, cudaStream_t st) {
-  int n_active = 0;
-  for (int b = 0; b < a.B; ++b) n_active += int((a.active.bits[b >> 5] >> (b & 31)) & 1u);
-  const bool one_unit =
-      a.mode == SFI_SELECT_LOGIT_SUM_SEQ || (a.mode == SFI_SELECT_FUSED && a.g_only >= 0);
-  const int units = n_active * (one_unit ? 1 : a.H_kv);
-  if (units == 0) return cudaSuccess;
-  const dim3 grid(select_chunks(units, a.max_len), units);
-  cudaError_t e = cudaSuccess;
-  if (a.mode == SFI_SELECT_FUSED) e = launch_dependent(sel_nu_kernel, grid, kSelNuT, st, a);
-  if (e == cudaSuccess) e = launch_dependent(sel_score_kernel<EV_G>, grid, kSelT, st, a);
-  if (e == cudaSuccess) {
-    const size_t smem = size_t(kListCap) * sizeof(unsigned long long);
-    e = cudaFuncSetAttribute(sel_list_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e == cudaSuccess) e = launch_dependent(sel_list_kernel, grid, kSelT, st, a, smem);
+int sel_blocks_per_sm() {
+  static std::atomic<int> cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  int n = cached[dev].load();
+  if (n == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sel_kernel<EV_G>, kSelT, kSelSmemMax) !=
+            cudaSuccess || n < 1)
+      n = 1;
+    cached[dev].store(n);
   }
-  return e;
+  return n;
+}
+
+// Chunks per unit: as many as keep every CTA of the launch resident at once
+// (the chunks of a unit wait for one another), chunks of at least
+// kSelMinChunk positions, at most kSelMaxChunks; one chunk per unit when the
+// units alone fill the GPU.  Shared memory: the chunk's keys and key norms
+// (the norms' space then holds the unit's candidates) when they fit, else
+// the candidates alone.
+template <int EV_G>
+cudaError_t launch_select_t(const SelectArgs& a0, cudaStream_t st) {
+  int n_active = 0;
+  for (int b = 0; b < a0.B; ++b) n_active += int((a0.active.bits[b >> 5] >> (b & 31)) & 1u);
+  const bool one_unit =
+      a0.mode == SFI_SELECT_LOGIT_SUM_SEQ || (a0.mode == SFI_SELECT_FUSED && a0.g_only >= 0);
+  const int units = n_active * (one_unit ? 1 : a0.H_kv);
+  if (units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(sel_kernel<EV_G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSelSmemMax);
+  if (e != cudaSuccess) return e;
+  const int resident = sel_blocks_per_sm<EV_G>() * device_sm_count();
+  int C = units <= kSelCandRows ? min(kSelMaxChunks, resident / units) : 1;
+  C = min(C, (a0.max_len + kSelMinChunk - 1) / kSelMinChunk);
+  C = max(C, 1);
+  const int ch = ((a0.max_len + C - 1) / C + 3) & ~3;
+  const size_t key_b = size_t(ch) * sizeof(uint32_t);
+  const size_t cand_b = C > 1 ? size_t(kSelCandCap) * sizeof(unsigned long long) : 0;
+  const size_t both = key_b + std::max(key_b, cand_b);
+  SelectArgs a = a0;
+  a.keys_smem = both <= size_t(kSelSmemMax) ? 1 : 0;
+  a.smem_split = a.keys_smem ? ch : 0;
+  a.wait_cycles = wait_limit_cycles();
+  return launch_dependent(sel_kernel<EV_G>, dim3(C, units), kSelT, st, a, a.keys_smem ? both : cand_b);
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {

@@ -81,6 +81,9 @@ struct FpassArgs {
 
 constexpr int kSelectMaxLen = 327680;  // positions per row a selection takes (documented limit)
 constexpr int kSelMaxChunks = 64;      // chunk CTAs per selecting unit, at most
+constexpr int kSelHistWords = 3 * 2048;  // a unit's three radix histograms
+constexpr int kSelCandCap = 8192;        // candidates (keys of the k-th key's top bin) gathered, at most
+constexpr int kSelCandRows = 256;        // units of a launch that split into chunks, at most
 
 struct SelectArgs {
   const float* evidence;  // f (fused mode) or per-KV-head logit sums (logit-sum mode)
@@ -99,13 +102,15 @@ struct SelectArgs {
   SeqMask active;
   uint32_t* status;
   // selector scratch (workspace), rows indexed like the per-position arrays
-  float* sel_nu;                 // [B*H_kv][kSelMaxChunks] chunk sums of key norms over E
-  uint32_t* sel_cnt;             // [B*H_kv][kSelMaxChunks] list entries per chunk
-  uint32_t* sel_hist;            // [B*H_kv][2048] top-digit histogram, zero between launches
-  uint32_t* sel_hist2;           // [B*H_kv][2048] next-digit histogram of the k-th key's top bin
-  uint32_t* sel_done;            // [B*H_kv] chunk CTAs finished, zero between launches
-  uint32_t* sel_keys;            // [B*H_kv][max_len] order keys of the ranked scores
-  unsigned long long* sel_list;  // [B*H_kv][max_len] (key << 32 | position) entries
+  float* sel_nu;        // [B*H_kv][kSelMaxChunks] chunk sums of key norms over E
+  uint32_t* sel_cnt;    // [B*H_kv][kSelMaxChunks][2] keys above / equal to the k-th per chunk
+  uint32_t* sel_hist;   // [B*H_kv][kSelHistWords] the three digit histograms, zero between launches
+  uint32_t* sel_ctr;    // [B*H_kv][4] barrier counter ([0]; rests with its low 31 bits at zero)
+  uint32_t* sel_keys;   // [B*H_kv][max_len] order keys that do not fit in shared memory
+  unsigned long long* sel_cand;  // [kSelCandRows][max_len] (key << 32 | position) per selecting unit
+  int32_t keys_smem;    // set by the launcher: the keys stay in shared memory
+  int32_t smem_split;   // set by the launcher: words of shared memory before the candidates
+  long long wait_cycles;  // set by the launcher: limit of each barrier wait, in SM clocks
   // Cross-head exclusivity (fused mode): the ranked score of position i is
   // s_i * exp(-excl_beta * excl[b][i]) when excl is set ([B][max_len] counts).
   const uint8_t* excl;
@@ -129,8 +134,7 @@ int verify_stage_rows();
 // Workspace plan: one layout serves every call of a given geometry.
 struct WsPlan {
   size_t status_off, counters_off, partials_off, logits_off, stats_off, s_off;
-  size_t sel_nu_off, sel_cnt_off, sel_hist_off, sel_hist2_off, sel_done_off, sel_keys_off,
-      sel_list_off;
+  size_t sel_nu_off, sel_cnt_off, sel_hist_off, sel_ctr_off, sel_keys_off, sel_cand_off;
   size_t total;
   int32_t max_items;
 };

@@ -298,9 +298,10 @@ def test_cfg1_decode_loop_64_steps(sfi, cfg1_layer):
 
 
 def test_select_top_bin_over_candidate_cap(sfi):
-    """More than 4096 keys of E share the k-th key's top radix digit (the top 11
-    bits of the fp32 order key), so the selector finishes the lower digits
-    with passes over every CTA's keys instead of a gathered candidate list.
+    """More than 8192 keys of E (the candidate list's capacity) share the k-th
+    key's top radix digit (the top 11 bits of the fp32 order key), so the
+    selector finishes the lower digits with histogram passes over every CTA's
+    keys instead of the gathered candidate list.
     KV head 0: 12000 distinct-or-tied scores in one narrow band; KV head 1:
     every score equal (the set is the lowest k positions of E)."""
     ns, win, k = 4, 256, 6000
@@ -328,16 +329,63 @@ def test_select_top_bin_over_candidate_cap(sfi):
     f64, kn64 = f[0, :, :n].astype(np.float64), kn[0, :, :n].astype(np.float64)
     s_ref = O.fuse(f64, O.prior_r(kn64, lo, hi), wl.lam)
     assert max_abs(s_gpu[0, :, :n], s_ref) <= S_TOL
-    # the premise: the k-th key's top digit holds more than 4096 keys of E
+    # the premise: the k-th key's top digit holds more than 8192 keys of E
     for g in range(2):
         keys = s_gpu[0, g, lo:hi].astype(np.float32).view(np.uint32)
         keys = np.where(keys & 0x80000000, ~keys, keys | 0x80000000) >> 21
         kth = np.sort(keys)[::-1][k - 1]
-        assert int(np.sum(keys == kth)) > 4096
+        assert int(np.sum(keys == kth)) > 8192
         sel = idx[0, g, :cnt[0, g]]
         check_selection(sel, s_ref[g], lo, hi, k)
         assert np.array_equal(sel, O.top_k(s_gpu[0, g].astype(np.float64), lo, hi, k))
     assert np.array_equal(idx[0, 1, :k], np.arange(lo, lo + k))
+
+
+def test_select_ties_across_chunks_within_candidate_cap(sfi):
+    """The k-th key's top digit holds most of E but fewer than 8192 keys, and
+    E spans several chunk CTAs: the gathered candidate list decides the lower
+    digits, and the keys equal to the k-th one that are kept are the lowest-
+    positioned ones across chunk boundaries.  KV head 0: 7900 scores in one
+    narrow band with about four keys per value; KV head 1: every score equal
+    (the set is the lowest k positions of E)."""
+    ns, win, k = 4, 256, 3000
+    n = ns + 7900 + win
+    wl = W.small(1, 8, 2, 64, "f32", [n], 23, n_sink=ns, window=win, k=k)
+    dl = DeviceLayer.build(wl)
+    lay = dl.layout(sfi, [n])
+    ws = sfi.alloc_workspace(lay)
+    rng = np.random.default_rng(23)
+    f = np.zeros((1, 2, lay.max_len), np.float32)
+    u = np.floor(rng.random(n) * 2000.0) / 2000.0
+    f[0, 0, :n] = (1e-4 * (1.0 + 0.1 * u)).astype(np.float32)
+    f[0, 1, :n] = np.float32(1.0 / n)
+    kn = np.zeros_like(f)
+    kn[0, :, :n] = np.float32(2.0)
+    prm = sfi.params(ns, win, k, wl.lam)
+    idx = torch.full((1, 2, k), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.full((1, 2), -1, dtype=torch.int32, device="cuda")
+    s_out = torch.full((1, 2, lay.max_len), -7.0, device="cuda")
+    for rep in range(2):  # the second call finds the counters the first one left
+        sfi.sfi_select(lay, prm, torch.from_numpy(f).cuda(), torch.from_numpy(kn).cuda(), idx, cnt, s_out, ws)
+        torch.cuda.synchronize()
+        assert sfi.sfi_read_status(ws) == 0
+        idx_h, cnt_h, s_gpu = idx.cpu().numpy(), cnt.cpu().numpy(), s_out.cpu().numpy()
+        lo, hi = O.eligible_range(n, ns, win)
+        f64, kn64 = f[0, :, :n].astype(np.float64), kn[0, :, :n].astype(np.float64)
+        s_ref = O.fuse(f64, O.prior_r(kn64, lo, hi), wl.lam)
+        assert max_abs(s_gpu[0, :, :n], s_ref) <= S_TOL
+        for g in range(2):
+            keys = s_gpu[0, g, lo:hi].astype(np.float32).view(np.uint32)
+            keys = np.where(keys & 0x80000000, ~keys, keys | 0x80000000)
+            kth = np.sort(keys)[::-1][k - 1]
+            in_bin = int(np.sum((keys >> 21) == (kth >> 21)))
+            assert k < in_bin <= 8192  # the premise
+            # ties at the k-th key straddle positions beyond one chunk
+            assert int(np.sum(keys == kth)) > 1
+            sel = idx_h[0, g, :cnt_h[0, g]]
+            check_selection(sel, s_ref[g], lo, hi, k)
+            assert np.array_equal(sel, O.top_k(s_gpu[0, g].astype(np.float64), lo, hi, k))
+        assert np.array_equal(idx_h[0, 1, :k], np.arange(lo, lo + k))
 
 
 def test_fast_only_launch_short_units(sfi):
