@@ -870,8 +870,61 @@ def run_ragged_sweep(args):
             ms = statistics.median(times)
             points.append({"k": k, "window": win, "ms": round(ms, 4), "alg_bytes": nbytes,
                            "GB/s": round(nbytes / ms / 1e6, 1)})
-    return {"ragged_sweep": points, "sequences": sh.batch, "slow": sorted(slow_set),
-            "contexts": lens, "kv_gb": round(sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9, 2)}
+    out = {"ragged_sweep": points, "sequences": sh.batch, "slow": sorted(slow_set),
+           "contexts": lens, "kv_gb": round(sum(t.numel() * t.element_size() for t in R.K + R.V) / 1e9, 2)}
+    del R
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        out["cpu_oracle"] = ragged_cpu_oracle(base, slow_set, lens)
+    return out
+
+
+def ragged_cpu_oracle(base, slow_set, lens, k: int = 4096, win: int = 256):
+    """The fp64 oracle on sampled sequences of the ragged batch, one core: the
+    slow step of the two longest slow sequences and the fast step of a short
+    and the longest fast one (over the oracle's own selection at n - 1), each
+    sequence's seeded bf16 bytes generated first; seconds per KV byte of each
+    kind, scaled to the mixed step's slow and fast bytes at (k, window)."""
+    from oracle import sfi_oracle as O
+    sh = base.shape
+    row = 2 * sh.n_kv_heads * sh.head_dim * sh.esize
+    slow = sorted(slow_set, key=lambda b: lens[b])[-2:]
+    fast_all = sorted((b for b in range(sh.batch) if b not in slow_set), key=lambda b: lens[b])
+    fast = [fast_all[0], fast_all[-1]]
+    t_slow = b_slow = t_fast = b_fast = 0.0
+    for b in slow + fast:
+        n = lens[b]
+        K64 = W.storage_to_f64(base.kv_storage("k", 0, b), "bf16")
+        V64 = W.storage_to_f64(base.kv_storage("v", 0, b), "bf16")
+        q0 = W.storage_to_f64(base.q_storage(0, 0, b), "bf16")
+        q1 = W.storage_to_f64(base.q_storage(0, 1, b), "bf16")
+        if b in slow_set:
+            c0 = time.perf_counter()
+            O.slow_step(q1, K64, V64, n, base.n_sink, win, k, base.lam)
+            t_slow += time.perf_counter() - c0
+            b_slow += n * row
+        else:
+            st = O.slow_step(q0, K64, V64, n - 1, base.n_sink, win, k, base.lam)
+            c0 = time.perf_counter()
+            O.fast_step(q1, K64, V64, n, st["idx"], base.n_sink, win)
+            t_fast += time.perf_counter() - c0
+            e = max(0, (n - 1) - win - base.n_sink)
+            b_fast += (min(base.n_sink, n) + min(k, e) + (n - max(base.n_sink, n - win))) * row
+        del K64, V64
+    step_slow = sum(lens[b] * row for b in slow_set)
+    step_fast = 0
+    for b in range(sh.batch):
+        if b not in slow_set:
+            n = lens[b]
+            e = max(0, (n - 1) - win - base.n_sink)
+            step_fast += (min(base.n_sink, n) + min(k, e) + (n - max(base.n_sink, n - win))) * row
+    step_s = t_slow / b_slow * step_slow + t_fast / b_fast * step_fast
+    return {"mixed_steps_per_s_1core": round(1.0 / step_s, 6), "step_s_1core": round(step_s, 2),
+            "k": k, "window": win, "cores": 1, "cpu_model": cpu_model(),
+            "sample": f"slow steps of sequences {slow} (n = {[lens[b] for b in slow]}) and fast steps of "
+                      f"sequences {fast} (n = {[lens[b] for b in fast]}), all 8 KV heads each, timed "
+                      f"whole; seconds per KV byte of each kind scaled to the mixed step's "
+                      f"{step_slow / 1e9:.2f} GB slow and {step_fast / 1e9:.3f} GB fast"}
 
 
 def run_config_table(args):

@@ -153,7 +153,7 @@ __device__ __forceinline__ T block_excl_scan(T v, T* sh, T& total) {
 // above its range, and the one thread whose range holds the krem-th key
 // walks its bins.  0 < krem <= the histogram's total.  Ends with a barrier.
 template <int NB>
-__device__ void block_pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_digit,
+__device__ __noinline__ void block_pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_digit,
                                  uint32_t* out_above, uint32_t* scan_sh) {
   constexpr int PER = NB / kSelT;
   static_assert(PER * kSelT == NB, "bins split evenly over the block");
@@ -478,18 +478,21 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
     } else {
       __syncthreads();  // the key norms kept in shared memory
     }
-    for (int base = s.p0; base < s.p1; base += kSelT * kSelU) {
-      float kv[kSelU];
-      uint32_t cx[kSelU];
+    // (fewer positions at a time than the global passes: the norms come from
+    // shared memory or L2, and a shorter loop body keeps the code small)
+    constexpr int U2 = 4;
+    for (int base = s.p0; base < s.p1; base += kSelT * U2) {
+      float kv[U2];
+      uint32_t cx[U2];
 #pragma unroll
-      for (int j = 0; j < kSelU; ++j) {
+      for (int j = 0; j < U2; ++j) {
         const int i = base + j * kSelT + tid;
         const bool e = i < s.p1 && i >= lo && i < hi;
         kv[j] = e ? (nu_s ? nu_s[i - s.p0] : kn[i]) : 0.f;
         cx[j] = exrow && e ? exrow[i] : 0u;
       }
 #pragma unroll
-      for (int j = 0; j < kSelU; ++j) {
+      for (int j = 0; j < U2; ++j) {
         const int i = base + j * kSelT + tid;
         const bool in = i < s.p1;
         emit(i, in, in ? __uint_as_float(keys[i - s.p0]) : 0.f, kv[j], cx[j], coef);
