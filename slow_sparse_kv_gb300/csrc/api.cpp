@@ -171,27 +171,30 @@ namespace {
 // Length of a launch, in stage times of a CTA streaming at its fair share of
 // HBM, when `grid` CTAs take items in order: n_a units of rows_a rows split
 // into ceil(rows_a / rpi_a) items each, then n_b units of rows_b rows split
-// by rpi_b.  List scheduling with a min-heap of the CTAs' free times; each
-// item costs its stages plus kItemCost (its start, epilogue and share of the
-// merge of split units).  Once the last item is taken, the CTAs still busy
+// by rpi_b.  List scheduling over the CTAs' free times; each item costs its
+// stages (a class-a stage weighted w_a / 10) plus kItemCost (its start,
+// epilogue and share of the merge of split units).  Once the last item is taken, the CTAs still busy
 // share HBM among fewer streams and speed up to at most `cap` times their
 // fair share: their own pipeline bounds them (measured: ~1.5 for plain
 // attention, ~1.0 when slow units also write their logits and key norms,
 // which holds each stage longer).
 double simulate_launch(long long n_a, int rows_a, long long rpi_a, long long n_b, int rows_b,
-                       long long rpi_b, int sr, int grid, double cap) {
-  constexpr long long kItemCost = 3;
-  // Item costs are whole stage counts, so the CTAs' free times are integers:
-  // free[t] counts the CTAs free at time t, and the earliest free time only
-  // grows as items are handed out.
+                       long long rpi_b, int sr, int grid, double cap, int w_a) {
+  // times in tenths of a plain stage: a stage of class b costs 10, one of
+  // class a w_a, an item's fixed cost 3 stages
+  constexpr long long kItemCost = 30;
+  const long long w[2] = {w_a, 10};
+  // Item costs are integers, so the CTAs' free times are integers: free[t]
+  // counts the CTAs free at time t, and the earliest free time only grows as
+  // items are handed out.
   long long horizon = 1;
   for (int cls = 0; cls < 2; ++cls) {
     const long long n = cls == 0 ? n_a : n_b;
     const int rows = cls == 0 ? rows_a : rows_b;
     const long long rpi = cls == 0 ? rpi_a : rpi_b;
-    if (n > 0 && rows > 0) horizon += n * (ceil_div(rows, sr) + ceil_div(rows, rpi) * kItemCost);
+    if (n > 0 && rows > 0) horizon += n * (ceil_div(rows, sr) * w[cls] + ceil_div(rows, rpi) * kItemCost);
   }
-  horizon = horizon / grid + 2 * (ceil_div(std::max(rows_a, rows_b), sr) + kItemCost) + 2;
+  horizon = horizon / grid + 2 * (ceil_div(std::max(rows_a, rows_b), sr) * std::max(w[0], w[1]) + kItemCost) + 2;
   std::vector<int> free_at(size_t(horizon), 0);
   free_at[0] = grid;
   long long t_min = 0;
@@ -208,7 +211,7 @@ double simulate_launch(long long n_a, int rows_a, long long rpi_a, long long n_b
       for (long long i = 0; i < k; ++i) {
         while (free_at[size_t(t_min)] == 0) ++t_min;
         --free_at[size_t(t_min)];
-        ++free_at[size_t(t_min + q + (i < r ? 1 : 0) + kItemCost)];
+        ++free_at[size_t(t_min + (q + (i < r ? 1 : 0)) * w[cls] + kItemCost)];
       }
   }
   // the tail: remaining work of every CTA after the last item was taken at
@@ -224,7 +227,7 @@ double simulate_launch(long long n_a, int rows_a, long long rpi_a, long long n_b
       }
       --active;
     }
-  return t;
+  return t / 10.0;
 }
 
 struct SplitKey {
@@ -263,6 +266,9 @@ ItemSplit choose_item_split(long long n_a, int rows_a, long long n_b, int rows_b
   if (n_b <= 0 || rows_b <= 0) n_b = 0, rows_b = 0;
   const SplitKey key{n_a, n_b, rows_a, rows_b, sr, grid, emit};
   const double cap = emit ? 1.0 : 1.5;
+  // a stage of a unit that also writes its logits and key norms holds the
+  // CTA ~1.5x as long as a plain one (measured per-stage warp times)
+  const int w_a = emit ? 15 : 10;
   static std::mutex mu;
   static std::vector<std::pair<SplitKey, ItemSplit>> cache;
   {
@@ -290,7 +296,7 @@ ItemSplit choose_item_split(long long n_a, int rows_a, long long n_b, int rows_b
   for (long long ra : ca)
     for (long long rb : cb) {
       if (can_fill && items_of(ra, rb) < grid) continue;
-      const double cost = simulate_launch(n_a, rows_a, ra, n_b, rows_b, rb, sr, grid, cap);
+      const double cost = simulate_launch(n_a, rows_a, ra, n_b, rows_b, rb, sr, grid, cap, w_a);
       if (cost < best_cost) {
         best_cost = cost;
         best = ItemSplit{int(ra), int(rb)};
