@@ -27,6 +27,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -39,6 +40,7 @@ constexpr int kRadixBins = 2048;
 constexpr int kRadixShift0 = 21;  // digits: bits 31..21, 20..10, 9..0 of the order key
 constexpr int kRadixShift1 = 10;
 constexpr int kSelMinChunk = 2048;     // positions per chunk, at least
+constexpr int kWalk = 8;               // keys per lane in flight in the walks over global keys
 constexpr int kSelSmemMax = 100 << 10;  // dynamic shared memory of a selector CTA, at most
 
 // The G logits of one position ([pos][G] rows are 4*G-byte aligned).
@@ -530,19 +532,33 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
     if (tid == 0) sh_nc = 0;
     __syncthreads();
     uint32_t above = 0;
-    for (int b0 = e0; b0 < e1; b0 += kSelT) {
-      const int i = b0 + tid;
-      const uint32_t key = i < e1 ? keys[i] : 0u;
-      const uint32_t dg = key >> kRadixShift0;
-      above += (i < e1 && dg > d0) ? 1u : 0u;
-      const unsigned m = __ballot_sync(kFull, i < e1 && dg == d0);
-      // slots in the chunk's region in any order: only counts and
-      // histograms are taken over the candidates
-      uint32_t at = 0;
-      if (lane == 0 && m) at = atomicAdd(&sh_nc, uint32_t(__popc(m)));
-      at = __shfl_sync(kFull, at, 0) + __popc(m & lt);
-      if ((m >> lane) & 1u) row[s.e0 + at] = (static_cast<unsigned long long>(key) << 32) | uint32_t(s.p0 + i);
-    }
+    auto append_walk = [&](auto kw) {
+      constexpr int KW = decltype(kw)::value;
+      for (int b0 = e0; b0 < e1; b0 += kSelT * KW) {
+        uint32_t kk[KW];
+#pragma unroll
+        for (int r = 0; r < KW; ++r) {
+          const int i = b0 + kSelT * r + tid;
+          kk[r] = i < e1 ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int r = 0; r < KW; ++r) {
+          const int i = b0 + kSelT * r + tid;
+          const uint32_t dg = kk[r] >> kRadixShift0;
+          above += (i < e1 && dg > d0) ? 1u : 0u;
+          const unsigned m = __ballot_sync(kFull, i < e1 && dg == d0);
+          // slots in the chunk's region in any order: only counts and
+          // histograms are taken over the candidates
+          uint32_t at = 0;
+          if (lane == 0 && m) at = atomicAdd(&sh_nc, uint32_t(__popc(m)));
+          at = __shfl_sync(kFull, at, 0) + __popc(m & lt);
+          if ((m >> lane) & 1u)
+            row[s.e0 + at] = (static_cast<unsigned long long>(kk[r]) << 32) | uint32_t(s.p0 + i);
+        }
+      }
+    };
+    if (a.keys_smem) append_walk(std::integral_constant<int, 1>{});
+    else append_walk(std::integral_constant<int, kWalk>{});
     above = block_count(above, scan_sh);
     if (tid == 0) {
       cnt[2 * c] = above;
@@ -673,12 +689,27 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
   const int seg = ((len + NW - 1) / NW + 31) / 32 * 32;
   const int s0 = min(e1, e0 + warp * seg), s1 = min(e1, s0 + seg);
   uint32_t wg = 0, wq = 0;
-  for (int base = s0; base < s1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < s1 ? keys[i] : 0u;
-    wg += __popc(__ballot_sync(kFull, i < s1 && key > tau));
-    wq += __popc(__ballot_sync(kFull, i < s1 && key == tau));
-  }
+  // (in the walks, KW keys per lane are loaded before any is used: 8 when
+  // the keys are in global memory, 1 from shared memory)
+  auto count_walk = [&](auto kw) {
+    constexpr int KW = decltype(kw)::value;
+    for (int base = s0; base < s1; base += 32 * KW) {
+      uint32_t kk[KW];
+#pragma unroll
+      for (int r = 0; r < KW; ++r) {
+        const int i = base + 32 * r + lane;
+        kk[r] = i < s1 ? keys[i] : 0u;
+      }
+#pragma unroll
+      for (int r = 0; r < KW; ++r) {
+        const bool in = base + 32 * r + lane < s1;
+        wg += __popc(__ballot_sync(kFull, in && kk[r] > tau));
+        wq += __popc(__ballot_sync(kFull, in && kk[r] == tau));
+      }
+    }
+  };
+  if (a.keys_smem) count_walk(std::integral_constant<int, 1>{});
+  else count_walk(std::integral_constant<int, kWalk>{});
   unsigned long long tot;
   const unsigned long long ex = block_excl_scan<unsigned long long>(
       lane == 0 ? (static_cast<unsigned long long>(wg) << 32) | wq : 0ull, scan64, tot);
@@ -712,25 +743,38 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
   }
   __syncthreads();
   uint32_t gb = sh_gb + uint32_t(w_ex >> 32), qb = sh_qb + uint32_t(w_ex);
-  for (int base = s0; base < s1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < s1 ? keys[i] : 0u;
-    const unsigned bg = __ballot_sync(kFull, i < s1 && key > tau);
-    const unsigned bq = __ballot_sync(kFull, i < s1 && key == tau);
-    const uint32_t g_at = gb + __popc(bg & lt), q_at = qb + __popc(bq & lt);
-    const int pos = s.p0 + i;
-    // slots stay below keff for consistent counts; the bound only guards
-    // the output row against inconsistent counts (a wait that gave up)
-    if ((bg >> lane) & 1u) {
-      const uint32_t slot = g_at + min(q_at, take_eq);
-      if (slot < uint32_t(s.keff))
-        for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + slot] = pos;
-    } else if (((bq >> lane) & 1u) && q_at < take_eq && g_at + q_at < uint32_t(s.keff)) {
-      for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + g_at + q_at] = pos;
+  auto out_walk = [&](auto kw) {
+    constexpr int KW = decltype(kw)::value;
+    for (int base = s0; base < s1; base += 32 * KW) {
+      uint32_t kk[KW];
+#pragma unroll
+      for (int r = 0; r < KW; ++r) {
+        const int i = base + 32 * r + lane;
+        kk[r] = i < s1 ? keys[i] : 0u;
+      }
+#pragma unroll
+      for (int r = 0; r < KW; ++r) {
+        const int i = base + 32 * r + lane;
+        const unsigned bg = __ballot_sync(kFull, i < s1 && kk[r] > tau);
+        const unsigned bq = __ballot_sync(kFull, i < s1 && kk[r] == tau);
+        const uint32_t g_at = gb + __popc(bg & lt), q_at = qb + __popc(bq & lt);
+        const int pos = s.p0 + i;
+        // slots stay below keff for consistent counts; the bound only guards
+        // the output row against inconsistent counts (a wait that gave up)
+        if ((bg >> lane) & 1u) {
+          const uint32_t slot = g_at + min(q_at, take_eq);
+          if (slot < uint32_t(s.keff))
+            for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + slot] = pos;
+        } else if (((bq >> lane) & 1u) && q_at < take_eq && g_at + q_at < uint32_t(s.keff)) {
+          for (int g = 0; g < n_rows; ++g) out_idx[size_t(g) * a.k + g_at + q_at] = pos;
+        }
+        gb += __popc(bg);
+        qb += __popc(bq);
+      }
     }
-    gb += __popc(bg);
-    qb += __popc(bq);
-  }
+  };
+  if (a.keys_smem) out_walk(std::integral_constant<int, 1>{});
+  else out_walk(std::integral_constant<int, kWalk>{});
 }
 
 cudaError_t launch_fpass(const FpassArgs& a, cudaStream_t st) {
