@@ -153,7 +153,8 @@ __device__ __forceinline__ T block_excl_scan(T v, T* sh, T& total) {
 // counts the keys in higher bins), with the whole block: thread t sums
 // NB / kSelT consecutive bins from the top, a block scan gives the count
 // above its range, and the one thread whose range holds the krem-th key
-// walks its bins.  0 < krem <= the histogram's total.  Ends with a barrier.
+// walks its bins.  0 < krem <= the histogram's total (else digit 0).  Ends
+// with a barrier.
 template <int NB>
 __device__ __noinline__ void block_pick_digit(const uint32_t* hist, uint32_t krem, uint32_t* out_digit,
                                  uint32_t* out_above, uint32_t* scan_sh) {
@@ -166,6 +167,12 @@ __device__ __noinline__ void block_pick_digit(const uint32_t* hist, uint32_t kre
   for (int j = 0; j < PER; ++j) {
     c[j] = hist[top - j];
     sum += c[j];
+  }
+  // digit 0 unless a thread finds the krem-th key (a histogram left
+  // inconsistent by a barrier wait that gave up): the digit stays in range
+  if (threadIdx.x == 0) {
+    *out_digit = 0u;
+    *out_above = 0u;
   }
   uint32_t tot;
   const uint32_t excl = block_excl_scan(sum, scan_sh, tot);
@@ -590,8 +597,12 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
     __syncthreads();
     const uint32_t nc = min(c_off[kSelMaxChunks], uint32_t(kSelCandCap));
     for (int cc = warp; cc < C; cc += NW) {  // each warp whole chunks, 8 loads in flight per lane
-      const uint32_t o0 = c_off[cc], n = min(c_off[cc + 1], nc) - min(o0, nc);
-      const unsigned long long* src = row + sel_chunk_e0(s, cc);
+      // (the bounds hold the copy inside the staging area and the row even
+      // when a barrier wait gave up and the counts are inconsistent)
+      const int e0c = sel_chunk_e0(s, cc);
+      const uint32_t o0 = min(c_off[cc], nc), o1 = max(o0, min(c_off[cc + 1], nc));
+      const uint32_t n = min(o1 - o0, uint32_t(max(a.max_len - e0c, 0)));
+      const unsigned long long* src = row + e0c;
       for (uint32_t jb = 0; jb < n; jb += 32 * 8) {
         unsigned long long ent[8];
 #pragma unroll

@@ -1,4 +1,4 @@
-"""Failure detection on the GPU without a fault: a pipeline wait that runs out.
+"""Failure detection on the GPU without a fault: a pipeline or barrier wait that runs out.
 
 Every consumer wait of the attention kernel for a stage of cache rows has a
 limit (sfi_set_wait_limit; about 2 s by default).  Here the limit is set to a
@@ -58,3 +58,48 @@ def test_wait_runs_out_then_recovers(sfi):
     for b in range(2):
         exp = O.dense_attention(q64[b], dl.K64[b], dl.V64[b], lens[b])[0]
         assert max_abs(after[b].cpu().numpy(), exp) <= O_TOL["bf16"]
+
+
+def test_selector_barrier_wait_runs_out_then_recovers(sfi):
+    """The selector's chunk CTAs of a unit wait for one another at barriers
+    with the same limit.  One sequence x 8 KV heads at 40000 positions splits
+    every unit into 20 chunk CTAs; with a one-clock limit the waits give up:
+    SFI_DEV_WAIT_TIMEOUT is set, every access stays in bounds (the counts the
+    CTAs then read are inconsistent) and the launch returns.  After the
+    workspace is zero-filled again, the default limit reproduces the bytes of
+    a selection made before the timeout."""
+    lens = [40000]
+    wl = W.small(1, 32, 8, 128, "bf16", lens, seed=78, n_sink=4, window=256, k=512)
+    dl = DeviceLayer.build(wl)
+    lay = dl.layout(sfi, lens)
+    ws = sfi.alloc_workspace(lay)
+    qd, _ = dl.queries(0)
+    out = torch.empty(1, 32, 128, device="cuda")
+    f = torch.empty(1, 8, lay.max_len, device="cuda")
+    kn = torch.empty(1, 8, lay.max_len, device="cuda")
+    sfi.sfi_slow_attn(lay, qd, dl.k, dl.v, out, f, kn, ws)
+    prm = sfi.params(4, 256, 512, wl.lam)
+    idx0 = torch.full((1, 8, 512), -1, dtype=torch.int32, device="cuda")
+    cnt0 = torch.full((1, 8), -1, dtype=torch.int32, device="cuda")
+    sfi.sfi_select(lay, prm, f, kn, idx0, cnt0, None, ws)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws) == 0
+
+    assert sfi.lib.sfi_set_wait_limit(1) == sfi.SFI_OK
+    idx = torch.full_like(idx0, -1)
+    cnt = torch.full_like(cnt0, -1)
+    for _ in range(2):  # a second launch on the dirty workspace also returns
+        sfi.sfi_select(lay, prm, f, kn, idx, cnt, None, ws)
+        torch.cuda.synchronize()
+        st = sfi.sfi_read_status(ws)
+        assert st & sfi.SFI_DEV_WAIT_TIMEOUT, st
+
+    assert sfi.lib.sfi_set_wait_limit(0) == sfi.SFI_OK
+    ws.zero_()
+    idx.fill_(-1)
+    cnt.fill_(-1)
+    sfi.sfi_select(lay, prm, f, kn, idx, cnt, None, ws)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_status(ws) == 0
+    assert torch.equal(cnt, cnt0)
+    assert torch.equal(idx, idx0)
