@@ -82,14 +82,14 @@ def schedule_counts(slow_masks: np.ndarray):
 # DRAM traffic of the attention kernel relative to its algorithmic bytes,
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # decode driver's mixed launch: batch 8 at context 131072, sequence 0
-# refreshing and seven fast -- 662.85 MB read + 7.34 MB written for
+# refreshing and seven fast -- 662.88 MB read + 6.96 MB written for
 # 661.77 MB algorithmic.  It holds for the kernel code it was taken on (the
 # SHA-256 of the sources below with comments and whitespace removed); after
 # any change to that code the roofline reports null traffic until the
 # capture is repeated.
-ATTN_TRAFFIC = {"ratio": (662854144 + 7339008) / 661766144,
+ATTN_TRAFFIC = {"ratio": (662879744 + 6963712) / 661766144,
                 "sources": ["attn_kernel.cuh", "attn_bf16.cu", "common.cuh"],
-                "sha256": "d5583f800971a357b6814e82037113b4aa90485488f0e9b504fdd90a239eccee"}
+                "sha256": "a58821b3dd1b7dfef030cdb40765773a44e8e0c653e0972f2501a41ed6b26a86"}
 
 
 def attn_code_hash() -> str:

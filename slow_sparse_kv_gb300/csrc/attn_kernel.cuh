@@ -124,8 +124,8 @@ struct ItemRing {
 };
 
 // Fetch the next item id for this CTA and publish it (first producer warp).
-// The CTA's first id was fetched at kernel start (first_id, lane 0), while
-// the unit table was being built.
+// A CTA's first item is its own index (no round trip before its first rows
+// are requested); later ones come from the work counter, past the grid.
 __device__ __forceinline__ int ring_fetch_publish(const AttnArgs& a, int total, const ItemRing& r,
                                                   uint32_t seq, volatile int* abort_flag,
                                                   int lane, unsigned first_id) {
@@ -134,7 +134,7 @@ __device__ __forceinline__ int ring_fetch_publish(const AttnArgs& a, int total, 
   // after an abort the CTA takes no further items (the work counters are
   // then left mid-count: the caller zero-fills the workspace again)
   if (lane == 0 && !(seq > 0 && *abort_flag)) {
-    const unsigned x = seq == 0 ? first_id : atomicAdd(a.work_ctr, 1u);
+    const unsigned x = seq == 0 ? first_id : gridDim.x + atomicAdd(a.work_ctr, 1u);
     if (x < unsigned(total)) {
       it = int(x);
     } else {
@@ -940,11 +940,9 @@ __global__ void __launch_bounds__(AttnCfg<T, D, G>::NT, 1)
   const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
   const uint32_t bar_empty = bar_full + C::NS * 8;
 
-  // the first producer warp's lane 0 takes the CTA's first item id now; the
-  // atomic's round trip overlaps the unit table's loads
-  unsigned first_id = 0;
+  // the CTA's first item is its own index (later ones from the work counter)
+  const unsigned first_id = blockIdx.x;
   const bool fetcher = warp == C::NCW && lane == 0;
-  if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
   if (a.len_copy && blockIdx.x == 0)
     for (int b = tid; b < a.B; b += C::NT) a.len_copy[b] = a.len[b];
   // A launch of fast units only, each cut into exactly fast_items items (the

@@ -335,10 +335,9 @@ __global__ void __launch_bounds__(VerifyCfg<D>::NT, 1)
   int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
   const uint32_t bar_full = smem_addr(smem + C::OFF_BAR);
   const uint32_t bar_empty = bar_full + C::NS * 8;
-  // the CTA's first item id, fetched while the unit table is built
-  unsigned first_id = 0;
+  // the CTA's first item is its own index (later ones from the work counter)
+  const unsigned first_id = blockIdx.x;
   const bool fetcher = warp == C::NCW && lane == 0;
-  if (fetcher) first_id = atomicAdd(a.work_ctr, 1u);
   const bool units_fit = attn_build_units<C::NT>(a, units, n_units, misc);  // fast_items is 0
   const int total = units[n_units];
   if (total > a.max_items || !units_fit) {
