@@ -577,8 +577,8 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
     if (warp == 0) {
       const uint32_t n0 = lane < C ? __ldcg(cnt + 2 * lane + 1) : 0u;
       const uint32_t n1 = lane + 32 < C ? __ldcg(cnt + 2 * (lane + 32) + 1) : 0u;
-      uint32_t g = 0;
-      for (int cc = lane; cc < c; cc += 32) g += __ldcg(cnt + 2 * cc);
+      const uint32_t a0 = lane < c ? __ldcg(cnt + 2 * lane) : 0u;
+      const uint32_t a1 = lane + 32 < c ? __ldcg(cnt + 2 * (lane + 32)) : 0u;
       uint32_t i0 = n0, i1 = n1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -589,6 +589,7 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
       c_off[lane] = i0 - n0;
       c_off[lane + 32] = t0 + i1 - n1;
       if (lane == 31) c_off[kSelMaxChunks] = t0 + i1;
+      uint32_t g = a0 + a1;
 #pragma unroll
       for (int o = 16; o; o >>= 1) g += __shfl_down_sync(kFull, g, o);
       if (lane == 0) sh_gb = g;  // keys above bin d0 in the lower chunks
@@ -596,27 +597,22 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
     for (int i = tid; i < kRadixBins; i += kSelT) hist[i] = 0;
     __syncthreads();
     const uint32_t nc = min(c_off[kSelMaxChunks], uint32_t(kSelCandCap));
-    for (int cc = warp; cc < C; cc += NW) {  // each warp whole chunks, 8 loads in flight per lane
-      // (the bounds hold the copy inside the staging area and the row even
-      // when a barrier wait gave up and the counts are inconsistent)
+    // every entry of every chunk copied straight into shared memory at once
+    // (asynchronous 8-byte copies; each warp walks whole chunks); the bounds
+    // hold the copy inside the staging area and the row even when a barrier
+    // wait gave up and the counts are inconsistent
+    for (int cc = warp; cc < C; cc += NW) {
       const int e0c = sel_chunk_e0(s, cc);
       const uint32_t o0 = min(c_off[cc], nc), o1 = max(o0, min(c_off[cc + 1], nc));
       const uint32_t n = min(o1 - o0, uint32_t(max(a.max_len - e0c, 0)));
       const unsigned long long* src = row + e0c;
-      for (uint32_t jb = 0; jb < n; jb += 32 * 8) {
-        unsigned long long ent[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const uint32_t jj = jb + uint32_t(r) * 32 + lane;
-          ent[r] = jj < n ? __ldcg(src + jj) : 0ull;
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const uint32_t jj = jb + uint32_t(r) * 32 + lane;
-          if (jj < n) cands[o0 + jj] = ent[r];
-        }
-      }
+      const uint32_t dst = smem_addr(cands + o0);
+      for (uint32_t jj = lane; jj < n; jj += 32)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst + 8u * jj), "l"(src + jj)
+                     : "memory");
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
     // ---- the two lower digits among the candidates
     for (uint32_t e = tid; e < nc; e += kSelT)
@@ -635,19 +631,18 @@ __global__ void __launch_bounds__(kSelT, 2) sel_kernel(const SelectArgs a) {
     block_pick_digit<1 << kRadixShift1>(hist, krem, &sh_digit, &sh_above, scan_sh);
     tau = (p1 << kRadixShift1) | sh_digit;
     take_eq = krem - sh_above;
-    // candidates of the lower chunks above / equal to tau
-    uint32_t g = 0, q = 0;
+    // candidates of the lower chunks above / equal to tau (both counts are
+    // below 2^16: one packed block sum)
+    uint32_t gq = 0;
     const uint32_t nlow = min(c_off[c], nc);
     for (uint32_t e = tid; e < nlow; e += kSelT) {
       const uint32_t key = uint32_t(cands[e] >> 32);
-      g += key > tau ? 1u : 0u;
-      q += key == tau ? 1u : 0u;
+      gq += key > tau ? 0x10000u : (key == tau ? 1u : 0u);
     }
-    g = block_count(g, scan_sh);
-    q = block_count(q, scan_sh);
+    gq = block_count(gq, scan_sh);
     if (tid == 0) {
-      sh_gb += g;
-      sh_qb = q;
+      sh_gb += gq >> 16;
+      sh_qb = gq & 0xffffu;
     }
   } else {
     // ---- the two lower digits by histogram rounds over all keys: each
