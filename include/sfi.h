@@ -124,10 +124,12 @@ int32_t sfi_device_sm_count(void);
 
 /* Failure detection (no counterpart on the pages): every attention and
  * verify launch gives each consumer warp's wait for a stage of cache rows a
- * limit in SM clocks.  A wait that runs out sets SFI_DEV_WAIT_TIMEOUT; its
- * CTA then skips the arithmetic of the stages it still holds, takes no
- * further work and returns (its output is not meaningful; zero-fill the
- * workspace before reusing it).  `cycles` applies to every later launch from
+ * limit in SM clocks, and every selector launch each wait of its chunk CTAs
+ * for one another.  A wait that runs out sets SFI_DEV_WAIT_TIMEOUT; an
+ * attention CTA then skips the arithmetic of the stages it still holds,
+ * takes no further work and returns, a selector CTA goes on without waiting
+ * (every access stays in bounds).  The call's output is then not
+ * meaningful; zero-fill the workspace before reusing it.  `cycles` applies to every later launch from
  * any thread of the process; 0 restores the default of 4e9 clocks (about 2 s).
  * SFI_ERR_INVALID_ARG for cycles < 0. */
 sfi_status sfi_set_wait_limit(int64_t cycles);
@@ -174,7 +176,12 @@ sfi_status sfi_slow_attn(const sfi_layout* layout, const void* q, const void* k,
  *   logit sum evidence[b][g][i] (same order and tie rule, its own set per KV
  *   head); knorm is unused, lambda and n_sink must be 0; s_out receives the
  *   ranked values.
- * idx_out: [B][H_kv][k] int32; count_out: [B][H_kv] int32 (device). */
+ * idx_out: [B][H_kv][k] int32; count_out: [B][H_kv] int32 (device).
+ * One launch; the CTAs that share a selecting unit wait for one another at
+ * up to five barriers, and the launch cuts units into several CTAs only when
+ * all its CTAs can be resident at once, so a concurrent launch on another
+ * stream can delay it but not block it (each wait has the limit of
+ * sfi_set_wait_limit). */
 size_t sfi_select_workspace_size(const sfi_layout* layout, const sfi_params* params);
 sfi_status sfi_select(const sfi_layout* layout, const sfi_params* params,
                       const float* evidence, const float* knorm,
