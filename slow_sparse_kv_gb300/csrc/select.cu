@@ -16,11 +16,13 @@
 // the per-sequence logit-sum mode -- is cut into C chunks of consecutive
 // positions, one CTA each, in one launch.  C is as large as keeps every CTA
 // of the launch resident at once, so that all SMs work on the few units of a
-// decode step; the C CTAs of a unit exchange the key-norm sum, three radix
-// histograms of the order keys (11 + 11 + 10 bits, integer atomics) and
-// their output counts through the workspace, and meet at up to five barriers
-// on a counter of the unit.  The keys stay in the CTA (shared memory) when
-// they fit.  Ties at the k-th key go to the lower positions exactly as the
+// decode step; the C CTAs of a unit exchange, through the workspace, the
+// key-norm sum, the histogram of the order keys' top 11 bits (integer
+// atomics) and the keys of the k-th key's top bin, from which every CTA
+// finds the lower 21 bits of the k-th key -- or, when that bin is crowded,
+// two more digit histograms (11 + 10 bits) and their output counts -- and
+// meet at three (up to five) barriers on a counter of the unit.  The keys
+// stay in the CTA (shared memory) when they fit.  Ties at the k-th key go to the lower positions exactly as the
 // definition says, and every sum runs in a fixed order, so the selection
 // does not depend on the schedule.
 #include <math.h>
